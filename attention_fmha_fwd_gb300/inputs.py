@@ -1,0 +1,90 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the smoke check.
+
+This module holds no attention arithmetic: it only draws numbers and names shapes.
+
+Recipe: one ``torch.Generator`` seeded with ``seed`` draws fp32 standard normals in the
+order q, k, v, each rounded to bf16 (round-to-nearest-even).  Variable-length sequence
+lengths come from a separate generator seeded the same way, drawn before q/k/v.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+
+def randn_bf16(gen: torch.Generator, shape) -> torch.Tensor:
+    """fp32 N(0, 1) from ``gen``, rounded to bf16 (CPU tensor)."""
+    return torch.randn(tuple(shape), dtype=torch.float32, generator=gen).to(torch.bfloat16)
+
+
+def qkv(B: int, M: int, Mkv: int, H: int, K: int, Kv: int | None = None,
+        Hkv: int | None = None, seed: int = 0):
+    """q [B,M,H,K], k [B,Mkv,Hkv,K], v [B,Mkv,Hkv,Kv] bf16 CPU tensors, drawn in that order."""
+    Kv = K if Kv is None else Kv
+    Hkv = H if Hkv is None else Hkv
+    g = torch.Generator().manual_seed(seed)
+    q = randn_bf16(g, (B, M, H, K))
+    k = randn_bf16(g, (B, Mkv, Hkv, K))
+    v = randn_bf16(g, (B, Mkv, Hkv, Kv))
+    return q, k, v
+
+
+def varlen_seqlens(n_seqs: int = 12, total: int = 16384, lo: int = 128, hi: int = 4096,
+                   seed: int = 0) -> list[int]:
+    """Sequence lengths for a packed batch: ``n_seqs`` integers uniform in [lo, hi],
+    rescaled proportionally to sum to ``total`` (each floored, at least 1; the
+    remainder goes to the last sequence)."""
+    g = torch.Generator().manual_seed(seed)
+    raw = torch.randint(lo, hi + 1, (n_seqs,), generator=g).tolist()
+    s = sum(raw)
+    lens = [max(1, (r * total) // s) for r in raw]
+    lens[-1] += total - sum(lens)
+    if lens[-1] < 1:
+        raise ValueError("cannot fit the lengths into the requested total")
+    return lens
+
+
+def cu_seqlens(lengths) -> list[int]:
+    """Cumulative offsets [0, L0, L0+L1, ...] of a packed batch."""
+    out = [0]
+    for n in lengths:
+        out.append(out[-1] + int(n))
+    return out
+
+
+def equal_chunks(Mkv: int, n: int) -> list[tuple[int, int]]:
+    """``n`` contiguous key ranges [start, end) covering [0, Mkv), as equal as possible."""
+    return [(c * Mkv // n, (c + 1) * Mkv // n) for c in range(n)]
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One named attention workload (shapes only)."""
+
+    name: str
+    B: int
+    M: int
+    Mkv: int
+    H: int
+    K: int
+    Kv: int
+    mask: str            # "none" | "causal" | "blockdiag_causal"
+    scale: float
+    chunks: tuple = ()   # split-KV chunk counts exercised (partial + merge)
+    n_seqs: int = 0      # packed sequences (block-diagonal masks)
+
+
+WORKLOADS = {
+    "tiny_fwd": Workload("tiny_fwd", 1, 128, 128, 2, 64, 64, "none", 0.125),
+    "causal_fwd": Workload("causal_fwd", 2, 2048, 2048, 32, 128, 128, "causal",
+                           1.0 / 128 ** 0.5),
+    "split_kv": Workload("split_kv", 1, 128, 1024, 16, 128, 128, "none", 1.0 / 128 ** 0.5,
+                         chunks=(2, 8)),
+    # K/V drawn as G=8 groups of 1 head each, flattened to 8 heads.
+    "decode_split_kv": Workload("decode_split_kv", 16, 1, 32768, 8, 128, 128, "none",
+                                1.0 / 128 ** 0.5, chunks=(16,)),
+    "varlen_packed": Workload("varlen_packed", 1, 16384, 16384, 32, 128, 128,
+                              "blockdiag_causal", 1.0 / 128 ** 0.5, n_seqs=12),
+}

@@ -1,0 +1,513 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Every ``pin_*`` function takes the oracle module as its argument and raises
+``AssertionError`` on a mismatch, so the same pins run against the real oracle
+(tests/test_oracle_pins.py) and against deliberately broken copies of it
+(tests/test_oracle_mutants.py, which shows each plausible mistake trips a pin).
+
+Sources of truth, none of them the oracle:
+  * a pure-Python brute force (loops, ``math.exp``), with the mask materialised element
+    by element from the pages' definitions (MSLK kernel reference, "Attention - Biases &
+    masks": ``LowerTriangularMask`` gives zeros on/below the diagonal and -inf above;
+    ``BlockDiagonalMask`` lets Q block i see only K/V block i; ``BlockDiagonalCausalMask``
+    is top-left causal inside every block);
+  * PyTorch's fp64 ``scaled_dot_product_attention`` and ``logsumexp`` (a special case
+    that reduces to a library routine);
+  * closed forms and invariants that hold for any input;
+  * hand-derived cases stored in tests/golden/closed_form_cases.json.
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form_cases.json")
+NEG_INF = float("-inf")
+
+
+# --------------------------------------------------------------------------------------
+# Pure-Python brute force
+# --------------------------------------------------------------------------------------
+
+def _seq_of(pos, cu):
+    for s in range(len(cu) - 1):
+        if cu[s] <= pos < cu[s + 1]:
+            return s
+    raise IndexError(pos)
+
+
+def materialize_bias(kind, M, Mkv, kv_offset=0, cu_q=None, cu_k=None):
+    """Dense additive bias [M][Mkv] of 0.0 / -inf, one element at a time."""
+    bias = [[0.0] * Mkv for _ in range(M)]
+    for i in range(M):
+        for j in range(Mkv):
+            if kind == 0:                                   # no mask
+                keep = True
+            elif kind == 1:                                 # top-left causal
+                keep = (kv_offset + j) <= i
+            else:                                           # block-diagonal (+ causal)
+                si, sj = _seq_of(i, cu_q), _seq_of(j, cu_k)
+                keep = si == sj
+                if keep and kind == 3:
+                    keep = (kv_offset + j - cu_k[sj]) <= (i - cu_q[si])
+            bias[i][j] = 0.0 if keep else NEG_INF
+    return bias
+
+
+def brute_attention(q, k, v, scale, kind=0, cu_q=None, cu_k=None, kv_offset=0):
+    """Loops over (b, h, i, j, d) with Python floats. Returns out [B][M][H][Kv], lse [B][H][M]."""
+    q, k, v = (np.asarray(t, dtype=np.float64).tolist() for t in (q, k, v))
+    B, M, H, K = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
+    Mkv, Hk, Kv = len(k[0]), len(k[0][0]), len(v[0][0][0])
+    s = float(np.float32(scale))
+    bias = materialize_bias(kind, M, Mkv, kv_offset, cu_q, cu_k)
+    out = [[[[0.0] * Kv for _ in range(H)] for _ in range(M)] for _ in range(B)]
+    lse = [[[NEG_INF] * M for _ in range(H)] for _ in range(B)]
+    for b in range(B):
+        for h in range(H):
+            hk = h if Hk == H else 0
+            for i in range(M):
+                x = []
+                for j in range(Mkv):
+                    dot = math.fsum(q[b][i][h][d] * k[b][j][hk][d] for d in range(K))
+                    x.append(s * dot + bias[i][j])
+                finite = [xj for xj in x if xj != NEG_INF]
+                if not finite:
+                    continue
+                mx = max(finite)
+                e = [math.exp(xj - mx) if xj != NEG_INF else 0.0 for xj in x]
+                z = math.fsum(e)
+                for d in range(Kv):
+                    out[b][i][h][d] = math.fsum(e[j] * v[b][j][hk][d] for j in range(Mkv)) / z
+                lse[b][h][i] = mx + math.log(z)
+    return np.array(out), np.array(lse)
+
+
+def brute_merge(outs, lses):
+    """Per-element LSE merge with Python floats."""
+    n = len(outs)
+    outs = [np.asarray(o, dtype=np.float64) for o in outs]
+    lses = [np.asarray(l_, dtype=np.float64) for l_ in lses]
+    B, M, H, Kv = outs[0].shape
+    out = np.zeros((B, M, H, Kv))
+    lse = np.full((B, H, M), NEG_INF)
+    for b in range(B):
+        for h in range(H):
+            for i in range(M):
+                ls = [float(lses[c][b, h, i]) for c in range(n)]
+                fin = [x for x in ls if x != NEG_INF]
+                if not fin:
+                    continue
+                tot = math.log(math.fsum(math.exp(x) for x in fin)) if max(fin) < 700 else None
+                if tot is None:
+                    mx = max(fin)
+                    tot = mx + math.log(math.fsum(math.exp(x - mx) for x in fin))
+                lse[b, h, i] = tot
+                for d in range(Kv):
+                    out[b, i, h, d] = math.fsum(
+                        math.exp(ls[c] - tot) * float(outs[c][b, i, h, d])
+                        for c in range(n) if ls[c] != NEG_INF)
+    return out, lse
+
+
+# --------------------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------------------
+
+def _rand(rng, shape, scale=1.0):
+    return rng.standard_normal(shape) * scale
+
+
+def _bf16_round(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    inf_a, inf_b = np.isneginf(a), np.isneginf(b)
+    assert np.array_equal(inf_a, inf_b), f"{what}: -inf pattern differs"
+    assert not np.isnan(a).any() and not np.isnan(b).any(), f"{what}: NaN"
+    fin = ~inf_a
+    if fin.any():
+        err = np.max(np.abs(a[fin] - b[fin]))
+        assert err <= tol, f"{what}: max |diff| {err:.3e} > {tol:.1e}"
+
+
+def _tiny_cases():
+    """Deterministic tiny shapes covering every mask, kv_offset, shared K/V heads."""
+    rng = np.random.default_rng(1234)
+    cases = []
+    for kind in (0, 1, 2, 3):
+        for trial in range(3):
+            K = int(rng.integers(1, 9))
+            Kv = int(rng.integers(1, 9))
+            H = int(rng.integers(1, 3))
+            Hk = H if trial != 2 else 1
+            if kind >= 2:
+                B = 1
+                nq = [int(x) for x in rng.integers(0, 6, size=3)]
+                nk = [int(x) for x in rng.integers(1, 6, size=3)]
+                cu_q = [0]
+                cu_k = [0]
+                for a, b in zip(nq, nk):
+                    cu_q.append(cu_q[-1] + a)
+                    cu_k.append(cu_k[-1] + b)
+                M, Mkv = cu_q[-1], cu_k[-1]
+                if M == 0:
+                    nq[0] = 2
+                    cu_q = [0, 2, 2 + nq[1], 2 + nq[1] + nq[2]]
+                    M = cu_q[-1]
+            else:
+                B = int(rng.integers(1, 3))
+                M = int(rng.integers(1, 18))
+                Mkv = int(rng.integers(1, 18))
+                cu_q = cu_k = None
+            kv_off = int(rng.integers(0, 4)) if kind in (1, 3) and trial == 1 else 0
+            q = _bf16_round(_rand(rng, (B, M, H, K)))
+            k = _bf16_round(_rand(rng, (B, Mkv, Hk, K)))
+            v = _bf16_round(_rand(rng, (B, Mkv, Hk, Kv)))
+            scale = float(rng.uniform(0.1, 1.5))
+            cases.append((kind, q, k, v, scale, cu_q, cu_k, kv_off))
+    return cases
+
+
+# --------------------------------------------------------------------------------------
+# Pins
+# --------------------------------------------------------------------------------------
+
+def pin_bruteforce(orc):
+    """Oracle == element-by-element brute force on tiny inputs, every mask, to 1e-12."""
+    for kind, q, k, v, scale, cu_q, cu_k, kv_off in _tiny_cases():
+        o_ref, l_ref = brute_attention(q, k, v, scale, kind, cu_q, cu_k, kv_off)
+        o, l_ = orc.attention(q, k, v, scale, kind, cu_q, cu_k, kv_off)
+        _close(o, o_ref, 1e-12, f"out kind={kind}")
+        _close(l_, l_ref, 1e-12, f"lse kind={kind}")
+
+
+def pin_torch_sdpa(orc):
+    """Oracle == torch fp64 scaled_dot_product_attention (+ logsumexp) with a boolean mask."""
+    rng = np.random.default_rng(7)
+    for kind, (M, Mkv) in ((0, (40, 57)), (1, (64, 64)), (1, (33, 70))):
+        B, H, K, Kv = 2, 3, 32, 24
+        q = _bf16_round(_rand(rng, (B, M, H, K)))
+        k = _bf16_round(_rand(rng, (B, Mkv, H, K)))
+        v = _bf16_round(_rand(rng, (B, Mkv, H, Kv)))
+        scale = 0.3
+        s64 = float(np.float32(scale))
+        tq, tk, tv = (torch.from_numpy(t).permute(0, 2, 1, 3) for t in (q, k, v))
+        if kind == 1:
+            allow = torch.ones(M, Mkv, dtype=torch.bool).tril()
+        else:
+            allow = torch.ones(M, Mkv, dtype=torch.bool)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk, tv, attn_mask=allow, scale=s64)
+        scores = (tq @ tk.transpose(-1, -2)) * s64
+        scores = scores.masked_fill(~allow, float("-inf"))
+        ref_lse = torch.logsumexp(scores, dim=-1)
+        o, l_ = orc.attention(q, k, v, scale, kind)
+        _close(o, ref.permute(0, 2, 1, 3).numpy(), 1e-12, "sdpa out")
+        _close(l_, ref_lse.numpy(), 1e-12, "sdpa lse")
+
+
+def pin_single_key(orc):
+    """Mkv = 1: out = v0 and lse = scale * q.k0 for every row."""
+    rng = np.random.default_rng(3)
+    q = _bf16_round(_rand(rng, (2, 5, 2, 8)))
+    k = _bf16_round(_rand(rng, (2, 1, 2, 8)))
+    v = _bf16_round(_rand(rng, (2, 1, 2, 6)))
+    o, l_ = orc.attention(q, k, v, 0.7)
+    s = float(np.float32(0.7))
+    for b in range(2):
+        for h in range(2):
+            for i in range(5):
+                _close(o[b, i, h], v[b, 0, h], 1e-14, "single key out")
+                expect = s * math.fsum(q[b, i, h, d] * k[b, 0, h, d] for d in range(8))
+                _close(l_[b, h, i], expect, 1e-12, "single key lse")
+
+
+def pin_constant_v(orc):
+    """Every value row equal to c: out = c whatever the scores (any mask, non-empty rows)."""
+    rng = np.random.default_rng(4)
+    q = _bf16_round(_rand(rng, (1, 9, 2, 16)))
+    k = _bf16_round(_rand(rng, (1, 12, 2, 16)))
+    c = np.array([0.5, -2.0, 3.25, 1.0])
+    v = np.broadcast_to(c, (1, 12, 2, 4)).copy()
+    for kind in (0, 1):
+        o, _ = orc.attention(q, k, v, 0.9, kind)
+        _close(o, np.broadcast_to(c, o.shape), 1e-13, "constant v")
+
+
+def pin_causal_row0(orc):
+    """Top-left causal, row 0 sees only key 0: out = v0, lse = scale * q0.k0."""
+    rng = np.random.default_rng(5)
+    q = _bf16_round(_rand(rng, (1, 6, 1, 8)))
+    k = _bf16_round(_rand(rng, (1, 9, 1, 8)))
+    v = _bf16_round(_rand(rng, (1, 9, 1, 5)))
+    o, l_ = orc.attention(q, k, v, 0.4, 1)
+    _close(o[0, 0, 0], v[0, 0, 0], 1e-14, "causal row0 out")
+    s = float(np.float32(0.4))
+    _close(l_[0, 0, 0], s * math.fsum(q[0, 0, 0] * k[0, 0, 0]), 1e-13, "causal row0 lse")
+    # row 1 sees exactly keys 0 and 1 (two-term softmax written out)
+    x0 = s * math.fsum(q[0, 1, 0] * k[0, 0, 0])
+    x1 = s * math.fsum(q[0, 1, 0] * k[0, 1, 0])
+    w1 = 1.0 / (1.0 + math.exp(x0 - x1))
+    _close(o[0, 1, 0], (1 - w1) * v[0, 0, 0] + w1 * v[0, 1, 0], 1e-13, "causal row1 out")
+
+
+def pin_zero_query(orc):
+    """q = 0: uniform weights over the allowed set; out = mean of v there, lse = ln|A_i|."""
+    rng = np.random.default_rng(6)
+    M, Mkv = 7, 10
+    q = np.zeros((1, M, 1, 8))
+    k = _bf16_round(_rand(rng, (1, Mkv, 1, 8)))
+    v = _bf16_round(_rand(rng, (1, Mkv, 1, 3)))
+    for kind, kv_off in ((0, 0), (1, 0), (1, 2)):
+        o, l_ = orc.attention(q, k, v, 1.0, kind, kv_offset=kv_off)
+        for i in range(M):
+            n = Mkv if kind == 0 else max(0, min(Mkv, i - kv_off + 1))
+            if n == 0:
+                assert l_[0, 0, i] == NEG_INF and np.all(o[0, i, 0] == 0.0), "empty row"
+                continue
+            _close(o[0, i, 0], v[0, :n, 0].mean(axis=0), 1e-14, "zero q out")
+            _close(l_[0, 0, i], math.log(n), 1e-14, "zero q lse")
+
+
+def pin_duplicate_keys(orc):
+    """Concatenating K and V with themselves (no mask): out unchanged, lse + ln 2."""
+    rng = np.random.default_rng(8)
+    q = _bf16_round(_rand(rng, (2, 6, 2, 8)))
+    k = _bf16_round(_rand(rng, (2, 11, 2, 8)))
+    v = _bf16_round(_rand(rng, (2, 11, 2, 7)))
+    o1, l1 = orc.attention(q, k, v, 0.6)
+    o2, l2 = orc.attention(q, np.concatenate([k, k], 1), np.concatenate([v, v], 1), 0.6)
+    _close(o2, o1, 1e-13, "dup out")
+    _close(l2, l1 + math.log(2.0), 1e-13, "dup lse")
+
+
+def pin_permute_keys(orc):
+    """Permuting the keys (and values alike) changes nothing when there is no mask."""
+    rng = np.random.default_rng(9)
+    q = _bf16_round(_rand(rng, (1, 8, 2, 8)))
+    k = _bf16_round(_rand(rng, (1, 13, 2, 8)))
+    v = _bf16_round(_rand(rng, (1, 13, 2, 4)))
+    perm = rng.permutation(13)
+    o1, l1 = orc.attention(q, k, v, 0.5)
+    o2, l2 = orc.attention(q, k[:, perm], v[:, perm], 0.5)
+    _close(o2, o1, 1e-13, "perm out")
+    _close(l2, l1, 1e-13, "perm lse")
+
+
+def pin_scale_folds_into_q(orc):
+    """attention(q, 2s) == attention(2q, s): the scale multiplies the scores."""
+    rng = np.random.default_rng(10)
+    q = _bf16_round(_rand(rng, (1, 5, 1, 8)))
+    k = _bf16_round(_rand(rng, (1, 7, 1, 8)))
+    v = _bf16_round(_rand(rng, (1, 7, 1, 3)))
+    o1, l1 = orc.attention(q, k, v, 0.5)
+    o2, l2 = orc.attention(2 * q, k, v, 0.25)
+    _close(o2, o1, 1e-13, "scale out")
+    _close(l2, l1, 1e-13, "scale lse")
+
+
+def pin_shared_kv_head(orc):
+    """One K/V head shared by all query heads == that head copied to every query head."""
+    rng = np.random.default_rng(11)
+    q = _bf16_round(_rand(rng, (1, 6, 3, 8)))
+    k1 = _bf16_round(_rand(rng, (1, 9, 1, 8)))
+    v1 = _bf16_round(_rand(rng, (1, 9, 1, 5)))
+    o1, l1 = orc.attention(q, k1, v1, 0.5, 1)
+    o2, l2 = orc.attention(q, np.repeat(k1, 3, 2), np.repeat(v1, 3, 2), 0.5, 1)
+    _close(o1, o2, 0.0, "shared head out")
+    _close(l1, l2, 0.0, "shared head lse")
+    # and each head matches brute force with its own query
+    ob, lb = brute_attention(q, k1, v1, 0.5, 1)
+    _close(o1, ob, 1e-12, "shared head brute out")
+    _close(l1, lb, 1e-12, "shared head brute lse")
+
+
+def _split_and_merge(orc, q, k, v, scale, kind, bounds, cu_q=None, cu_k_chunks=None):
+    outs, lses = [], []
+    for c, (s0, s1) in enumerate(bounds):
+        cu_k = None if cu_k_chunks is None else cu_k_chunks[c]
+        o, l_ = orc.attention_partial(q, k[:, s0:s1], v[:, s0:s1], scale, kind, cu_q, cu_k,
+                                      kv_offset=s0 if kind == 1 else 0)
+        outs.append(o)
+        lses.append(l_)
+    return orc.merge_attentions(outs, lses)
+
+
+def pin_merge_any_chunking(orc):
+    """Merge of partials over any disjoint chunking == full attention (no mask and causal)."""
+    rng = np.random.default_rng(12)
+    q = _bf16_round(_rand(rng, (2, 9, 2, 8)))
+    k = _bf16_round(_rand(rng, (2, 16, 2, 8)))
+    v = _bf16_round(_rand(rng, (2, 16, 2, 6)))
+    for kind in (0, 1):
+        o_full, l_full = orc.attention(q, k, v, 0.5, kind)
+        for bounds in ([(0, 8), (8, 16)], [(0, 3), (3, 4), (4, 11), (11, 16)],
+                       [(j, j + 1) for j in range(16)], [(0, 16)]):
+            o, l_ = _split_and_merge(orc, q, k, v, 0.5, kind, bounds)
+            _close(o, o_full, 1e-13, f"merge out kind={kind} n={len(bounds)}")
+            _close(l_, l_full, 1e-13, f"merge lse kind={kind} n={len(bounds)}")
+
+
+def pin_merge_against_brute(orc):
+    """Oracle merge == per-element brute-force merge on random chunk results, incl. -inf."""
+    rng = np.random.default_rng(13)
+    n, B, M, H, Kv = 3, 2, 5, 2, 4
+    outs = [_rand(rng, (B, M, H, Kv)) for _ in range(n)]
+    lses = [_rand(rng, (B, H, M), 3.0) for _ in range(n)]
+    lses[1][0, 1, 2] = NEG_INF
+    lses[0][1, 0, 4] = lses[1][1, 0, 4] = lses[2][1, 0, 4] = NEG_INF
+    o, l_ = orc.merge_attentions(np.stack(outs), np.stack(lses))
+    ob, lb = brute_merge(outs, lses)
+    _close(o, ob, 1e-13, "merge brute out")
+    _close(l_, lb, 1e-13, "merge brute lse")
+
+
+def pin_merge_identities(orc):
+    """Single chunk is the identity; chunk order is irrelevant; a -inf chunk has no effect."""
+    rng = np.random.default_rng(14)
+    B, M, H, Kv = 1, 6, 2, 5
+    outs = [_rand(rng, (B, M, H, Kv)) for _ in range(4)]
+    lses = [_rand(rng, (B, H, M)) for _ in range(4)]
+    o, l_ = orc.merge_attentions(outs[:1], lses[:1])
+    _close(o, outs[0], 1e-15, "identity out")
+    _close(l_, lses[0], 1e-15, "identity lse")
+    o1, l1 = orc.merge_attentions(outs, lses)
+    perm = [2, 0, 3, 1]
+    o2, l2 = orc.merge_attentions([outs[i] for i in perm], [lses[i] for i in perm])
+    _close(o1, o2, 1e-14, "perm out")
+    _close(l1, l2, 1e-14, "perm lse")
+    junk = _rand(rng, (B, M, H, Kv)) * 1e3
+    o3, l3 = orc.merge_attentions(outs + [junk], lses + [np.full((B, H, M), NEG_INF)])
+    _close(o3, o1, 1e-14, "-inf chunk out")
+    _close(l3, l1, 1e-14, "-inf chunk lse")
+    try:
+        orc.merge_attentions([], [])
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("zero chunks must be rejected")
+
+
+def pin_varlen_equals_per_sequence(orc):
+    """Packed block-diagonal (causal) attention == each sequence attended on its own."""
+    rng = np.random.default_rng(15)
+    lq, lk = [3, 5, 1, 4], [4, 5, 2, 6]
+    cu_q = [0, 3, 8, 9, 13]
+    cu_k = [0, 4, 9, 11, 17]
+    q = _bf16_round(_rand(rng, (1, 13, 2, 8)))
+    k = _bf16_round(_rand(rng, (1, 17, 2, 8)))
+    v = _bf16_round(_rand(rng, (1, 17, 2, 6)))
+    for kind, dense in ((2, 0), (3, 1)):
+        o, l_ = orc.attention(q, k, v, 0.5, kind, cu_q, cu_k)
+        for s in range(4):
+            qs, ks = cu_q[s], cu_k[s]
+            o_s, l_s = orc.attention(q[:, qs:qs + lq[s]], k[:, ks:ks + lk[s]],
+                                     v[:, ks:ks + lk[s]], 0.5, dense)
+            _close(o[:, qs:qs + lq[s]], o_s, 1e-14, f"varlen out kind={kind}")
+            _close(l_[:, :, qs:qs + lq[s]], l_s, 1e-14, f"varlen lse kind={kind}")
+
+
+def pin_varlen_partial_offset(orc):
+    """Block-diagonal causal partials over per-sequence key chunks, merged == full."""
+    rng = np.random.default_rng(16)
+    lens = [6, 3, 7]
+    cu = [0, 6, 9, 16]
+    q = _bf16_round(_rand(rng, (1, 16, 1, 8)))
+    k = _bf16_round(_rand(rng, (1, 16, 1, 8)))
+    v = _bf16_round(_rand(rng, (1, 16, 1, 4)))
+    o_full, l_full = orc.attention(q, k, v, 0.5, 3, cu, cu)
+    # chunk c takes keys [c*2, c*2+2) of every sequence (shorter sequences run out)
+    outs, lses = [], []
+    for c in range(4):
+        idx, cu_kc = [], [0]
+        for s, L in enumerate(lens):
+            sel = [cu[s] + j for j in range(2 * c, min(L, 2 * c + 2))]
+            idx += sel
+            cu_kc.append(cu_kc[-1] + len(sel))
+        o, l_ = orc.attention_partial(q, k[:, idx], v[:, idx], 0.5, 3, cu, cu_kc,
+                                      kv_offset=2 * c)
+        outs.append(o)
+        lses.append(l_)
+    o, l_ = orc.merge_attentions(outs, lses)
+    _close(o, o_full, 1e-13, "varlen partial out")
+    _close(l_, l_full, 1e-13, "varlen partial lse")
+
+
+def pin_empty_rows(orc):
+    """Rows with no allowed key give out = 0 and lse = -inf (causal chunk past the row)."""
+    rng = np.random.default_rng(17)
+    q = _bf16_round(_rand(rng, (1, 4, 1, 8)))
+    k = _bf16_round(_rand(rng, (1, 3, 1, 8)))
+    v = _bf16_round(_rand(rng, (1, 3, 1, 4)))
+    o, l_ = orc.attention_partial(q, k, v, 0.5, 1, kv_offset=2)
+    assert np.all(o[0, :2] == 0.0) and np.all(np.isneginf(l_[0, 0, :2])), "empty rows"
+    assert np.all(np.isfinite(l_[0, 0, 2:])), "rows 2, 3 have keys"
+
+
+def _ev(x, env):
+    """Evaluate a nested list whose leaves are numbers or closed-form expressions."""
+    if isinstance(x, list):
+        return [_ev(e, env) for e in x]
+    if isinstance(x, str):
+        return float(eval(x, {"__builtins__": {}}, env))
+    return float(x)
+
+
+def pin_golden_cases(orc):
+    """Hand-derived closed-form cases (tests/golden/closed_form_cases.json)."""
+    with open(GOLDEN) as f:
+        spec = json.load(f)
+    env = {"log": math.log, "inf": float("inf")}
+    for case in spec["attention"]:
+        q, k, v = (np.array(_ev(case[n], env)) for n in ("q", "k", "v"))
+        o, l_ = orc.attention(q, k, v, case["scale"], case["mask_kind"])
+        _close(o, np.array(_ev(case["out"], env)), 1e-12, case["name"] + " out")
+        _close(l_, np.array(_ev(case["lse"], env)), 1e-12, case["name"] + " lse")
+    for case in spec["merge"]:
+        outs = np.array(_ev(case["out_split"], env))
+        lses = np.array(_ev(case["lse_split"], env))
+        o, l_ = orc.merge_attentions(outs, lses)
+        _close(o, np.array(_ev(case["out"], env)), 1e-12, case["name"] + " out")
+        _close(l_, np.array(_ev(case["lse"], env)), 1e-12, case["name"] + " lse")
+
+
+def pin_widen_bf16(orc):
+    """Bit widening of bf16 == PyTorch's bf16 -> fp64 conversion for every non-NaN pattern."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    got = orc.widen_bf16_bits(bits)
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok]), "bf16 widening"
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "bf16 NaN patterns"
+
+
+PINS = [
+    pin_bruteforce,
+    pin_torch_sdpa,
+    pin_single_key,
+    pin_constant_v,
+    pin_causal_row0,
+    pin_zero_query,
+    pin_duplicate_keys,
+    pin_permute_keys,
+    pin_scale_folds_into_q,
+    pin_shared_kv_head,
+    pin_merge_any_chunking,
+    pin_merge_against_brute,
+    pin_merge_identities,
+    pin_varlen_equals_per_sequence,
+    pin_varlen_partial_offset,
+    pin_empty_rows,
+    pin_golden_cases,
+    pin_widen_bf16,
+]

@@ -1,0 +1,63 @@
+"""Each plausible mistake planted in a copy of the oracle trips at least one pin.
+
+The mutants are text substitutions on oracle/attention.py, loaded as throwaway
+modules on the CPU; the real oracle is never modified.
+"""
+
+import importlib.util
+import os
+import sys
+import types
+
+import pytest
+
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "attention.py")
+
+MUTANTS = {
+    "causal_strict_diagonal": ("allowed = kj <= qi", "allowed = kj < qi"),
+    "causal_ignores_offset": ("kj = k_pos0 + np.arange(Lk)[None, :]",
+                              "kj = np.arange(Lk)[None, :]"),
+    "scale_dropped": ("x = scale64 * (qb @ kb.T)", "x = (qb @ kb.T)"),
+    "scores_use_values": ("x = scale64 * (qb @ kb.T)", "x = scale64 * (qb @ vb.T)"),
+    "lse_wrong_sign": ("lse = m + np.log(l)", "lse = m - np.log(l)"),
+    "lse_drops_max": ("lse = m + np.log(l)", "lse = np.log(l)"),
+    "out_not_normalised": ("out = (p @ vb) / l[:, None]", "out = (p @ vb)"),
+    "exp_not_shifted": ("p = np.exp(x - np.where(empty, 0.0, m)[:, None])", "p = np.exp(x)"),
+    "empty_rows_not_zeroed": ("    out[empty] = 0.0\n", ""),
+    "shared_head_always_zero": ("hk = h if k.shape[2] == H else 0", "hk = 0"),
+    "blockdiag_sees_all_keys": ("_block(qb_all[qs:qe], kb_all[ks:ke], vb_all[ks:ke], s64,",
+                                "_block(qb_all[qs:qe], kb_all, vb_all, s64,"),
+    "blockdiag_absolute_positions": ("mask_kind == MASK_BLOCKDIAG_CAUSAL, 0, kv_offset)",
+                                     "mask_kind == MASK_BLOCKDIAG_CAUSAL, qs, ks + kv_offset)"),
+    "merge_averages": ("coef = w / sum_w[None]", "coef = np.ones_like(w) / w.shape[0]"),
+    "merge_lse_drops_shift": ("lse = m_star + np.log(sum_w)", "lse = np.log(sum_w)"),
+    "merge_unnormalised": ("coef = w / sum_w[None]", "coef = w"),
+    "merge_first_chunk_only": ("for c, o in enumerate(outs):", "for c, o in enumerate(outs[:1]):"),
+    "scale_not_float32": ("return float(np.float32(scale))", "return float(scale)"),
+    "bf16_widen_wrong_shift": ("<< np.uint32(16)", "<< np.uint32(15)"),
+}
+
+
+def _load_mutant(name, find, replace):
+    with open(SRC) as f:
+        src = f.read()
+    assert src.count(find) == 1, f"mutant {name}: pattern must occur exactly once"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    mod.__file__ = SRC
+    exec(compile(src.replace(find, replace), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    mod = _load_mutant(name, *MUTANTS[name])
+    failures = []
+    for pin in oracle_pins.PINS:
+        try:
+            pin(mod)
+        except Exception as e:  # noqa: BLE001 - any failure (assert, shape error) counts
+            failures.append((pin.__name__, type(e).__name__))
+    assert failures, f"no pin caught mutant {name}"
