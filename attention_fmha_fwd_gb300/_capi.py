@@ -1,0 +1,107 @@
+"""ctypes declarations of the C ABI in include/mslk_attn.h (names and types only).
+
+Loading fails loudly: there is no fallback when libmslk_attn.so is missing.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmslk_attn.so")
+
+MSLK_OK = 0
+MSLK_ERR_INVALID_ARG = 1
+MSLK_ERR_UNSUPPORTED = 2
+MSLK_ERR_MISALIGNED = 3
+MSLK_ERR_CUDA = 4
+MSLK_ERR_DEVICE_TIMEOUT = 5
+STATUS_NAMES = {
+    0: "MSLK_OK", 1: "MSLK_ERR_INVALID_ARG", 2: "MSLK_ERR_UNSUPPORTED",
+    3: "MSLK_ERR_MISALIGNED", 4: "MSLK_ERR_CUDA", 5: "MSLK_ERR_DEVICE_TIMEOUT",
+}
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_BLOCKDIAG = 2
+MASK_BLOCKDIAG_CAUSAL = 3
+DTYPE_BF16 = 0
+DTYPE_FP32 = 1
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("m", ctypes.c_int64), ("h", ctypes.c_int64)]
+
+
+class Seqlens(ctypes.Structure):
+    _fields_ = [
+        ("cu_seqlens_q", ctypes.c_void_p),
+        ("cu_seqlens_k", ctypes.c_void_p),
+        ("n_seqs", ctypes.c_int32),
+        ("max_seqlen_q", ctypes.c_int32),
+        ("max_seqlen_k", ctypes.c_int32),
+    ]
+
+
+class MslkError(RuntimeError):
+    """A non-OK mslk_status, with the library's reason string."""
+
+    def __init__(self, status: int, reason: str):
+        self.status = status
+        self.reason = reason
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {reason}")
+
+
+_P = ctypes.c_void_p
+_S = ctypes.POINTER(Strides)
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+
+# name -> (restype, argtypes), in header order.
+SIGNATURES = {
+    "mslk_attn_fwd": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32, _i32,
+                             ctypes.c_float, _i32, ctypes.POINTER(Seqlens), _P, _P, _P]),
+    "mslk_attn_partial": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32, _i32,
+                                 ctypes.c_float, _i32, ctypes.POINTER(Seqlens), _i64, _P, _i32,
+                                 _P, _P]),
+    "mslk_merge_attentions": (_i32, [_P, _P, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _S, _S,
+                                     _P, _i32, _P, _P]),
+    "mslk_last_error": (ctypes.c_char_p, []),
+    "mslk_device_status": (_i32, [_P]),
+    "mslk_set_wait_timeout_ns": (None, [_i64]),
+    "mslk_diag_bounded_wait": (_i32, [_P]),
+    "mslk_set_path_policy": (None, [_i32]),
+    "mslk_version": (_i32, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libmslk_attn.so (once) and declare its functions."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build it with attention_fmha_fwd_gb300.build.build() "
+                "(nvcc, sm_103a); there is no fallback implementation")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def check(status: int) -> None:
+    if status != MSLK_OK:
+        reason = load().mslk_last_error()
+        raise MslkError(status, reason.decode() if reason else "")

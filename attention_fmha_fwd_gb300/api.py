@@ -1,0 +1,231 @@
+"""PyTorch-facing calls over the C ABI: marshal tensors into pointers, strides and sizes.
+
+PyTorch supplies device memory and the stream; every step of the computation runs in
+libmslk_attn.so's CUDA kernels.  The calls mirror MSLK's fMHA API ("Attention - Core
+fMHA"): forward with optional LSE, partial attention over one K/V chunk, and the exact
+LSE merge.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+import torch
+
+from . import _capi
+from ._capi import MslkError, Seqlens, Strides, check
+
+MASKS = {
+    "none": _capi.MASK_NONE,
+    "causal": _capi.MASK_CAUSAL,
+    "blockdiag": _capi.MASK_BLOCKDIAG,
+    "blockdiag_causal": _capi.MASK_BLOCKDIAG_CAUSAL,
+}
+_DTYPES = {torch.bfloat16: _capi.DTYPE_BF16, torch.float32: _capi.DTYPE_FP32}
+
+
+def _mask_kind(mask) -> int:
+    if isinstance(mask, str):
+        if mask not in MASKS:
+            raise ValueError(f"unknown mask {mask!r}; expected one of {sorted(MASKS)}")
+        return MASKS[mask]
+    return int(mask)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _bmhk_strides(t: torch.Tensor, name: str) -> Strides:
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, M, H, D], got shape {tuple(t.shape)}")
+    if t.shape[3] > 1 and t.stride(3) != 1:
+        raise ValueError(f"{name}: the last dimension must have stride 1")
+    return Strides(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _as_bmhk(t: torch.Tensor) -> torch.Tensor:
+    """BMK -> BM1K (a view); BMHK unchanged."""
+    if t.dim() == 3:
+        return t.unsqueeze(2)
+    return t
+
+
+def _check_inputs(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (the library reads device memory)")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+
+
+def _seqlens(mask_kind, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k):
+    if mask_kind not in (_capi.MASK_BLOCKDIAG, _capi.MASK_BLOCKDIAG_CAUSAL):
+        return None, ()
+    if cu_seqlens_q is None or cu_seqlens_k is None:
+        raise ValueError("block-diagonal masks need cu_seqlens_q and cu_seqlens_k")
+    keep = []
+    cq, ck = cu_seqlens_q, cu_seqlens_k
+    if cq.dtype != torch.int32 or not cq.is_cuda or not cq.is_contiguous():
+        raise ValueError("cu_seqlens_q must be a contiguous int32 CUDA tensor")
+    if ck.dtype != torch.int32 or not ck.is_cuda or not ck.is_contiguous():
+        raise ValueError("cu_seqlens_k must be a contiguous int32 CUDA tensor")
+    if max_seqlen_q is None or max_seqlen_k is None:
+        raise ValueError("block-diagonal masks need max_seqlen_q and max_seqlen_k (host ints)")
+    sl = Seqlens(cq.data_ptr(), ck.data_ptr(), cq.numel() - 1, int(max_seqlen_q), int(max_seqlen_k))
+    keep.append(sl)
+    return ctypes.byref(sl), keep
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", scale=None,
+             cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
+             out=None, lse=True, stream=None):
+    """Fused attention forward; returns (out, lse) with lse None when ``lse=False``.
+
+    q [B,M,H,K], k [B,Mkv,H,K], v [B,Mkv,H,Kv] bf16 CUDA tensors (BMK inputs are viewed
+    as one head).  ``lse`` may be True (allocate), False (skip) or an fp32 [B,H,M] tensor.
+    """
+    q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
+    _check_inputs(q, k, v)
+    B, M, H, K = q.shape
+    Mkv, Kv = k.shape[1], v.shape[3]
+    mk = _mask_kind(mask)
+    if out is None:
+        out = torch.empty((B, M, H, Kv), dtype=torch.bfloat16, device=q.device)
+    if lse is True:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    sq, sk, sv, so = (_bmhk_strides(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
+    lib = _capi.load()
+    check(lib.mslk_attn_fwd(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(sq), ctypes.byref(sk),
+                            ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H, K, Kv,
+                            0.0 if scale is None else float(scale), mk, sl, _ptr(out),
+                            _ptr(lse), _stream_handle(stream)))
+    return out, lse
+
+
+def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none",
+                 scale=None, kv_offset: int = 0, cu_seqlens_q=None, cu_seqlens_k=None,
+                 max_seqlen_q=None, max_seqlen_k=None, out_dtype=torch.float32, out=None,
+                 lse=None, stream=None):
+    """Attention over one disjoint K/V chunk; returns (out, lse) for merge_attentions.
+
+    ``kv_offset`` is the position of the chunk's first key (causal masks only).
+    """
+    q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
+    _check_inputs(q, k, v)
+    B, M, H, K = q.shape
+    Mkv, Kv = k.shape[1], v.shape[3]
+    mk = _mask_kind(mask)
+    if out_dtype not in _DTYPES:
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    if out is None:
+        out = torch.empty((B, M, H, Kv), dtype=out_dtype, device=q.device)
+    elif out.dtype != out_dtype:
+        raise ValueError("out dtype does not match out_dtype")
+    if lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    sq, sk, sv, so = (_bmhk_strides(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
+    lib = _capi.load()
+    check(lib.mslk_attn_partial(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(sq), ctypes.byref(sk),
+                                ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H, K, Kv,
+                                0.0 if scale is None else float(scale), mk, sl, int(kv_offset),
+                                _ptr(out), _DTYPES[out_dtype], _ptr(lse),
+                                _stream_handle(stream)))
+    return out, lse
+
+
+def _stacked(parts, what):
+    """A list of equally spaced same-shape tensors -> (base tensor, chunk stride) without copies."""
+    if isinstance(parts, torch.Tensor):
+        return parts[0], (parts.stride(0) if parts.shape[0] > 1 else 0), parts.shape[0]
+    parts = list(parts)
+    if not parts:
+        raise MslkError(_capi.MSLK_ERR_INVALID_ARG, f"merge_attentions: no {what} chunks")
+    base = parts[0]
+    es = base.element_size()
+    if len(parts) == 1:
+        return base, 0, 1
+    d = parts[1].data_ptr() - base.data_ptr()
+    ok = d > 0 and d % es == 0 and all(
+        p.shape == base.shape and p.stride() == base.stride() and p.dtype == base.dtype and
+        p.data_ptr() - base.data_ptr() == i * d for i, p in enumerate(parts))
+    if not ok:  # not one strided allocation: stack them (argument marshalling)
+        st = torch.stack(parts)
+        return st[0], st.stride(0), st.shape[0]
+    return base, d // es, len(parts)
+
+
+def merge_attentions(out_split, lse_split, *, write_lse=True, output_dtype=torch.bfloat16,
+                     out=None, lse=None, stream=None):
+    """Exact LSE merge of chunk results (stacked [n,B,M,H,Kv] fp32, or a list of chunks).
+
+    Returns (out, lse) with lse None when ``write_lse`` is False.
+    """
+    o0, cs_o, n = _stacked(out_split, "output")
+    l0, cs_l, n_l = _stacked(lse_split, "lse")
+    if n != n_l:
+        raise ValueError("different numbers of output and lse chunks")
+    if o0.dtype != torch.float32 or l0.dtype != torch.float32:
+        raise ValueError("chunk outputs and lse must be float32")
+    if not l0.is_contiguous():
+        raise ValueError("each lse chunk must be a contiguous [B,H,M] tensor")
+    B, M, H, Kv = o0.shape
+    if output_dtype not in _DTYPES:
+        raise ValueError("output_dtype must be torch.bfloat16 or torch.float32")
+    if out is None:
+        out = torch.empty((B, M, H, Kv), dtype=output_dtype, device=o0.device)
+    if write_lse and lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=o0.device)
+    if not write_lse:
+        lse = None
+    ss = _bmhk_strides(o0, "out_split")
+    so = _bmhk_strides(out, "out")
+    lib = _capi.load()
+    check(lib.mslk_merge_attentions(_ptr(o0), _ptr(l0), n, cs_o, cs_l, B, M, H, Kv,
+                                    ctypes.byref(ss), ctypes.byref(so), _ptr(out),
+                                    _DTYPES[out.dtype], _ptr(lse), _stream_handle(stream)))
+    return out, lse
+
+
+def device_status(stream=None) -> int:
+    """Synchronise ``stream``; return the status of the device error word (and clear it)."""
+    return int(_capi.load().mslk_device_status(_stream_handle(stream)))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _capi.load().mslk_set_wait_timeout_ns(int(ns))
+
+
+def diag_bounded_wait(stream=None) -> None:
+    check(_capi.load().mslk_diag_bounded_wait(_stream_handle(stream)))
+
+
+def set_path_policy(policy: int) -> None:
+    """0 automatic, 1 always the tensor-core kernel."""
+    _capi.load().mslk_set_path_policy(int(policy))
+
+
+def last_error() -> str:
+    r = _capi.load().mslk_last_error()
+    return r.decode() if r else ""
+
+
+def version() -> int:
+    return int(_capi.load().mslk_version())
+
+
+__all__: Sequence[str] = [
+    "attn_fwd", "attn_partial", "merge_attentions", "device_status", "set_wait_timeout_ns",
+    "diag_bounded_wait", "set_path_policy", "last_error", "version", "MslkError", "MASKS",
+]

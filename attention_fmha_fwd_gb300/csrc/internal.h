@@ -1,0 +1,74 @@
+// internal.h — launch descriptions shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mslk_attn.h"
+
+namespace mslk {
+
+// A validated attention problem (forward or partial), strides in elements.
+struct AttnProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  mslk_strides sq, sk, sv, so;
+  int B, M, Mkv, H, K, Kv;
+  float scale;          // already defaulted (> 0)
+  int mask_kind;
+  const int32_t* cu_q;  // device, block-diagonal kinds only
+  const int32_t* cu_k;
+  int n_seqs, max_seqlen_q, max_seqlen_k;
+  int64_t kv_offset;    // 0 for the forward call
+  void* out;
+  bool out_fp32;
+  float* lse;           // may be null (forward without lse)
+  bool kv_head_shared;  // k/v head stride 0: every query head reads K/V head 0
+};
+
+struct MergeProblem {
+  const float* out_split;
+  const float* lse_split;
+  int n_chunks;
+  int64_t cs_out, cs_lse;
+  int B, M, H, Kv;
+  mslk_strides ss, so;
+  void* out;
+  bool out_fp32;
+  float* lse;
+};
+
+// Where bounded in-kernel waits report, and how long they wait.
+struct DeviceCtl {
+  unsigned int* err;
+  unsigned long long timeout_ns;
+};
+
+// Error-word bits.
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+constexpr bool is_causal(int mask_kind) {
+  return mask_kind == MSLK_MASK_CAUSAL || mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL;
+}
+constexpr bool is_blockdiag(int mask_kind) {
+  return mask_kind == MSLK_MASK_BLOCKDIAG || mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL;
+}
+
+// Largest query-row count the CUDA-core decode kernel takes.
+constexpr int kDecodeMaxRows = 8;
+
+// Tensor-core (tcgen05) forward/partial kernel.  `why` receives a reason on failure.
+cudaError_t launch_fmha_tc(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
+                           const char** why);
+// CUDA-core streaming kernel for M <= kDecodeMaxRows with dense masks.
+cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream);
+// out = 0, lse = -inf for every row (no keys at all).
+cudaError_t launch_fill_empty(const AttnProblem& p, cudaStream_t stream);
+// LSE merge.
+cudaError_t launch_merge(const MergeProblem& p, cudaStream_t stream);
+// Diagnostic bounded wait on a barrier that never completes.
+cudaError_t launch_bounded_wait_diag(const DeviceCtl& ctl, cudaStream_t stream);
+
+}  // namespace mslk

@@ -1,0 +1,332 @@
+// mslk_attn.cu — the C ABI: argument validation with reasons, path selection, the
+// per-device error word of the bounded in-kernel waits, and two small kernels
+// (empty-key fill, bounded-wait diagnostic).
+//
+// Validation follows the pages' support checks (an operator's not_supported_reasons
+// and check_lastdim_alignment_stride1): every rejection returns before any launch,
+// writes nothing, and leaves its reason in mslk_last_error().
+
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mslk {
+namespace {
+
+thread_local char g_last_error[512] = "";
+std::atomic<long long> g_timeout_ns{2000000000LL};
+
+// 0 = automatic, 1 = always the tensor-core kernel, 2 = the decode kernel where it applies.
+std::atomic<int> g_path_policy{0};
+
+mslk_status fail(mslk_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+mslk_status fail(mslk_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+mslk_status ok() {
+  g_last_error[0] = '\0';
+  return MSLK_OK;
+}
+
+__device__ unsigned int g_error_word;
+
+// Device address of g_error_word for the current device (looked up once per device).
+unsigned int* error_word_ptr() {
+  constexpr int kMaxDevices = 64;
+  static unsigned int* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Stride rule for tensors read by TMA or written with 16-byte vectors: every stride of a
+// dimension with extent > 1 is a positive multiple of `mult` elements.  A stride of 0 is
+// allowed on the head dimension of k/v when `allow_zero_head`.
+const char* check_strides(const mslk_strides& s, long long batch, long long rows, long long heads,
+                          int mult, bool allow_zero_head) {
+  if (s.b < 0 || s.m < 0 || s.h < 0) return "negative stride";
+  if (batch > 1 && (s.b == 0 || s.b % mult)) return "batch stride";
+  if (rows > 1 && (s.m == 0 || s.m % mult)) return "sequence stride";
+  if (heads > 1) {
+    if (s.h == 0 && !allow_zero_head) return "head stride";
+    if (s.h % mult) return "head stride";
+  }
+  return nullptr;
+}
+
+mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const void* v,
+                          const mslk_strides* sq, const mslk_strides* sk, const mslk_strides* sv,
+                          const mslk_strides* so, int32_t B, int32_t M, int32_t Mkv, int32_t H,
+                          int32_t K, int32_t Kv, float scale, int32_t mask_kind,
+                          const mslk_seqlens* seqlens, int64_t kv_offset, void* out,
+                          int32_t out_dtype, float* lse, bool lse_required, const char* who) {
+  if (B < 0 || M < 0 || Mkv < 0 || H < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative size", who);
+  if (mask_kind < MSLK_MASK_NONE || mask_kind > MSLK_MASK_BLOCKDIAG_CAUSAL)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: unknown mask_kind %d", who, mask_kind);
+  if (out_dtype != MSLK_DTYPE_BF16 && out_dtype != MSLK_DTYPE_FP32)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: unknown out_dtype %d", who, out_dtype);
+  if (sq == nullptr || sk == nullptr || sv == nullptr || so == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: null strides", who);
+  if (K != Kv)
+    return fail(MSLK_ERR_UNSUPPORTED, "%s: K (%d) != Kv (%d) is not supported", who, K, Kv);
+  if (K != 64 && K != 128)
+    return fail(MSLK_ERR_UNSUPPORTED, "%s: head dim %d not supported (64 or 128)", who, K);
+  p = AttnProblem{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.sq = *sq;
+  p.sk = *sk;
+  p.sv = *sv;
+  p.so = *so;
+  p.B = B;
+  p.M = M;
+  p.Mkv = Mkv;
+  p.H = H;
+  p.K = K;
+  p.Kv = Kv;
+  p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : 1.0f / std::sqrt(static_cast<float>(K));
+  p.mask_kind = mask_kind;
+  p.kv_offset = kv_offset;
+  p.out = out;
+  p.out_fp32 = out_dtype == MSLK_DTYPE_FP32;
+  p.lse = lse;
+  if (B == 0 || H == 0 || M == 0) return ok();  // nothing to compute
+  if (out == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: out is null", who);
+  if (lse_required && lse == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: lse is required", who);
+  if (is_blockdiag(mask_kind)) {
+    if (B != 1)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: block-diagonal masks take a packed batch (B = 1), got B = %d",
+                  who, B);
+    if (seqlens == nullptr || seqlens->cu_seqlens_q == nullptr || seqlens->cu_seqlens_k == nullptr)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: block-diagonal mask needs cu_seqlens_q/k", who);
+    if (seqlens->n_seqs < 1 || seqlens->max_seqlen_q < 1 || seqlens->max_seqlen_q > M ||
+        seqlens->max_seqlen_k < 0 || seqlens->max_seqlen_k > Mkv)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: bad seqlens (n_seqs %d, max_seqlen_q %d, max_seqlen_k %d)",
+                  who, seqlens->n_seqs, seqlens->max_seqlen_q, seqlens->max_seqlen_k);
+    p.cu_q = seqlens->cu_seqlens_q;
+    p.cu_k = seqlens->cu_seqlens_k;
+    p.n_seqs = seqlens->n_seqs;
+    p.max_seqlen_q = seqlens->max_seqlen_q;
+    p.max_seqlen_k = seqlens->max_seqlen_k;
+  }
+  if (Mkv == 0) return ok();  // every row empty; q/k/v are not read
+  if (q == nullptr || k == nullptr || v == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: q/k/v is null", who);
+  if ((sk->h == 0) != (sv->h == 0) && H > 1)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: k and v must both or neither use a shared (stride 0) head", who);
+  p.kv_head_shared = H > 1 && sk->h == 0;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+    return fail(MSLK_ERR_MISALIGNED, "%s: q/k/v base must be 16-byte aligned", who);
+  if (const char* w = check_strides(*sq, B, M, H, 8, false))
+    return fail(MSLK_ERR_MISALIGNED, "%s: q %s must be a positive multiple of 8 elements (16 bytes)", who, w);
+  if (const char* w = check_strides(*sk, B, Mkv, H, 8, true))
+    return fail(MSLK_ERR_MISALIGNED, "%s: k %s must be a positive multiple of 8 elements (16 bytes)", who, w);
+  if (const char* w = check_strides(*sv, B, Mkv, H, 8, true))
+    return fail(MSLK_ERR_MISALIGNED, "%s: v %s must be a positive multiple of 8 elements (16 bytes)", who, w);
+  if (!aligned16(out)) return fail(MSLK_ERR_MISALIGNED, "%s: out base must be 16-byte aligned", who);
+  if (const char* w = check_strides(*so, B, M, H, p.out_fp32 ? 4 : 8, false))
+    return fail(MSLK_ERR_MISALIGNED, "%s: out %s must be a positive multiple of 16 bytes", who, w);
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(MSLK_ERR_MISALIGNED, "%s: lse must be 4-byte aligned", who);
+  if (kv_offset < -(1LL << 31) || kv_offset > (1LL << 31))
+    return fail(MSLK_ERR_INVALID_ARG, "%s: kv_offset out of range", who);
+  return ok();
+}
+
+__global__ void fill_empty_kernel(void* out, int out_fp32, long long so_b, long long so_m,
+                                  long long so_h, float* lse, int B, int M, int H, int D) {
+  const long long n = static_cast<long long>(B) * M * H;
+  for (long long r = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; r < n;
+       r += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int h = static_cast<int>(r % H);
+    const int m = static_cast<int>((r / H) % M);
+    const int b = static_cast<int>(r / (static_cast<long long>(H) * M));
+    for (int c = 0; c < D; ++c) {
+      const long long off = b * so_b + m * so_m + h * so_h + c;
+      if (out_fp32)
+        static_cast<float*>(out)[off] = 0.f;
+      else
+        static_cast<__nv_bfloat16*>(out)[off] = __float2bfloat16(0.f);
+    }
+    if (lse != nullptr) lse[(static_cast<long long>(b) * H + h) * M + m] = -INFINITY;
+  }
+}
+
+// One thread waits, bounded, on a barrier that nothing completes.
+__global__ void bounded_wait_diag_kernel(unsigned int* err, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(b, 0)) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      atomicOr(err, kErrWaitTimeout);
+      break;
+    }
+  }
+}
+
+DeviceCtl device_ctl() {
+  return DeviceCtl{error_word_ptr(), static_cast<unsigned long long>(g_timeout_ns.load())};
+}
+
+mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who) {
+  if (p.B == 0 || p.H == 0 || p.M == 0) return ok();
+  if (p.Mkv == 0) {
+    fill_empty_kernel<<<256, 256, 0, stream>>>(p.out, p.out_fp32 ? 1 : 0, p.so.b, p.so.m, p.so.h,
+                                              p.lse, p.B, p.M, p.H, p.Kv);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+    return ok();
+  }
+  const DeviceCtl ctl = device_ctl();
+  if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "%s: no CUDA device / module", who);
+  const int policy = g_path_policy.load();
+  const bool decode_ok = p.M <= kDecodeMaxRows && !is_blockdiag(p.mask_kind);
+  cudaError_t e;
+  const char* why = "launch failed";
+  if (decode_ok && policy != 1) {
+    e = launch_fmha_decode(p, ctl, stream);
+  } else {
+    e = launch_fmha_tc(p, ctl, stream, &why);
+  }
+  if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "%s: %s (%s)", who, why, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+}  // namespace mslk
+
+using namespace mslk;
+
+extern "C" {
+
+mslk_status mslk_attn_fwd(const void* q, const void* k, const void* v, const mslk_strides* sq,
+                          const mslk_strides* sk, const mslk_strides* sv, const mslk_strides* so,
+                          int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv,
+                          float scale, int32_t mask_kind, const mslk_seqlens* seqlens, void* out,
+                          float* lse, void* stream) {
+  AttnProblem p;
+  const mslk_status s = validate_attn(p, q, k, v, sq, sk, sv, so, B, M, Mkv, H, K, Kv, scale,
+                                      mask_kind, seqlens, 0, out, MSLK_DTYPE_BF16, lse, false,
+                                      "mslk_attn_fwd");
+  if (s != MSLK_OK) return s;
+  return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_fwd");
+}
+
+mslk_status mslk_attn_partial(const void* q, const void* k, const void* v, const mslk_strides* sq,
+                              const mslk_strides* sk, const mslk_strides* sv, const mslk_strides* so,
+                              int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv,
+                              float scale, int32_t mask_kind, const mslk_seqlens* seqlens,
+                              int64_t kv_offset, void* out, int32_t out_dtype, float* lse,
+                              void* stream) {
+  AttnProblem p;
+  const mslk_status s = validate_attn(p, q, k, v, sq, sk, sv, so, B, M, Mkv, H, K, Kv, scale,
+                                      mask_kind, seqlens, kv_offset, out, out_dtype, lse, true,
+                                      "mslk_attn_partial");
+  if (s != MSLK_OK) return s;
+  return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_partial");
+}
+
+mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split, int32_t n_chunks,
+                                  int64_t chunk_stride_out, int64_t chunk_stride_lse, int32_t B,
+                                  int32_t M, int32_t H, int32_t Kv, const mslk_strides* s_split,
+                                  const mslk_strides* so, void* out, int32_t out_dtype, float* lse,
+                                  void* stream) {
+  const char* who = "mslk_merge_attentions";
+  if (n_chunks < 1) return fail(MSLK_ERR_INVALID_ARG, "%s: n_chunks must be >= 1 (got %d)", who, n_chunks);
+  if (B < 0 || M < 0 || H < 0 || Kv < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative size", who);
+  if (out_dtype != MSLK_DTYPE_BF16 && out_dtype != MSLK_DTYPE_FP32)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: unknown out_dtype %d", who, out_dtype);
+  if (s_split == nullptr || so == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: null strides", who);
+  if (B == 0 || M == 0 || H == 0) return ok();
+  if (Kv == 0 || Kv % 4) return fail(MSLK_ERR_UNSUPPORTED, "%s: Kv (%d) must be a positive multiple of 4", who, Kv);
+  if (out_split == nullptr || lse_split == nullptr || out == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: null pointer", who);
+  if (!aligned16(out_split) || !aligned16(out))
+    return fail(MSLK_ERR_MISALIGNED, "%s: out_split/out must be 16-byte aligned", who);
+  if (n_chunks > 1 && (chunk_stride_out <= 0 || chunk_stride_out % 4))
+    return fail(MSLK_ERR_MISALIGNED, "%s: chunk_stride_out must be a positive multiple of 4", who);
+  if (n_chunks > 1 && chunk_stride_lse <= 0)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: chunk_stride_lse must be positive", who);
+  if (const char* w = check_strides(*s_split, B, M, H, 4, false))
+    return fail(MSLK_ERR_MISALIGNED, "%s: out_split %s must be a positive multiple of 4 elements", who, w);
+  const bool out_fp32 = out_dtype == MSLK_DTYPE_FP32;
+  if (const char* w = check_strides(*so, B, M, H, out_fp32 ? 4 : 8, false))
+    return fail(MSLK_ERR_MISALIGNED, "%s: out %s must be a positive multiple of 16 bytes", who, w);
+  MergeProblem p{};
+  p.out_split = out_split;
+  p.lse_split = lse_split;
+  p.n_chunks = n_chunks;
+  p.cs_out = chunk_stride_out;
+  p.cs_lse = chunk_stride_lse;
+  p.B = B;
+  p.M = M;
+  p.H = H;
+  p.Kv = Kv;
+  p.ss = *s_split;
+  p.so = *so;
+  p.out = out;
+  p.out_fp32 = out_fp32;
+  p.lse = lse;
+  const cudaError_t e = launch_merge(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+  return ok();
+}
+
+const char* mslk_last_error(void) { return g_last_error; }
+
+mslk_status mslk_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "mslk_device_status: %s", cudaGetErrorString(e));
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+  if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "mslk_device_status: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    if (word & kErrWaitTimeout)
+      return fail(MSLK_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded wait");
+  }
+  return ok();
+}
+
+void mslk_set_wait_timeout_ns(int64_t ns) { g_timeout_ns.store(ns < 100000 ? 100000 : ns); }
+
+mslk_status mslk_diag_bounded_wait(void* stream) {
+  const DeviceCtl ctl = device_ctl();
+  if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "mslk_diag_bounded_wait: no CUDA device");
+  bounded_wait_diag_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(ctl.err, ctl.timeout_ns);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "mslk_diag_bounded_wait: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+void mslk_set_path_policy(int32_t policy) { g_path_policy.store(policy); }
+
+int32_t mslk_version(void) { return 100; }
+
+}  // extern "C"

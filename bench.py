@@ -1,0 +1,456 @@
+"""Benchmark: causal attention forward, B=2, M=Mkv=2048, H=32, K=Kv=128, bf16.
+
+One step = one mslk_attn_fwd call (the whole hot path for this workload: every key tile,
+online softmax, output and LSE) on resident inputs.  Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+`--impl reference` times the fp64 CPU oracle (the only reference this project has) on a
+bounded sample of the same workload.  Under torchrun (N > 1) every rank runs its own
+copy of the workload (weak scaling, no collective on the data path); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s (causal-adjusted) & % BF16 tensor peak; merge GB/s % HBM"
+WORKLOAD = "causal_fwd"
+# This pool's measured GB300 peaks (copied from the driver's probe); the file, when
+# present, takes precedence.
+PEAKS_FALLBACK = {"bf16_tflops": 1887.2, "bf16_tflops_sustained": 1710.7, "hbm_gbs": 6788.6}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SRC = os.path.join(ROOT, "attention_fmha_fwd_gb300", "csrc", "fmha_tc.cu")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in PEAKS_FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(PEAKS_FALLBACK), "measured (pool probe, copied)"
+
+
+def causal_pairs(M, Mkv, kv_offset=0):
+    """Allowed (query, key) pairs of a top-left causal mask."""
+    total = 0
+    for i in range(M):
+        last = min(Mkv - 1, i - kv_offset)
+        if last >= 0:
+            total += last + 1
+    return total
+
+
+def fwd_flops(w):
+    """Exact causal-adjusted FLOPs: 2*(K + Kv) per allowed (query, key) pair."""
+    return causal_pairs(w.M, w.Mkv) * 2 * (w.K + w.Kv) * w.B * w.H
+
+
+def kernel_sha():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+        e = d[kernel_key]
+        if e.get("source_sha") != kernel_sha():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return None
+        win = [s for t, s in self.samples if t0 <= t <= t1] or [s for _, s in self.samples[-3:]]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[0]) for s in win if num(s[0]) is not None]
+        mx = [num(s[1]) for s in win if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in win for n, v in zip(names, s[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(win)}
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(per_rank_seconds: float, per_rank_units: float, world: int, backend_reduce):
+    """Whole-job throughput: all ranks' units / the slowest rank's time."""
+    t_max = backend_reduce(per_rank_seconds)
+    return per_rank_units * world / t_max, t_max
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle_sample(q, k, v, w, budget_s, max_heads=None):
+    """The fp64 oracle on whole (batch, head) pairs of the workload until ~budget_s."""
+    import oracle
+
+    qf, kf, vf = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    pairs_per_head = causal_pairs(w.M, w.Mkv)
+    flops = 0.0
+    heads = 0
+    t0 = time.perf_counter()
+    for b in range(w.B):
+        for h in range(w.H):
+            oracle.attention_head(qf, kf, vf, b, h, w.scale, oracle.MASK_CAUSAL)
+            flops += pairs_per_head * 2 * (w.K + w.Kv)
+            heads += 1
+            if (max_heads and heads >= max_heads) or time.perf_counter() - t0 >= budget_s:
+                return flops, time.perf_counter() - t0, heads
+    return flops, time.perf_counter() - t0, heads
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    from attention_fmha_fwd_gb300 import inputs
+
+    w = inputs.WORKLOADS[WORKLOAD]
+    q, k, v = inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0)
+    per_step_heads = 2
+    times, flops = [], 0.0
+    for s in range(args.warmup + args.steps):
+        f, t, _ = time_oracle_sample(q, k, v, w, budget_s=1e9, max_heads=per_step_heads)
+        if s >= args.warmup:
+            times.append(t)
+            flops = f
+    mean_t = sum(times) / len(times)
+    value = flops / mean_t / 1e12
+    sample = f"{per_step_heads} of {w.B * w.H} (batch, head) pairs per step, all 2048 rows"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": mean_t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "causal_fwd B=2 M=Mkv=2048 H=32 K=Kv=128 causal (top-left)",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+
+        def reduce_max(x):
+            t = torch.tensor([x], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+
+        def barrier():
+            dist.barrier()
+    else:
+        torch.cuda.set_device(0)
+
+        def reduce_max(x):
+            return x
+
+        def barrier():
+            pass
+
+    import attention_fmha_fwd_gb300 as fa
+    from attention_fmha_fwd_gb300 import build, inputs
+
+    build.build()
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = inputs.WORKLOADS[WORKLOAD]
+    q, k, v = inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty((w.B, w.M, w.H, w.Kv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    flops = fwd_flops(w)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.attn_fwd(qd, kd, vd, mask="causal", scale=w.scale, out=out, lse=lse)
+
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    # keep the GPU busy briefly so the clock sampler sees load before the timed region
+    t_end = time.time() + 0.3
+    while time.time() < t_end:
+        step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()                       # L2 flushed between timed steps
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t1 = time.time()
+    per = [s.elapsed_time(e) * 1e-3 for s, e in zip(starts, ends)]
+    t_step = sum(per) / len(per)
+    value, t_max = aggregate(t_step, flops, world, reduce_max)
+    value /= 1e12
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    # ---- end to end through the public call: pinned host in, host out
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) * 1e-3 / e2e_steps
+    e2e_value, _ = aggregate(t_e2e, flops, world, reduce_max)
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    secondary = measure_secondary(fa, inputs, dev, flush, peaks) if (rank == 0 and not args.no_secondary) else None
+
+    if rank == 0:
+        achieved = flops / t_step / 1e12
+        traffic = traffic_for("fmha_tc_kernel<128> causal_fwd")
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "causal_fwd B=2 M=Mkv=2048 H=32 K=Kv=128 causal (top-left)",
+                       "flops_per_step": flops, "flop_count": "exact causal pairs x 2(K+Kv)",
+                       "l2": "flushed (256 MB write) between timed steps",
+                       "inputs": "seeded N(0,1) bf16, seed 0", "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": achieved,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                         "kernel": "fmha_tc_kernel<128>", "peak_source": peak_src + " bf16 burst"},
+            "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "secondary": secondary,
+        }
+        if not args.no_cpu_baseline:
+            f, t, heads = time_oracle_sample(q, k, v, w, budget_s=args.cpu_budget)
+            line["cpu_baseline"] = {
+                "value": f / t / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+                "kind": "oracle",
+                "sample": f"{heads} of {w.B * w.H} (batch, head) pairs, all 2048 rows, fp64 numpy"}
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _time_it(fn, reps, stream, flush):
+    import torch
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    return statistics.median(ts)
+
+
+def measure_secondary(fa, inputs, dev, flush, peaks):
+    """Merge roofline shape, decode split-KV and varlen throughput (context numbers)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    res = {}
+    # merge: 8 chunks of [2, 2048, 32, 128] fp32 -> bf16 out + fp32 lse
+    n, B, M, H, Kv = 8, 2, 2048, 32, 128
+    g = torch.Generator(device=dev).manual_seed(0)
+    outs = torch.randn((n, B, M, H, Kv), generator=g, device=dev)
+    lses = torch.randn((n, B, H, M), generator=g, device=dev)
+    mo = torch.empty((B, M, H, Kv), dtype=torch.bfloat16, device=dev)
+    ml = torch.empty((B, H, M), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        fa.merge_attentions(outs, lses, out=mo, lse=ml)
+    t = _time_it(lambda: fa.merge_attentions(outs, lses, out=mo, lse=ml), 20, stream, flush)
+    nbytes = outs.numel() * 4 + lses.numel() * 4 + mo.numel() * 2 + ml.numel() * 4
+    res["merge_8x[2,2048,32,128]"] = {"us": t * 1e6, "GB/s": nbytes / t / 1e9,
+                                      "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
+                                      "bytes": nbytes}
+    del outs, lses
+    # decode split-KV: 16 x 1 query, 32768 keys, 8 heads, 16 chunks of 2048 + merge
+    w = inputs.WORKLOADS["decode_split_kv"]
+    q, k, v = inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    bounds = inputs.equal_chunks(w.Mkv, 16)
+    po = torch.empty((16, w.B, w.M, w.H, w.Kv), dtype=torch.float32, device=dev)
+    pl = torch.empty((16, w.B, w.H, w.M), dtype=torch.float32, device=dev)
+    fo = torch.empty((w.B, w.M, w.H, w.Kv), dtype=torch.bfloat16, device=dev)
+    fl = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=dev)
+
+    def partials():
+        for c, (a, b) in enumerate(bounds):
+            fa.attn_partial(qd, kd[:, a:b], vd[:, a:b], scale=w.scale, out=po[c], lse=pl[c])
+
+    for _ in range(2):
+        partials()
+    t_p = _time_it(partials, 10, stream, flush)
+    t_m = _time_it(lambda: fa.merge_attentions(po, pl, out=fo, lse=fl), 10, stream, flush)
+    kv_bytes = (kd.numel() + vd.numel()) * 2
+    res["decode_split_kv_16x2048"] = {"partials_us": t_p * 1e6, "merge_us": t_m * 1e6,
+                                      "partial_GB/s": kv_bytes / t_p / 1e9,
+                                      "frac_hbm": kv_bytes / t_p / 1e9 / peaks["hbm_gbs"],
+                                      "launches": 17}
+    del kd, vd, k, v
+    # varlen packed block-diagonal causal
+    w = inputs.WORKLOADS["varlen_packed"]
+    lens = inputs.varlen_seqlens(w.n_seqs, w.M, seed=0)
+    cu = torch.tensor(inputs.cu_seqlens(lens), dtype=torch.int32, device=dev)
+    q, k, v = inputs.qkv(1, w.M, w.Mkv, w.H, w.K, seed=0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    vo = torch.empty((1, w.M, w.H, w.Kv), dtype=torch.bfloat16, device=dev)
+    vl = torch.empty((1, w.H, w.M), dtype=torch.float32, device=dev)
+
+    def vstep():
+        fa.attn_fwd(qd, kd, vd, mask="blockdiag_causal", scale=w.scale, cu_seqlens_q=cu,
+                    cu_seqlens_k=cu, max_seqlen_q=max(lens), max_seqlen_k=max(lens),
+                    out=vo, lse=vl)
+
+    for _ in range(3):
+        vstep()
+    t_v = _time_it(vstep, 10, stream, flush)
+    vflops = sum(L * (L + 1) // 2 for L in lens) * 2 * (w.K + w.Kv) * w.H
+    res["varlen_packed_12seq_16384"] = {"us": t_v * 1e6, "TFLOP/s": vflops / t_v / 1e12,
+                                        "frac_bf16": vflops / t_v / 1e12 / peaks["bf16_tflops"],
+                                        "seqlens": lens}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

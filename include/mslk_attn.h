@@ -1,0 +1,201 @@
+/*
+ * mslk_attn.h — C ABI of the GB300 (sm_103a) fused multi-head attention forward library.
+ *
+ * What the calls compute (MSLK kernel reference, "Attention - Core fMHA"):
+ *
+ *   out[b,i,h,:] = sum_{j in A_i} softmax_j(scale * q[b,i,h,:] . k[b,j,h,:]) * v[b,j,h,:]
+ *   lse[b,h,i]   = ln sum_{j in A_i} exp(scale * q[b,i,h,:] . k[b,j,h,:])
+ *
+ * without materialising the score matrix.  A_i is the set of keys the mask allows
+ * for query row i (MSLK kernel reference, "Attention - Biases & masks").  A row whose
+ * allowed set is empty gets out = 0 and lse = -inf.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are [B, M, H, D] (q, out), [B, Mkv, H, D] (k, v): batch, sequence, head,
+ *    head dim.  The last dimension has stride 1; the other three strides are free and
+ *    given in ELEMENTS by mslk_strides (MSLK kernel reference, memory_efficient_attention
+ *    constraints: "last dimension must have stride 1; other dimensions may be
+ *    non-contiguous").  The output has the query layout with its last dimension
+ *    replaced by the value head dim.
+ *  - GQA / MQA: the caller expands K/V to H heads (the pages: MSLK does not broadcast
+ *    K/V heads).  A head stride of 0 on k and v (an expand() of one head) is accepted.
+ *  - q, k, v are bf16.  K == Kv and K is 64 or 128; other head dims return
+ *    MSLK_ERR_UNSUPPORTED.
+ *  - lse is fp32 [B, H, M], contiguous.  Packed variable-length batches (B = 1) use
+ *    [1, H, total_q].
+ *  - Every pointer is caller-owned DEVICE memory (except the mslk_seqlens struct and
+ *    the mslk_strides structs, which live on the host and are read during the call).
+ *    The library allocates no device memory and keeps no state between calls, apart
+ *    from a per-device error word read by mslk_device_status().
+ *  - Alignment: q, k, v, out base pointers 16-byte aligned; every free stride times the
+ *    element size a multiple of 16 bytes (the tensor-memory-accelerator copy rule).
+ *    Violations return MSLK_ERR_MISALIGNED.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream).  Argument errors return before any launch and write nothing.  A failed
+ *    launch returns MSLK_ERR_CUDA.  Kernels bound every internal wait; a wait that runs
+ *    out sets the device error word, which mslk_device_status() reports as
+ *    MSLK_ERR_DEVICE_TIMEOUT.
+ *  - scale <= 0 or NaN selects the default 1/sqrt(K) (scale=None in the pages).
+ *  - Results are deterministic: no atomics on the data path; the same inputs give the
+ *    same bits.
+ */
+#ifndef MSLK_ATTN_H
+#define MSLK_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSLK_OK = 0,
+  MSLK_ERR_INVALID_ARG = 1,     /* null pointer, bad size, bad mask/seqlens combination */
+  MSLK_ERR_UNSUPPORTED = 2,     /* valid request this build does not implement (head dim) */
+  MSLK_ERR_MISALIGNED = 3,      /* base pointer or stride breaks the 16-byte rule */
+  MSLK_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
+  MSLK_ERR_DEVICE_TIMEOUT = 5   /* a bounded in-kernel wait ran out (mslk_device_status) */
+} mslk_status;
+
+/* Mask kinds (MSLK kernel reference, "Attention - Biases & masks"). */
+typedef enum {
+  MSLK_MASK_NONE = 0,              /* every key */
+  MSLK_MASK_CAUSAL = 1,            /* LowerTriangularMask: top-left, key position <= query row */
+  MSLK_MASK_BLOCKDIAG = 2,         /* BlockDiagonalMask: packed sequences, B = 1 */
+  MSLK_MASK_BLOCKDIAG_CAUSAL = 3   /* BlockDiagonalCausalMask: top-left causal inside each block */
+} mslk_mask_kind;
+
+typedef enum { MSLK_DTYPE_BF16 = 0, MSLK_DTYPE_FP32 = 1 } mslk_dtype;
+
+/* Element strides of the batch, sequence and head dimensions (head dim stride is 1). */
+typedef struct {
+  int64_t b, m, h;
+} mslk_strides;
+
+/*
+ * Sequence metadata of a packed batch (BlockDiagonalMask.from_seqlens; the standalone
+ * Blackwell facade's cu_seqlens_q / cu_seqlens_k / max_seq_len_q / max_seq_len_k).
+ * cu_seqlens_q/k are DEVICE int32 arrays of n_seqs + 1 non-decreasing offsets starting
+ * at 0 and ending at M / Mkv.  max_seqlen_q must be >= every query length (rows of longer
+ * sequences beyond it are not computed).  Offsets outside [0, M] / [0, Mkv] are clamped
+ * by the kernels, never dereferenced.  Ignored (may be NULL) for the dense masks.
+ */
+typedef struct {
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int32_t n_seqs;
+  int32_t max_seqlen_q;
+  int32_t max_seqlen_k;
+} mslk_seqlens;
+
+/*
+ * mslk_attn_fwd — fused attention forward returning out and (optionally) lse.
+ * MSLK kernel reference, "Attention - Core fMHA" > memory_efficient_attention_forward
+ * (out only, lse == NULL) and memory_efficient_attention_forward_requires_grad
+ * (returns (output, lse)); raw op "Attention - Raw Blackwell torch ops" > fmha_fwd.
+ *
+ *   q [B,M,H,K] bf16 (strides sq), k [B,Mkv,H,K] bf16 (sk), v [B,Mkv,H,Kv] bf16 (sv).
+ *   out [B,M,H,Kv] bf16 (strides so), written for every row.
+ *   lse [B,H,M] fp32 contiguous, or NULL to skip it.
+ *   mask_kind: mslk_mask_kind.  Block-diagonal kinds need B == 1 and `seqlens`.
+ *   Dropout is not part of this API (the pages' forward-with-LSE call rejects it).
+ * Sizes: B, M, H, Mkv >= 0 (B, M or H == 0: nothing to do; Mkv == 0: out = 0, lse = -inf).
+ */
+mslk_status mslk_attn_fwd(const void* q, const void* k, const void* v,
+                          const mslk_strides* sq, const mslk_strides* sk,
+                          const mslk_strides* sv, const mslk_strides* so,
+                          int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv,
+                          float scale, int32_t mask_kind, const mslk_seqlens* seqlens,
+                          void* out, float* lse, void* stream);
+
+/*
+ * mslk_attn_partial — attention over ONE disjoint key/value chunk, for exact split-KV.
+ * MSLK kernel reference, "Attention - Core fMHA" > memory_efficient_attention_partial:
+ * call it once per chunk with the same queries, then combine with mslk_merge_attentions.
+ *
+ * Arguments as mslk_attn_fwd, with k/v (and Mkv) describing the chunk only, plus:
+ *   kv_offset  position of the chunk's first key in the full key sequence (inside each
+ *              packed sequence for the block-diagonal kinds).  Only causal kinds read
+ *              it: key j of the chunk is allowed for row i iff kv_offset + j <= i.
+ *   out_dtype  MSLK_DTYPE_FP32 (recommended: keeps the merge exact to fp32) or
+ *              MSLK_DTYPE_BF16.  out strides `so` are in elements of that type.
+ *   lse        required, fp32 [B,H,M] contiguous.  Rows with no allowed key in this chunk
+ *              get out = 0, lse = -inf, so the merge gives the chunk zero weight.
+ */
+mslk_status mslk_attn_partial(const void* q, const void* k, const void* v,
+                              const mslk_strides* sq, const mslk_strides* sk,
+                              const mslk_strides* sv, const mslk_strides* so,
+                              int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K,
+                              int32_t Kv, float scale, int32_t mask_kind,
+                              const mslk_seqlens* seqlens, int64_t kv_offset, void* out,
+                              int32_t out_dtype, float* lse, void* stream);
+
+/*
+ * mslk_merge_attentions — exact log-sum-exp merge of n chunk results into preallocated
+ * outputs.  MSLK kernel reference, "Attention - Core fMHA" > merge_attentions (exact
+ * normalised output over the union of chunks, not an average; write_lse; output_dtype)
+ * and "Attention - Merge & storage utilities" > triton_splitk.merge_attentions
+ * (in-place into preallocated outputs) / fmha_merge_attentions_varargs.
+ *
+ *   out_split  fp32, chunk c at out_split + c*chunk_stride_out, each [B,M,H,Kv] with
+ *              strides s_split (chunks stacked on a leading axis, or any equally spaced
+ *              views).
+ *   lse_split  fp32, chunk c at lse_split + c*chunk_stride_lse, each [B,H,M] contiguous.
+ *   n_chunks   >= 1 (zero partials is an error, as merge_attentions_autograd raises).
+ *   out        [B,M,H,Kv] of out_dtype (BF16 or FP32), strides so.
+ *   lse        fp32 [B,H,M] contiguous, or NULL (write_lse = False).
+ * Per row: LSE = M* + ln sum_c exp(lse_c - M*) with M* = max_c lse_c;
+ * out = sum_c exp(lse_c - LSE) * out_c; a row whose chunks are all -inf gets out = 0 and
+ * LSE = -inf.  Kv must be a multiple of 4; out_split and the strides 16-byte aligned.
+ */
+mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split,
+                                  int32_t n_chunks, int64_t chunk_stride_out,
+                                  int64_t chunk_stride_lse, int32_t B, int32_t M, int32_t H,
+                                  int32_t Kv, const mslk_strides* s_split,
+                                  const mslk_strides* so, void* out, int32_t out_dtype,
+                                  float* lse, void* stream);
+
+/*
+ * Reason for the last non-OK status returned on the calling thread (like the pages'
+ * not_supported_reasons).  Thread-local; valid until the thread's next library call.
+ */
+const char* mslk_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns MSLK_ERR_DEVICE_TIMEOUT if any kernel since the last check gave up on a
+ * bounded wait (the kernel then wrote nothing further and returned), MSLK_ERR_CUDA if
+ * the synchronisation itself failed, else MSLK_OK.
+ */
+mslk_status mslk_device_status(void* stream);
+
+/*
+ * Sets the limit of every in-kernel wait, in nanoseconds (default 2e9; minimum 1e5).
+ * Process-wide; read at launch time.
+ */
+void mslk_set_wait_timeout_ns(int64_t ns);
+
+/*
+ * Diagnostic: launches one CTA that waits on a barrier nothing ever completes, bounded by
+ * the current wait limit, so callers can see the timeout path end cleanly.  Returns the
+ * launch status; the timeout itself is reported by mslk_device_status().
+ */
+mslk_status mslk_diag_bounded_wait(void* stream);
+
+/*
+ * Kernel choice, process-wide: 0 automatic (default: the CUDA-core decode kernel for
+ * M <= 8 with dense masks, the tensor-core kernel otherwise), 1 always the tensor-core
+ * kernel, 2 same as 0.  Both kernels compute the same function; tests use this to run
+ * one problem through both.
+ */
+void mslk_set_path_policy(int32_t policy);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t mslk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSLK_ATTN_H */

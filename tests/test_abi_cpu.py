@@ -1,0 +1,146 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every declared symbol, and
+rejects bad arguments with the documented status before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_fmha_fwd_gb300 import _capi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mslk_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _capi.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:mslk_status|void|int32_t|const char\*)\s+(mslk_\w+)\s*\(",
+                       text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("mslk_attn_fwd", "mslk_attn_partial", "mslk_merge_attentions", "mslk_last_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/mslk_attn.h but not exported"
+    assert set(names) == set(_capi.SIGNATURES), "binding and header disagree"
+
+
+def test_version(lib):
+    assert lib.mslk_version() == 100
+
+
+S = _capi.Strides
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, sq=S(8 * 128 * 64, 8 * 128, 128), sk=None, sv=None, so=None,
+             B=2, M=64, Mkv=64, H=8, K=128, Kv=128, scale=0.0, mask=0, seqlens=None,
+             out=FAKE, lse=FAKE)
+    a.update(kw)
+    for n in ("sk", "sv", "so"):
+        if a[n] is None:
+            a[n] = a["sq"]
+    ref = lambda s: None if s is False else ctypes.byref(s)  # noqa: E731
+    st = lib.mslk_attn_fwd(a["q"], a["k"], a["v"], ref(a["sq"]), ref(a["sk"]), ref(a["sv"]),
+                           ref(a["so"]), a["B"], a["M"], a["Mkv"], a["H"], a["K"], a["Kv"],
+                           a["scale"], a["mask"], a["seqlens"], a["out"], a["lse"], None)
+    return st, lib.mslk_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(K=96, Kv=96), _capi.MSLK_ERR_UNSUPPORTED, "head dim"),
+    (dict(K=128, Kv=64), _capi.MSLK_ERR_UNSUPPORTED, "Kv"),
+    (dict(mask=7), _capi.MSLK_ERR_INVALID_ARG, "mask_kind"),
+    (dict(B=-1), _capi.MSLK_ERR_INVALID_ARG, "negative"),
+    (dict(sq=False), _capi.MSLK_ERR_INVALID_ARG, "null strides"),
+    (dict(out=None), _capi.MSLK_ERR_INVALID_ARG, "out is null"),
+    (dict(q=None), _capi.MSLK_ERR_INVALID_ARG, "null"),
+    (dict(q=FAKE + 8), _capi.MSLK_ERR_MISALIGNED, "16-byte"),
+    (dict(out=FAKE + 4), _capi.MSLK_ERR_MISALIGNED, "out base"),
+    (dict(sq=S(8 * 128 * 64, 8 * 128 + 4, 128)), _capi.MSLK_ERR_MISALIGNED, "q sequence stride"),
+    (dict(sk=S(8 * 128 * 64, 8 * 128, 0)), _capi.MSLK_ERR_INVALID_ARG, "shared"),
+    (dict(sq=S(8 * 128 * 64, 8 * 128, 0)), _capi.MSLK_ERR_MISALIGNED, "q head stride"),
+    (dict(sq=S(-1, 8 * 128, 128)), _capi.MSLK_ERR_MISALIGNED, "negative"),
+    (dict(mask=2), _capi.MSLK_ERR_INVALID_ARG, "packed batch"),
+    (dict(mask=3, B=1), _capi.MSLK_ERR_INVALID_ARG, "cu_seqlens"),
+])
+def test_fwd_rejects(lib, kw, status, needle):
+    st, why = _fwd(lib, **kw)
+    assert st == status, why
+    assert needle in why
+
+
+def test_fwd_bad_seqlens(lib):
+    sl = _capi.Seqlens(FAKE, FAKE, 0, 10, 10)
+    st, why = _fwd(lib, mask=2, B=1, seqlens=ctypes.byref(sl))
+    assert st == _capi.MSLK_ERR_INVALID_ARG and "seqlens" in why
+    sl = _capi.Seqlens(FAKE, FAKE, 2, 65, 10)  # max_seqlen_q > M
+    st, why = _fwd(lib, mask=2, B=1, seqlens=ctypes.byref(sl))
+    assert st == _capi.MSLK_ERR_INVALID_ARG
+
+
+def test_fwd_empty_sizes_are_noops(lib):
+    for kw in (dict(M=0), dict(B=0), dict(H=0)):
+        st, why = _fwd(lib, out=None, q=None, **kw)
+        assert st == _capi.MSLK_OK, why
+
+
+def test_partial_requires_lse(lib):
+    s = S(8 * 128 * 64, 8 * 128, 128)
+    st = lib.mslk_attn_partial(FAKE, FAKE, FAKE, ctypes.byref(s), ctypes.byref(s), ctypes.byref(s),
+                               ctypes.byref(s), 2, 64, 64, 8, 128, 128, 0.0, 0, None, 0, FAKE,
+                               _capi.DTYPE_FP32, None, None)
+    assert st == _capi.MSLK_ERR_INVALID_ARG
+    assert "lse is required" in lib.mslk_last_error().decode()
+    st = lib.mslk_attn_partial(FAKE, FAKE, FAKE, ctypes.byref(s), ctypes.byref(s), ctypes.byref(s),
+                               ctypes.byref(s), 2, 64, 64, 8, 128, 128, 0.0, 0, None, 0, FAKE,
+                               5, FAKE, None)
+    assert st == _capi.MSLK_ERR_INVALID_ARG
+
+
+def _merge(lib, n=2, Kv=128, cs_out=2 * 64 * 8 * 128, out_split=FAKE, out=FAKE, dtype=0):
+    s = S(64 * 8 * 128, 8 * 128, 128)
+    st = lib.mslk_merge_attentions(out_split, FAKE, n, cs_out, 2 * 8 * 64, 2, 64, 8, Kv,
+                                   ctypes.byref(s), ctypes.byref(s), out, dtype, FAKE, None)
+    return st, lib.mslk_last_error().decode()
+
+
+def test_merge_rejects(lib):
+    assert _merge(lib, n=0)[0] == _capi.MSLK_ERR_INVALID_ARG      # zero partials is an error
+    assert _merge(lib, Kv=126)[0] == _capi.MSLK_ERR_UNSUPPORTED
+    assert _merge(lib, out_split=FAKE + 4)[0] == _capi.MSLK_ERR_MISALIGNED
+    assert _merge(lib, cs_out=6)[0] == _capi.MSLK_ERR_MISALIGNED
+    assert _merge(lib, dtype=9)[0] == _capi.MSLK_ERR_INVALID_ARG
+    assert _merge(lib, out=None)[0] == _capi.MSLK_ERR_INVALID_ARG
+
+
+def test_valid_call_without_device_reports_cuda_error(lib):
+    """A well-formed call gets past validation and fails cleanly at the CUDA layer when
+    there is no device (this container); on a GPU machine it would launch."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, why = _fwd(lib)
+    assert st == _capi.MSLK_ERR_CUDA, why
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _capi.load(str(tmp_path / "libmslk_attn.so"))
