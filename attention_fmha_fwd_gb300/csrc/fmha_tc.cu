@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <cstdio>
 #include <mutex>
 
 #include "internal.h"
@@ -145,7 +146,7 @@ MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_smem, uint32_t v_smem, bool a
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const TcArgs a) {
   using L = Layout<D>;
@@ -574,7 +575,15 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   }
   fmha_tc_kernel<D><<<grid, kThreads, Lt::kAlloc, stream>>>(tq, tk, tv, a);
   e = cudaGetLastError();
-  if (e != cudaSuccess) *why = "fmha_tc_kernel launch failed";
+  if (e != cudaSuccess) {
+    static thread_local char msg[160];
+    cudaFuncAttributes fa{};
+    cudaFuncGetAttributes(&fa, fmha_tc_kernel<D>);
+    snprintf(msg, sizeof(msg),
+             "fmha_tc_kernel launch failed (regs/thread %d, max threads/block %d, dyn smem %d)",
+             fa.numRegs, fa.maxThreadsPerBlock, Lt::kAlloc);
+    *why = msg;
+  }
   return e;
 }
 

@@ -256,13 +256,14 @@ def run_gpu(args):
     def step():
         fa.attn_fwd(qd, kd, vd, mask="causal", scale=w.scale, out=out, lse=lse)
 
-    sampler = ClockSampler(dev.index) if rank == 0 else None
+    sampler = ClockSampler(dev.index) if (rank == 0 and not args.profile_mode) else None
     for _ in range(args.warmup):
         step()
-    # keep the GPU busy briefly so the clock sampler sees load before the timed region
-    t_end = time.time() + 0.3
-    while time.time() < t_end:
-        step()
+    if not args.profile_mode:
+        # keep the GPU busy briefly so the clock sampler sees load before the timed region
+        t_end = time.time() + 0.3
+        while time.time() < t_end:
+            step()
     torch.cuda.synchronize()
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -285,6 +286,12 @@ def run_gpu(args):
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
+
+    if args.profile_mode:
+        if rank == 0:
+            print(json.dumps({"profile_mode": True, "ms_per_step": t_step * 1e3,
+                              "value": value, "unit": "TFLOP/s"}))
+        return 0
 
     # ---- end to end through the public call: pinned host in, host out
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
@@ -444,6 +451,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--profile-mode", action="store_true",
+                    help="only the warm-up and timed steps (for ncu); prints a short line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -289,9 +289,10 @@ def test_varlen_partial_merge():
         it = torch.tensor(idx, dtype=torch.long, device="cuda")
         kc, vc = kd[:, it].contiguous(), vd[:, it].contiguous()
         ckd = torch.tensor(cuc, dtype=torch.int32, device="cuda")
+        max_k = max(b - a for a, b in zip(cuc[:-1], cuc[1:]))
         o, l_ = fa.attn_partial(qd, kc, vc, mask="blockdiag_causal", kv_offset=64 * c,
                                 cu_seqlens_q=cqd, cu_seqlens_k=ckd, max_seqlen_q=max(lens),
-                                max_seqlen_k=64)
+                                max_seqlen_k=max_k)
         outs.append(o)
         lses.append(l_)
     out, lse = fa.merge_attentions(outs, lses)
