@@ -13,14 +13,19 @@
 //   warp  8     tcgen05.mma issue (one thread) + TMEM allocation
 //   warp  9     TMA producer (one thread)
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D),
-// fp32 accumulators, row r of a tile in lane r.
-// Shared memory: Q0, Q1, a ring of K/V tiles, P0, P1 (bf16 probabilities), all in the
-// 128-byte-swizzled K-major layout TMA writes (V is read MN-major by the PV MMA).
+// fp32 accumulators, row r of a tile in lane r.  The bf16 probabilities P_t overwrite the
+// first 64 columns of S_t (two values per column) and feed the PV MMA from tensor memory.
+// Shared memory: Q0, Q1 and a 5-stage ring of K/V tiles, in the 128-byte-swizzled
+// K-major layout TMA writes (V is read MN-major by the PV MMA).
+// The MMA and TMA roles run as whole converged warps that issue through one elected lane:
+// their operands stay warp-uniform, so they need few issue slots while the softmax
+// warpgroups keep the SM's schedulers busy.
 //
 // MMA order (ping-pong: the tensor core works on one tile while the other tile's
 // softmax runs):  S0_0 S1_0 | PV0_j S0_{j+1} PV1_j S1_{j+1} | ...
 // S_t(j+1) is committed after PV_t(j), so when a softmax warpgroup sees S_t(j+1) its
-// O_t is stable (it may rescale it) and its P buffer is free.
+// O_t is stable (it may rescale it) and PV_t(j) has finished reading P_t; MMAs issued by
+// one thread execute in order, so S_t(j+1) overwrites P_t(j) only after PV_t(j) read it.
 //
 // Online softmax in base 2: m2 = running max of scale*log2(e)*s; p = 2^(scale*log2e*s - m2);
 // l = running sum of p.  The running max used for p is only raised when the row max
@@ -60,12 +65,10 @@ template <int D>
 struct Layout {
   static constexpr int kKBlocks = D / 64;
   static constexpr int kTileBytes = kBlockM * D * 2;  // Q, K or V tile (128 rows)
-  static constexpr int kStages = (D == 128) ? 3 : 5;
-  static constexpr int kPBytes = kBlockM * kBlockN * 2;
+  static constexpr int kStages = (D == 128) ? 5 : 8;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
-  static constexpr int kPOff = kKVOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kPOff + kQTiles * kPBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain
   static constexpr int kNumBars = 1 + 2 * kStages + 6 + 1;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // abort flag, tmem slot
@@ -115,34 +118,45 @@ MSLK_DEV bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& w, bool hon
   return wait_slow(bar, parity, w, honor_abort);
 }
 
+// Whole-warp wait with a warp-uniform result; the warp is converged afterwards.
+MSLK_DEV bool wait_bar_warp(uint32_t bar, uint32_t parity, const WaitCtl& w, bool honor_abort = true) {
+  const bool ok = __all_sync(0xffffffffu, wait_bar(bar, parity, w, honor_abort));
+  __syncwarp();
+  return ok;
+}
+
 MSLK_DEV float u2f(uint32_t x) { return __uint_as_float(x); }
 MSLK_DEV uint32_t f2u(float x) { return __float_as_uint(x); }
 
-// S_t = Q_t K^T over the head dim, 16 columns per MMA.
-template <int D>
-MSLK_DEV void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, false);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * kSwizzleAtom + (kk % 4) * 32;
-    mma_f16_ss(d_tmem, smem_desc_sw128(q_smem + off, 16, 1024),
-               smem_desc_sw128(k_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
-  }
+// Shared-memory descriptors are built once per buffer; stepping to the next 16-element
+// slice only adds a constant to the start-address field (16-byte units), so each MMA
+// issue is two integer adds and the instruction itself.
+MSLK_DEV uint64_t desc_kmajor(uint32_t saddr) { return smem_desc_sw128(saddr, 16, 1024); }
+MSLK_DEV uint64_t desc_mnmajor(uint32_t saddr) { return smem_desc_sw128(saddr, kSwizzleAtom, 1024); }
+// Start-address step (16-byte units) of K-slice kk in a K-major 128-byte-swizzled tile.
+__host__ __device__ constexpr uint32_t kmajor_step(int kk) {
+  return static_cast<uint32_t>(((kk / 4) * kSwizzleAtom + (kk % 4) * 32) >> 4);
 }
 
-// O_t (+)= P_t V over the 128 keys of the tile, 16 keys per MMA.  V is read MN-major:
-// 8-key groups 1024 bytes apart (SBO), 64-column halves of the head dim 16 KiB apart (LBO).
+// S_t = Q_t K^T over the head dim, 16 columns per MMA.
 template <int D>
-MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_smem, uint32_t v_smem, bool accumulate) {
+MSLK_DEV void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+    mma_f16_ss_elect(d_tmem, q_desc + kmajor_step(kk), k_desc + kmajor_step(kk), idesc, kk > 0 ? 1u : 0u);
+}
+
+// O_t (+)= P_t V over the 128 keys of the tile, 16 keys per MMA.  P_t is read from tensor
+// memory (16 bf16 keys = 8 columns per MMA); V is read MN-major: 8-key groups 1024 bytes
+// apart (SBO), 64-column halves of the head dim 16 KiB apart (LBO); 16 keys are 2048 bytes.
+template <int D>
+MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, D, true);
 #pragma unroll
-  for (int kk = 0; kk < kBlockN / 16; ++kk) {
-    const uint32_t a_off = (kk / 4) * kSwizzleAtom + (kk % 4) * 32;
-    const uint32_t b_off = kk * 16 * 128;
-    mma_f16_ss(o_tmem, smem_desc_sw128(p_smem + a_off, 16, 1024),
-               smem_desc_sw128(v_smem + b_off, kSwizzleAtom, 1024), idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < kBlockN / 16; ++kk)
+    mma_f16_ts_elect(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint32_t>(kk * 2048 / 16),
+                     idesc, kk > 0 ? 1u : accumulate);
 }
 
 template <int D>
@@ -224,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_base = smem_u32(smem);
   auto q_addr = [&](int t) { return s_base + L::kQOff + t * L::kTileBytes; };
   auto kv_addr = [&](int s) { return s_base + L::kKVOff + s * L::kTileBytes; };
-  auto p_addr = [&](int t) { return s_base + L::kPOff + t * L::kPBytes; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -234,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
-      mbar_init(p_full(t), kBlockM);
+      mbar_init(p_full(t), kBlockM / 32);  // one arrival per softmax warp
       mbar_init(o_done(t), 1);
     }
     mbar_init(bar_drain, 1);
@@ -257,88 +270,89 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kWarpLoad) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, kQTiles * L::kTileBytes);
-      for (int t = 0; t < kQTiles; ++t)
+    // ------------------------------------------------------------ TMA producer (whole warp)
+    mbar_arrive_expect_tx_elect(bar_q, kQTiles * L::kTileBytes);
+    for (int t = 0; t < kQTiles; ++t)
+      for (int kb = 0; kb < L::kKBlocks; ++kb)
+        tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, bar_q, kb * 64,
+                          q_base + r0 + t * kBlockM, h, b);
+    int it = 0;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      for (int which = 0; which < 2; ++which, ++it) {  // K_j then V_j
+        const int s = it % L::kStages;
+        if (!(ok = wait_bar_warp(kv_empty(s), ((it / L::kStages) & 1) ^ 1, wc))) break;
+        mbar_arrive_expect_tx_elect(kv_full(s), L::kTileBytes);
+        const CUtensorMap* tm = which ? &tm_v : &tm_k;
         for (int kb = 0; kb < L::kKBlocks; ++kb)
-          tma_load_4d(q_addr(t) + kb * kSwizzleAtom, &tm_q, bar_q, kb * 64,
-                      q_base + r0 + t * kBlockM, h, b);
-      int it = 0;
-      bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        for (int which = 0; which < 2; ++which, ++it) {  // K_j then V_j
-          const int s = it % L::kStages;
-          if (!wait_bar(kv_empty(s), ((it / L::kStages) & 1) ^ 1, wc)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(kv_full(s), L::kTileBytes);
-          const CUtensorMap* tm = which ? &tm_v : &tm_k;
-          for (int kb = 0; kb < L::kKBlocks; ++kb)
-            tma_load_4d(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64,
-                        k_base + j * kBlockN, hk, b);
-        }
-      }
-      if (!ok) {  // let every copy this thread issued land before the CTA exits
-        wait_bar(bar_q, 0, wc, false);
-        for (int k = max(0, it - L::kStages); k < it; ++k)
-          wait_bar(kv_full(k % L::kStages), (k / L::kStages) & 1, wc, false);
+          tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64,
+                            k_base + j * kBlockN, hk, b);
       }
     }
+    if (!ok) {  // let every copy this warp issued land before the CTA exits
+      wait_bar_warp(bar_q, 0, wc, false);
+      for (int k = max(0, it - L::kStages); k < it; ++k)
+        wait_bar_warp(kv_full(k % L::kStages), (k / L::kStages) & 1, wc, false);
+    }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    {
       const uint32_t tm_s[2] = {tmem + 0u, tmem + 128u};
       const uint32_t tm_o[2] = {tmem + 256u, tmem + 384u};
-      bool ok = wait_bar(bar_q, 0, wc);
+      const uint64_t q_desc[2] = {desc_kmajor(q_addr(0)), desc_kmajor(q_addr(1))};
+      // Ring stages are kTileBytes apart: stage s adds s * kTileBytes / 16 to the address field.
+      const uint64_t kdesc0 = desc_kmajor(kv_addr(0));
+      const uint64_t vdesc0 = desc_mnmajor(kv_addr(0));
+      auto kv_kdesc = [&](int st) { return kdesc0 + static_cast<uint32_t>(st * (L::kTileBytes >> 4)); };
+      auto kv_vdesc = [&](int st) { return vdesc0 + static_cast<uint32_t>(st * (L::kTileBytes >> 4)); };
+      bool ok = wait_bar_warp(bar_q, 0, wc);
       int it = 0;
-      if (ok) ok = wait_bar(kv_full(0), 0, wc);
+      if (ok) ok = wait_bar_warp(kv_full(0), 0, wc);
       if (ok) {
         tc_fence_after();
-        issue_qk<D>(tm_s[0], q_addr(0), kv_addr(0));
-        mma_commit(s_full(0));
-        issue_qk<D>(tm_s[1], q_addr(1), kv_addr(0));
-        mma_commit(s_full(1));
-        mma_commit(kv_empty(0));
+        issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(0));
+        mma_commit_elect(s_full(0));
+        issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(0));
+        mma_commit_elect(s_full(1));
+        mma_commit_elect(kv_empty(0));
         it = 1;
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int sv = it % L::kStages;
-        if (!(ok = wait_bar(kv_full(sv), (it / L::kStages) & 1, wc))) break;
+        if (!(ok = wait_bar_warp(kv_full(sv), (it / L::kStages) & 1, wc))) break;
         ++it;
         const bool more = j + 1 < n_tiles;
         int sk = 0;
         // Q tile 0: PV0_j, then S0_{j+1}
-        if (!(ok = wait_bar(p_full(0), j & 1, wc))) break;
+        if (!(ok = wait_bar_warp(p_full(0), j & 1, wc))) break;
         tc_fence_after();
-        issue_pv<D>(tm_o[0], p_addr(0), kv_addr(sv), j > 0);
+        issue_pv<D>(tm_o[0], tm_s[0], kv_vdesc(sv), j > 0 ? 1u : 0u);
         if (more) {
           sk = it % L::kStages;
-          if (!(ok = wait_bar(kv_full(sk), (it / L::kStages) & 1, wc))) break;
+          if (!(ok = wait_bar_warp(kv_full(sk), (it / L::kStages) & 1, wc))) break;
           ++it;
           tc_fence_after();
-          issue_qk<D>(tm_s[0], q_addr(0), kv_addr(sk));
-          mma_commit(s_full(0));
+          issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk));
+          mma_commit_elect(s_full(0));
         } else {
-          mma_commit(o_done(0));
+          mma_commit_elect(o_done(0));
         }
         // Q tile 1: PV1_j, then S1_{j+1}
-        if (!(ok = wait_bar(p_full(1), j & 1, wc))) break;
+        if (!(ok = wait_bar_warp(p_full(1), j & 1, wc))) break;
         tc_fence_after();
-        issue_pv<D>(tm_o[1], p_addr(1), kv_addr(sv), j > 0);
-        mma_commit(kv_empty(sv));
+        issue_pv<D>(tm_o[1], tm_s[1], kv_vdesc(sv), j > 0 ? 1u : 0u);
+        mma_commit_elect(kv_empty(sv));
         if (more) {
-          issue_qk<D>(tm_s[1], q_addr(1), kv_addr(sk));
-          mma_commit(s_full(1));
-          mma_commit(kv_empty(sk));
+          issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk));
+          mma_commit_elect(s_full(1));
+          mma_commit_elect(kv_empty(sk));
         } else {
-          mma_commit(o_done(1));
+          mma_commit_elect(o_done(1));
         }
       }
       if (!ok) {  // wait for every MMA this thread issued
-        mma_commit(bar_drain);
-        wait_bar(bar_drain, 0, wc, false);
+        mma_commit_elect(bar_drain);
+        wait_bar_warp(bar_drain, 0, wc, false);
       }
     }
   } else {
@@ -350,7 +364,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t to = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_bits;
     const int row_first = r0 + t * kBlockM;   // first row of this Q tile (sequence coords)
     const int r = row_first + row_in_tile;
-    uint8_t* p_row = smem + L::kPOff + t * L::kPBytes + row_in_tile * 128;
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
@@ -362,15 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
-      uint32_t sa[64], sb[64];
-      tmem_ld_32x32b_x64(ts, sa);
-      tmem_ld_32x32b_x64(ts + 64, sb);
+      uint32_t sr[kBlockN];
+      tmem_ld_32x32b_x128(ts, sr);
       float s[kBlockN];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        s[c] = u2f(sa[c]);
-        s[c + 64] = u2f(sb[c]);
-      }
+      for (int c = 0; c < kBlockN; ++c) s[c] = u2f(sr[c]);
 
       const int key0 = j * kBlockN;
       const bool need_mask =
@@ -384,9 +393,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) s[c] = (c <= lim_c) ? s[c] : -INFINITY;
       }
-      float mx = s[0];
+      // Row max as 8 independent chains (a single chain would serialise 127 maxes).
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kBlockN; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_run, mx * sl2);
       const bool rescale = m_new > m_run + kRescaleThreshold;
       float alpha = 1.f;
@@ -396,25 +412,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_run *= alpha;
       const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      float rs = 0.f;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
 #pragma unroll
-      for (int ch = 0; ch < kBlockN / 8; ++ch) {  // 16-byte chunks of the P row
-        float p[8];
+      for (int half = 0; half < 2; ++half) {  // P as packed bf16 pairs over S's first 64 columns
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = ex2_approx(fmaf(s[ch * 8 + e], sl2, -msub));
-          rs += p[e];
+        for (int ch = 0; ch < 8; ++ch) {
+          float p[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            p[e] = ex2_approx(fmaf(s[half * 64 + ch * 8 + e], sl2, -msub));
+            rs8[e] += p[e];
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pk[ch * 4 + e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
         }
-        uint4 w;
-        w.x = pack_bf16x2(p[0], p[1]);
-        w.y = pack_bf16x2(p[2], p[3]);
-        w.z = pack_bf16x2(p[4], p[5]);
-        w.w = pack_bf16x2(p[6], p[7]);
-        const int kb = ch / 8;
-        const int c16 = (ch % 8) ^ (row_in_tile & 7);  // 128-byte swizzle
-        *reinterpret_cast<uint4*>(p_row + kb * kSwizzleAtom + c16 * 16) = w;
+        tmem_st_32x32b_x32(ts + half * 32, pk);
       }
-      l_run += rs;
+      l_run += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled, and
         // PV_t(j) is not issued before this warpgroup arrives on p_full.
@@ -428,9 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full(t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(t));  // one arrival per warp
     }
 
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(o_done(t), 0, wc));
