@@ -67,7 +67,7 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
 // out = 0, lse = -inf for every row (no keys at all).
 cudaError_t launch_fill_empty(const AttnProblem& p, cudaStream_t stream);
 // LSE merge.
-cudaError_t launch_merge(const MergeProblem& p, cudaStream_t stream);
+cudaError_t launch_merge(const MergeProblem& p, const DeviceCtl& ctl, cudaStream_t stream);
 // Diagnostic bounded wait on a barrier that never completes.
 cudaError_t launch_bounded_wait_diag(const DeviceCtl& ctl, cudaStream_t stream);
 

@@ -4,9 +4,11 @@
 // Per output row (b, m, h):  M* = max_c lse_c,  LSE = M* + ln sum_c exp(lse_c - M*),
 // out = sum_c exp(lse_c - LSE) out_c; every chunk -inf -> out = 0, LSE = -inf.
 //
-// HBM-bound: one warp per row, rows ordered (b, h, m) so a block's lse reads are
-// contiguous; each lane reads 16-byte float4 pieces of every chunk row (a 512-byte row
-// per warp instruction at Kv = 128) with up to 8 chunk loads in flight per lane.
+// HBM-bound: one warp per row, rows ordered (b, m, h) so neighbouring warps read
+// neighbouring pieces of every chunk (sequential streams through each chunk); each lane
+// reads 16-byte float4 pieces of every chunk row (a 512-byte row per warp instruction at
+// Kv = 128), up to 8 chunks in flight per lane together with their lse, folded with a
+// running maximum.
 
 #include <cuda_bf16.h>
 
@@ -44,57 +46,69 @@ MSLK_DEV float4 ldg_f4(const float* p) {
   return r;
 }
 
+// G = chunks folded per memory round trip (2, 4 or 8): fewer for small n keeps the
+// registers low and the number of rows in flight per SM high.
+template <int G>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeArgs a) {
   const int lane = threadIdx.x % 32;
   const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + threadIdx.x / 32;
   if (row >= a.rows) return;
-  const int m = static_cast<int>(row % a.M);
-  const long long bh = row / a.M;
-  const int h = static_cast<int>(bh % a.H);
-  const int b = static_cast<int>(bh / a.H);
-  const long long lse_idx = bh * a.M + m;  // [B, H, M]
-
-  // Chunk weights, in base 2: w_c = 2^(log2e*lse_c - log2e*LSE).
-  float mstar = -INFINITY;
-  for (int c = lane; c < a.n; c += 32) mstar = fmaxf(mstar, a.lse_split[c * a.cs_lse + lse_idx]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, o));
-  const float msub2 = (mstar == -INFINITY) ? 0.f : mstar * kLog2e;
-  float sumw = 0.f;
-  for (int c = lane; c < a.n; c += 32)
-    sumw += ex2_approx(fmaf(a.lse_split[c * a.cs_lse + lse_idx], kLog2e, -msub2));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sumw += __shfl_xor_sync(0xffffffffu, sumw, o);
-  const bool empty = !(sumw > 0.f);
-  const float lse2 = msub2 + lg2_approx(sumw);  // log2e * LSE
-  const float inv_sum = empty ? 0.f : 1.f / sumw;
-
+  const int h = static_cast<int>(row % a.H);
+  const long long bm_ = row / a.H;
+  const int m = static_cast<int>(bm_ % a.M);
+  const int b = static_cast<int>(bm_ / a.M);
+  const long long lse_idx = (static_cast<long long>(b) * a.H + h) * a.M + m;  // [B, H, M]
   const float* src = a.out_split + b * a.ss_b + m * a.ss_m + h * a.ss_h;
+  const float* lsrc = a.lse_split + lse_idx;
+
   for (int d0 = lane * 4; d0 < a.Kv; d0 += 128) {
+    // Chunks are folded G at a time with a running maximum (all in base 2):
+    //   mx = max lse seen so far, sw = sum_c 2^(l2e*lse_c - mx), acc = sum_c 2^(...) out_c.
+    // A group's chunk rows and lse values are requested together (lane u fetches the lse
+    // of chunk u and shares it), so each group costs one memory round trip.
+    float mx = -INFINITY, sw = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < a.n; c0 += 8) {
-      float4 x[8];
-      float w[8];
+    for (int c0 = 0; c0 < a.n; c0 += G) {
+      float4 x[G];
+      const float* p = src + c0 * a.cs_out + d0;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int c = c0 + u;
-        if (c < a.n) {
-          x[u] = ldg_f4(src + c * a.cs_out + d0);
-          // exp(lse_c - LSE) = 2^(log2e lse_c - msub2) / sumw
-          w[u] = ex2_approx(fmaf(a.lse_split[c * a.cs_lse + lse_idx], kLog2e, -msub2)) * inv_sum;
-        } else {
-          x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          w[u] = 0.f;
-        }
+      for (int u = 0; u < G; ++u) {
+        x[u] = (c0 + u < a.n) ? ldg_f4(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+        p += a.cs_out;
       }
+      const float mine = (lane < G && c0 + lane < a.n) ? __ldg(lsrc + (c0 + lane) * a.cs_lse) * kLog2e
+                                                       : -INFINITY;
+      float l2[G];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x = fmaf(w[u], x[u].x, acc.x);
-        acc.y = fmaf(w[u], x[u].y, acc.y);
-        acc.z = fmaf(w[u], x[u].z, acc.z);
-        acc.w = fmaf(w[u], x[u].w, acc.w);
+      for (int u = 0; u < G; ++u) l2[u] = __shfl_sync(0xffffffffu, mine, u);
+      float bm = l2[0];
+#pragma unroll
+      for (int u = 1; u < G; ++u) bm = fmaxf(bm, l2[u]);
+      const float nm = fmaxf(mx, bm);
+      if (nm == -INFINITY) continue;  // every chunk so far is empty
+      const float r = ex2_approx(mx - nm);  // mx = -inf -> 0
+      sw *= r;
+      acc.x *= r;
+      acc.y *= r;
+      acc.z *= r;
+      acc.w *= r;
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+        const float wgt = ex2_approx(l2[u] - nm);  // empty chunk -> 0
+        sw += wgt;
+        acc.x = fmaf(wgt, x[u].x, acc.x);
+        acc.y = fmaf(wgt, x[u].y, acc.y);
+        acc.z = fmaf(wgt, x[u].z, acc.z);
+        acc.w = fmaf(wgt, x[u].w, acc.w);
       }
+      mx = nm;
     }
+    const bool empty = !(sw > 0.f);
+    const float inv = empty ? 0.f : 1.f / sw;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
     if (a.out_fp32) {
       float* o = static_cast<float*>(a.out) + b * a.so_b + m * a.so_m + h * a.so_h + d0;
       *reinterpret_cast<float4*>(o) = acc;
@@ -102,13 +116,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeA
       __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + b * a.so_b + m * a.so_m + h * a.so_h + d0;
       *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
     }
+    if (d0 == 0 && a.lse != nullptr) a.lse[lse_idx] = empty ? -INFINITY : (mx + lg2_approx(sw)) * kLn2;
   }
-  if (lane == 0 && a.lse != nullptr) a.lse[lse_idx] = empty ? -INFINITY : lse2 * kLn2;
 }
 
 }  // namespace
 
-cudaError_t launch_merge(const MergeProblem& p, cudaStream_t stream) {
+cudaError_t launch_merge(const MergeProblem& p, const DeviceCtl& ctl, cudaStream_t stream) {
+  (void)ctl;  // no waits in this kernel
   MergeArgs a{};
   a.out_split = p.out_split;
   a.lse_split = p.lse_split;
@@ -129,9 +144,14 @@ cudaError_t launch_merge(const MergeProblem& p, cudaStream_t stream) {
   a.so_h = p.so.h;
   a.lse = p.lse;
   a.rows = static_cast<long long>(p.B) * p.H * p.M;
+  if (a.rows == 0) return cudaSuccess;
   const long long blocks = (a.rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  if (blocks == 0) return cudaSuccess;
-  merge_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+  if (a.n <= 2)
+    merge_kernel<2><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+  else if (a.n <= 4)
+    merge_kernel<4><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+  else
+    merge_kernel<8><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -292,7 +292,9 @@ mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split
   p.out = out;
   p.out_fp32 = out_fp32;
   p.lse = lse;
-  const cudaError_t e = launch_merge(p, static_cast<cudaStream_t>(stream));
+  const DeviceCtl ctl = device_ctl();
+  if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "%s: no CUDA device / module", who);
+  const cudaError_t e = launch_merge(p, ctl, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
   return ok();
 }

@@ -59,6 +59,24 @@ MSLK_DEV void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int32_t 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes on `bar`.
+// Both addresses 16-byte aligned, size a multiple of 16.
+MSLK_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// 16-byte asynchronous copy global -> shared by this thread (bypassing L1), grouped with
+// cp.async.commit_group and awaited per thread with cp.async.wait_group.
+MSLK_DEV void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+MSLK_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+MSLK_DEV void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
 // (tcgen05.mma operands written with st.shared).
 MSLK_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
