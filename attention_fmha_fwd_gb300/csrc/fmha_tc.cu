@@ -7,7 +7,10 @@
 // as in MSLK's memory_efficient_attention ("Attention - Core fMHA"), streaming K/V in
 // 128-key tiles so the score matrix never leaves the SM.
 //
-// Per CTA (320 threads, one CTA per SM):
+// Persistent: one CTA per SM walks a static list of units (heavy-first, snake-assigned);
+// barrier phases carry across units, so the next unit's Q/K/V loads and first MMAs
+// overlap the current unit's last tiles and epilogue.
+// Per CTA (320 threads):
 //   warps 0-3   softmax for Q tile 0 (thread t owns row t = TMEM lane t)
 //   warps 4-7   softmax for Q tile 1
 //   warp  8     tcgen05.mma issue (one thread) + TMEM allocation
@@ -38,9 +41,11 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -65,12 +70,16 @@ template <int D>
 struct Layout {
   static constexpr int kKBlocks = D / 64;
   static constexpr int kTileBytes = kBlockM * D * 2;  // Q, K or V tile (128 rows)
-  static constexpr int kStages = (D == 128) ? 5 : 8;
+  static constexpr int kStages = (D == 128) ? 4 : 8;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
-  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 6 + 1;
+  // Output staging: one 16 KiB buffer per softmax warpgroup (128 rows x 128 bytes, the
+  // 128-byte-swizzled layout of one TMA store box).
+  static constexpr int kStageOutBytes = kBlockM * 128;
+  static constexpr int kOutOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kOutOff + kQTiles * kStageOutBytes;
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], o_free[2], drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // abort flag, tmem slot
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
@@ -78,6 +87,8 @@ struct Layout {
 
 struct TcArgs {
   int M, Mkv, H;
+  int Z;            // batches, or packed sequences
+  int total_units;  // units_m * H * Z
   int hk_shared;
   int causal, varlen;
   int units_m;
@@ -89,6 +100,7 @@ struct TcArgs {
   int out_fp32;
   long long so_b, so_m, so_h;
   float* lse;
+  int tma_store;    // 1: write output tiles through shared memory with TMA stores
   unsigned int* err;
   unsigned long long timeout_ns;
 };
@@ -159,78 +171,92 @@ MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32
                      idesc, kk > 0 ? 1u : accumulate);
 }
 
+// One work unit: 256 query rows of one (batch or packed sequence, head).
+struct Unit {
+  int b, h, hk;
+  int q_base, Lq, k_base, Lk;
+  int r0;
+  int n_tiles;  // key tiles of the unit (= of Q tile 1)
+  int n0;       // key tiles Q tile 0 needs (fewer under a causal mask); n0 <= n_tiles
+};
+
+// Unit i of the heavy-first order: unit rows descend level by level (causal units late in
+// the sequence see the most keys), heads vary fastest within a level.  Returns false if
+// the unit has no rows (a packed sequence shorter than the unit's first row).
+MSLK_DEV bool decode_unit(const TcArgs& a, int i, Unit& u) {
+  const int per_level = a.H * a.Z;
+  const int level = i / per_level;
+  const int rem = i - level * per_level;
+  const int unit_m = a.units_m - 1 - level;
+  u.h = rem % a.H;
+  const int z = rem / a.H;
+  u.hk = a.hk_shared ? 0 : u.h;
+  if (a.varlen) {
+    u.b = 0;
+    const int qs = min(max(a.cu_q[z], 0), a.M);
+    const int qe = min(max(a.cu_q[z + 1], qs), a.M);
+    const int ks = min(max(a.cu_k[z], 0), a.Mkv);
+    const int ke = min(max(a.cu_k[z + 1], ks), a.Mkv);
+    u.q_base = qs;
+    u.Lq = qe - qs;
+    u.k_base = ks;
+    u.Lk = ke - ks;
+  } else {
+    u.b = z;
+    u.q_base = 0;
+    u.Lq = a.M;
+    u.k_base = 0;
+    u.Lk = a.Mkv;
+  }
+  u.r0 = unit_m * kUnitRows;
+  if (u.r0 >= u.Lq) return false;
+  u.n_tiles = (u.Lk + kBlockN - 1) / kBlockN;
+  u.n0 = u.n_tiles;
+  if (a.causal) {
+    const long long all = u.n_tiles;
+    const long long last_row = min(u.r0 + kUnitRows - 1, u.Lq - 1);
+    const long long kmax = last_row - a.kv_offset;  // last allowed key of the unit
+    u.n_tiles = kmax < 0 ? 0 : static_cast<int>(min(all, kmax / kBlockN + 1));
+    const long long last0 = min(u.r0 + kBlockM - 1, u.Lq - 1);
+    const long long kmax0 = last0 - a.kv_offset;  // last allowed key of Q tile 0
+    u.n0 = kmax0 < 0 ? 0 : static_cast<int>(min(all, kmax0 / kBlockN + 1));
+  }
+  return true;
+}
+
+// Static schedule over the heavy-first order, in snake rounds: CTA c takes position c of
+// even rounds and position G-1-c of odd rounds, which evens out the per-CTA work.
+MSLK_DEV int unit_at(int round, int c, int G) {
+  return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const TcArgs a) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const TcArgs a) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-
-  // ---------------------------------------------------------------- work unit
-  const int unit = a.units_m - 1 - static_cast<int>(blockIdx.x);  // late (heavy) rows first
-  const int h = blockIdx.y;
-  const int z = blockIdx.z;
-  int b, q_base, Lq, k_base, Lk;
-  if (a.varlen) {
-    b = 0;
-    const int qs = min(max(a.cu_q[z], 0), a.M);
-    const int qe = min(max(a.cu_q[z + 1], qs), a.M);
-    const int ks = min(max(a.cu_k[z], 0), a.Mkv);
-    const int ke = min(max(a.cu_k[z + 1], ks), a.Mkv);
-    q_base = qs;
-    Lq = qe - qs;
-    k_base = ks;
-    Lk = ke - ks;
-  } else {
-    b = z;
-    q_base = 0;
-    Lq = a.M;
-    k_base = 0;
-    Lk = a.Mkv;
-  }
-  const int r0 = unit * kUnitRows;
-  if (r0 >= Lq) return;
-  int n_tiles = (Lk + kBlockN - 1) / kBlockN;
-  if (a.causal) {
-    const long long last_row = min(r0 + kUnitRows - 1, Lq - 1);
-    const long long kmax = last_row - a.kv_offset;  // last allowed key of the unit
-    n_tiles = kmax < 0 ? 0 : static_cast<int>(min(static_cast<long long>(n_tiles), kmax / kBlockN + 1));
-  }
-  const int hk = a.hk_shared ? 0 : h;
-
-  if (n_tiles == 0) {  // no allowed key for any row of the unit
-    const int rows = min(kUnitRows, Lq - r0);
-    for (int idx = threadIdx.x; idx < rows * (D / 4); idx += kThreads) {
-      const long long row = q_base + r0 + idx / (D / 4);
-      const int c = (idx % (D / 4)) * 4;
-      if (a.out_fp32) {
-        float* o = static_cast<float*>(a.out) + b * a.so_b + row * a.so_m + h * a.so_h + c;
-        *reinterpret_cast<float4*>(o) = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + b * a.so_b + row * a.so_m + h * a.so_h + c;
-        *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
-      }
-    }
-    if (a.lse != nullptr)
-      for (int r = threadIdx.x; r < rows; r += kThreads)
-        a.lse[(static_cast<long long>(b) * a.H + h) * a.M + q_base + r0 + r] = -INFINITY;
-    return;
-  }
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+  const int n_rounds = (a.total_units + G - 1) / G;
 
   // ---------------------------------------------------------------- setup
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t bar_q = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + L::kStages + s); };
-  auto s_full = [&](int t) { return bar0 + 8u * (1 + 2 * L::kStages + t); };
-  auto p_full = [&](int t) { return bar0 + 8u * (3 + 2 * L::kStages + t); };
-  auto o_done = [&](int t) { return bar0 + 8u * (5 + 2 * L::kStages + t); };
-  const uint32_t bar_drain = bar0 + 8u * (7 + 2 * L::kStages);
+  const uint32_t q_full = bar0;
+  const uint32_t q_empty = bar0 + 8u;
+  auto kv_full = [&](int s) { return bar0 + 8u * (2 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (2 + L::kStages + s); };
+  auto s_full = [&](int t) { return bar0 + 8u * (2 + 2 * L::kStages + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (4 + 2 * L::kStages + t); };
+  auto o_done = [&](int t) { return bar0 + 8u * (6 + 2 * L::kStages + t); };
+  auto o_free = [&](int t) { return bar0 + 8u * (8 + 2 * L::kStages + t); };
+  const uint32_t bar_drain = bar0 + 8u * (10 + 2 * L::kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff + 8);
   const WaitCtl wc{abort_flag, a.err, a.timeout_ns};
@@ -240,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto kv_addr = [&](int s) { return s_base + L::kKVOff + s * L::kTileBytes; };
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
@@ -249,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_full(t), 1);
       mbar_init(p_full(t), kBlockM / 32);  // one arrival per softmax warp
       mbar_init(o_done(t), 1);
+      mbar_init(o_free(t), kBlockM / 32);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -258,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    if (a.tma_store) tma_prefetch_desc(&tm_o);
   }
   if (warp == kWarpMma) {
     __syncwarp();
@@ -271,74 +300,103 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer (whole warp)
-    mbar_arrive_expect_tx_elect(bar_q, kQTiles * L::kTileBytes);
-    for (int t = 0; t < kQTiles; ++t)
-      for (int kb = 0; kb < L::kKBlocks; ++kb)
-        tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, bar_q, kb * 64,
-                          q_base + r0 + t * kBlockM, h, b);
-    int it = 0;
-    bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      for (int which = 0; which < 2; ++which, ++it) {  // K_j then V_j
-        const int s = it % L::kStages;
-        if (!(ok = wait_bar_warp(kv_empty(s), ((it / L::kStages) & 1) ^ 1, wc))) break;
-        mbar_arrive_expect_tx_elect(kv_full(s), L::kTileBytes);
-        const CUtensorMap* tm = which ? &tm_v : &tm_k;
+    int uc = 0, it = 0;
+    bool ok = true, q_pending = false;
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int i = unit_at(k, cta, G);
+      Unit u;
+      if (i >= a.total_units || !decode_unit(a, i, u) || u.n_tiles == 0) continue;
+      // Q of this unit may overwrite the previous unit's Q once its last S MMA was issued.
+      if (!(ok = wait_bar_warp(q_empty, (uc & 1) ^ 1, wc))) break;
+      mbar_arrive_expect_tx_elect(q_full, kQTiles * L::kTileBytes);
+      for (int t = 0; t < kQTiles; ++t)
         for (int kb = 0; kb < L::kKBlocks; ++kb)
-          tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64,
-                            k_base + j * kBlockN, hk, b);
+          tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, q_full, kb * 64,
+                            u.q_base + u.r0 + t * kBlockM, u.h, u.b);
+      q_pending = true;
+      for (int j = 0; j < u.n_tiles && ok; ++j) {
+        for (int which = 0; which < 2; ++which, ++it) {  // K_j then V_j
+          const int s = it % L::kStages;
+          if (!(ok = wait_bar_warp(kv_empty(s), ((it / L::kStages) & 1) ^ 1, wc))) break;
+          mbar_arrive_expect_tx_elect(kv_full(s), L::kTileBytes);
+          const CUtensorMap* tm = which ? &tm_v : &tm_k;
+          for (int kb = 0; kb < L::kKBlocks; ++kb)
+            tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64,
+                              u.k_base + j * kBlockN, u.hk, u.b);
+        }
+      }
+      if (ok) {
+        ++uc;
+        q_pending = false;
       }
     }
     if (!ok) {  // let every copy this warp issued land before the CTA exits
-      wait_bar_warp(bar_q, 0, wc, false);
+      if (q_pending) wait_bar_warp(q_full, uc & 1, wc, false);
       for (int k = max(0, it - L::kStages); k < it; ++k)
         wait_bar_warp(kv_full(k % L::kStages), (k / L::kStages) & 1, wc, false);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer (whole warp)
-    {
-      const uint32_t tm_s[2] = {tmem + 0u, tmem + 128u};
-      const uint32_t tm_o[2] = {tmem + 256u, tmem + 384u};
-      const uint64_t q_desc[2] = {desc_kmajor(q_addr(0)), desc_kmajor(q_addr(1))};
-      // Ring stages are kTileBytes apart: stage s adds s * kTileBytes / 16 to the address field.
-      const uint64_t kdesc0 = desc_kmajor(kv_addr(0));
-      const uint64_t vdesc0 = desc_mnmajor(kv_addr(0));
-      auto kv_kdesc = [&](int st) { return kdesc0 + static_cast<uint32_t>(st * (L::kTileBytes >> 4)); };
-      auto kv_vdesc = [&](int st) { return vdesc0 + static_cast<uint32_t>(st * (L::kTileBytes >> 4)); };
-      bool ok = wait_bar_warp(bar_q, 0, wc);
-      int it = 0;
-      if (ok) ok = wait_bar_warp(kv_full(0), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(0));
+    const uint32_t tm_s[2] = {tmem + 0u, tmem + 128u};
+    const uint32_t tm_o[2] = {tmem + 256u, tmem + 384u};
+    const uint64_t q_desc[2] = {desc_kmajor(q_addr(0)), desc_kmajor(q_addr(1))};
+    // Ring stages are kTileBytes apart: stage s adds s * kTileBytes / 16 to the address field.
+    const uint64_t kdesc0 = desc_kmajor(kv_addr(0));
+    const uint64_t vdesc0 = desc_mnmajor(kv_addr(0));
+    auto kv_kdesc = [&](int st) { return kdesc0 + static_cast<uint32_t>(st * (L::kTileBytes >> 4)); };
+    auto kv_vdesc = [&](int st) { return vdesc0 + static_cast<uint32_t>(st * (L::kTileBytes >> 4)); };
+    // uc: units; uc_t / jg_t: units and key tiles of Q tile t (its barrier phases).
+    int uc = 0, it = 0, uc0 = 0, uc1 = 0, jg0 = 0, jg1 = 0;
+    bool ok = true;
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int i = unit_at(k, cta, G);
+      Unit u;
+      if (i >= a.total_units || !decode_unit(a, i, u) || u.n_tiles == 0) continue;
+      const int n = u.n_tiles;
+      const int n0 = u.n0;
+      if (!(ok = wait_bar_warp(q_full, uc & 1, wc))) break;
+      const int sk0 = it % L::kStages;
+      if (!(ok = wait_bar_warp(kv_full(sk0), (it / L::kStages) & 1, wc))) break;
+      ++it;
+      tc_fence_after();
+      // S_t(0): S_t is free (its last P was consumed by the previous unit's PV_t, which
+      // was issued before this and executes first).
+      if (n0 > 0) {
+        issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk0));
         mma_commit_elect(s_full(0));
-        issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(0));
-        mma_commit_elect(s_full(1));
-        mma_commit_elect(kv_empty(0));
-        it = 1;
       }
-      for (int j = 0; j < n_tiles && ok; ++j) {
+      issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk0));
+      mma_commit_elect(s_full(1));
+      mma_commit_elect(kv_empty(sk0));
+      if (n == 1) mma_commit_elect(q_empty);
+      for (int j = 0; j < n && ok; ++j) {
         const int sv = it % L::kStages;
         if (!(ok = wait_bar_warp(kv_full(sv), (it / L::kStages) & 1, wc))) break;
         ++it;
-        const bool more = j + 1 < n_tiles;
+        const bool more = j + 1 < n;
         int sk = 0;
-        // Q tile 0: PV0_j, then S0_{j+1}
-        if (!(ok = wait_bar_warp(p_full(0), j & 1, wc))) break;
-        tc_fence_after();
-        issue_pv<D>(tm_o[0], tm_s[0], kv_vdesc(sv), j > 0 ? 1u : 0u);
+        // Q tile 0 (only while its rows still see keys): PV0_j, then S0_{j+1}
+        if (j < n0) {
+          if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
+          if (j == 0 && !(ok = wait_bar_warp(o_free(0), (uc0 & 1) ^ 1, wc))) break;
+          tc_fence_after();
+          issue_pv<D>(tm_o[0], tm_s[0], kv_vdesc(sv), j > 0 ? 1u : 0u);
+          if (j == n0 - 1) mma_commit_elect(o_done(0));
+          ++jg0;
+        }
         if (more) {
           sk = it % L::kStages;
           if (!(ok = wait_bar_warp(kv_full(sk), (it / L::kStages) & 1, wc))) break;
           ++it;
           tc_fence_after();
-          issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk));
-          mma_commit_elect(s_full(0));
-        } else {
-          mma_commit_elect(o_done(0));
+          if (j + 1 < n0) {
+            issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk));
+            mma_commit_elect(s_full(0));
+          }
         }
         // Q tile 1: PV1_j, then S1_{j+1}
-        if (!(ok = wait_bar_warp(p_full(1), j & 1, wc))) break;
+        if (!(ok = wait_bar_warp(p_full(1), jg1 & 1, wc))) break;
+        if (j == 0 && !(ok = wait_bar_warp(o_free(1), (uc1 & 1) ^ 1, wc))) break;
         tc_fence_after();
         issue_pv<D>(tm_o[1], tm_s[1], kv_vdesc(sv), j > 0 ? 1u : 0u);
         mma_commit_elect(kv_empty(sv));
@@ -346,14 +404,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk));
           mma_commit_elect(s_full(1));
           mma_commit_elect(kv_empty(sk));
+          if (j + 2 == n) mma_commit_elect(q_empty);  // the unit's last S MMA was issued
         } else {
           mma_commit_elect(o_done(1));
         }
+        ++jg1;
       }
-      if (!ok) {  // wait for every MMA this thread issued
-        mma_commit_elect(bar_drain);
-        wait_bar_warp(bar_drain, 0, wc, false);
+      if (ok) {
+        ++uc;
+        ++uc1;
+        if (n0 > 0) ++uc0;
       }
+    }
+    if (!ok) {  // wait for every MMA this warp issued
+      mma_commit_elect(bar_drain);
+      wait_bar_warp(bar_drain, 0, wc, false);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -362,135 +427,258 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_bits = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t ts = tmem + static_cast<uint32_t>(t * 128) + lane_bits;
     const uint32_t to = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_bits;
-    const int row_first = r0 + t * kBlockM;   // first row of this Q tile (sequence coords)
-    const int r = row_first + row_in_tile;
     const float sl2 = a.scale_log2;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
+    int uc = 0, jg = 0;
     bool ok = true;
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int i = unit_at(k, cta, G);
+      Unit u;
+      if (i >= a.total_units || !decode_unit(a, i, u)) continue;
+      const int row_first = u.r0 + t * kBlockM;  // first row of this Q tile (sequence coords)
+      const int r = row_first + row_in_tile;
+      const bool valid = r < u.Lq;
+      const long long row = static_cast<long long>(u.q_base) + r;
+      const int n_t = (t == 0) ? u.n0 : u.n_tiles;  // key tiles this Q tile sees
+      if (n_t == 0) {  // no allowed key for any row of this Q tile
+        if (valid) {
+          for (int c = 0; c < D; c += 4) {
+            if (a.out_fp32) {
+              float* o = static_cast<float*>(a.out) + u.b * a.so_b + row * a.so_m + u.h * a.so_h + c;
+              *reinterpret_cast<float4*>(o) = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+              __nv_bfloat16* o =
+                  static_cast<__nv_bfloat16*>(a.out) + u.b * a.so_b + row * a.so_m + u.h * a.so_h + c;
+              *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
+            }
+          }
+          if (a.lse != nullptr) a.lse[(static_cast<long long>(u.b) * a.H + u.h) * a.M + row] = -INFINITY;
+        }
+        continue;
+      }
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      for (int j = 0; j < n_t; ++j, ++jg) {
+        // tcgen05.ld is warp-collective: take every wait decision warp-uniformly.
+        ok = __all_sync(0xffffffffu, wait_bar(s_full(t), jg & 1, wc));
+        if (!ok) break;
+        __syncwarp();
+        tc_fence_after();
+        const int key0 = j * kBlockN;
+        const bool need_mask =
+            (key0 + kBlockN > u.Lk) || (a.causal && (a.kv_offset + key0 + kBlockN - 1 > row_first));
+        // Column c of this tile is allowed iff c <= lim_c (key < Lk, and for causal masks
+        // kv_offset + key <= r); lim_c = 127 when the whole tile is allowed.
+        int lim_c = kBlockN - 1;
+        if (need_mask) {
+          long long lim = static_cast<long long>(u.Lk) - 1 - key0;
+          if (a.causal) lim = min(lim, static_cast<long long>(r) - a.kv_offset - key0);
+          lim_c = static_cast<int>(max(-1LL, min(lim, static_cast<long long>(kBlockN - 1))));
+        }
+        // Two passes over the S row in tensor memory: pass 1 takes the row max, pass 2
+        // forms p = 2^(s*scale*log2e - m) (bf16, packed in pairs over S's first 64
+        // columns; quarter q of P lands in columns [16q, 16q+16), all of which pass 2 has
+        // already read) and the row sum.  Interior tiles (every column allowed) run fully
+        // unrolled code; tiles crossing a mask limit classify 32/64-column bands
+        // warp-uniformly so only the band(s) holding a row's limit test each column.
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+        if (!need_mask) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t sr[64];
+            tmem_ld_32x32b_x64(ts + half * 64, sr);
+#pragma unroll
+            for (int c = 0; c < 64; c += 16)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], u2f(sr[c + e]), u2f(sr[c + 8 + e]));
+          }
+        } else {
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            const int c0 = half * 64;
+            if (__all_sync(0xffffffffu, lim_c < c0)) continue;
+            uint32_t sr[64];
+            tmem_ld_32x32b_x64(ts + c0, sr);
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c0 + c > lim_c) sr[c] = 0xFF800000u;  // -inf
+#pragma unroll
+            for (int c = 0; c < 64; c += 16)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], u2f(sr[c + e]), u2f(sr[c + 8 + e]));
+          }
+        }
+        const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7])));
+        const float m_new = fmaxf(m_run, mx * sl2);
+        const bool rescale = m_new > m_run + kRescaleThreshold;
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = ex2_approx(m_run - m_new);
+          m_run = m_new;
+        }
+        l_run *= alpha;
+        const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+        float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
+        // p for 32 columns (in sr) -> 16 packed bf16 pairs
+        const uint64_t sl2x2 = pack_f2(sl2, sl2);
+        const uint64_t nmx2 = pack_f2(-msub, -msub);
+        auto exp_band = [&](const uint32_t (&sr)[32], uint32_t (&pk)[16]) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[2 * e]), u2f(sr[2 * e + 1])), sl2x2, nmx2));
+            const float p0 = ex2_approx(x.x);
+            const float p1 = ex2_approx(x.y);
+            rs8[(2 * e) % 8] += p0;
+            rs8[(2 * e + 1) % 8] += p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+        };
+        if (!need_mask) {
+#pragma unroll
+          for (int qtr = 0; qtr < 4; ++qtr) {
+            uint32_t sr[32], pk[16];
+            tmem_ld_32x32b_x32(ts + qtr * 32, sr);
+            exp_band(sr, pk);
+            tmem_st_32x32b_x16(ts + qtr * 16, pk);
+          }
+        } else {
+#pragma unroll 1
+          for (int qtr = 0; qtr < 4; ++qtr) {
+            const int c0 = qtr * 32;
+            uint32_t sr[32], pk[16];
+            if (__all_sync(0xffffffffu, lim_c < c0)) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pk[e] = 0u;
+            } else {
+              tmem_ld_32x32b_x32(ts + c0, sr);
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (c0 + c > lim_c) sr[c] = 0xFF800000u;  // -inf: 2^-inf = 0
+              exp_band(sr, pk);
+            }
+            tmem_st_32x32b_x16(ts + qtr * 16, pk);
+          }
+        }
+        l_run += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled, and
+          // PV_t(j) is not issued before this warpgroup arrives on p_full.
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(to + c0, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * alpha);
+            tmem_st_32x32b_x32(to + c0, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(t));  // one arrival per warp
+      }
+      if (!ok) break;
 
-    for (int j = 0; j < n_tiles; ++j) {
-      // tcgen05.ld is warp-collective: take every wait decision warp-uniformly.
-      ok = __all_sync(0xffffffffu, wait_bar(s_full(t), j & 1, wc));
+      // ---- epilogue: wait for the unit's last PV_t, read O_t, hand it back, then store.
+      ok = __all_sync(0xffffffffu, wait_bar(o_done(t), uc & 1, wc));
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
-      uint32_t sr[kBlockN];
-      tmem_ld_32x32b_x128(ts, sr);
-      float s[kBlockN];
-#pragma unroll
-      for (int c = 0; c < kBlockN; ++c) s[c] = u2f(sr[c]);
-
-      const int key0 = j * kBlockN;
-      const bool need_mask =
-          (key0 + kBlockN > Lk) || (a.causal && (a.kv_offset + key0 + kBlockN - 1 > row_first));
-      if (need_mask) {
-        // Column c of this tile is allowed iff c <= lim (key < Lk, and for causal masks
-        // kv_offset + key <= r).
-        long long lim = static_cast<long long>(Lk) - 1 - key0;
-        if (a.causal) lim = min(lim, static_cast<long long>(r) - a.kv_offset - key0);
-        const int lim_c = static_cast<int>(max(-1LL, min(lim, static_cast<long long>(kBlockN))));
-#pragma unroll
-        for (int c = 0; c < kBlockN; ++c) s[c] = (c <= lim_c) ? s[c] : -INFINITY;
-      }
-      // Row max as 8 independent chains (a single chain would serialise 127 maxes).
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < kBlockN; c += 8)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const bool rescale = m_new > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = ex2_approx(m_run - m_new);
-        m_run = m_new;
-      }
-      l_run *= alpha;
-      const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // P as packed bf16 pairs over S's first 64 columns
-        uint32_t pk[32];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          float p[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            p[e] = ex2_approx(fmaf(s[half * 64 + ch * 8 + e], sl2, -msub));
-            rs8[e] += p[e];
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) pk[ch * 4 + e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
-        }
-        tmem_st_32x32b_x32(ts + half * 32, pk);
-      }
-      l_run += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled, and
-        // PV_t(j) is not issued before this warpgroup arrives on p_full.
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(to + c0, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-          tmem_st_32x32b_x32(to + c0, o);
-        }
-        tmem_st_wait();
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(t));  // one arrival per warp
-    }
-
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(o_done(t), 0, wc));
-    if (ok) {
-      __syncwarp();
-      tc_fence_after();
-      const bool valid = r < Lq;
       const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      const long long row = static_cast<long long>(q_base) + r;
+      // Output tiles go through this warpgroup's staging buffer and one TMA store per
+      // 128-byte column band, except the tail tile of a packed sequence (a whole 128-row
+      // box would spill into the next sequence), which is stored row by row.
+      const bool use_tma = a.tma_store && !(a.varlen && row_first + kBlockM > u.Lq);
+      const bool leader = (warp % 4) == 0 && lane == 0;
+      uint8_t* stage = smem + L::kOutOff + t * L::kStageOutBytes + row_in_tile * 128;
+      const uint32_t stage_base = s_base + L::kOutOff + t * L::kStageOutBytes;
+      if (a.out_fp32) {
+        // 4-byte outputs: bands of 32 columns
+#pragma unroll 1
+        for (int band = 0; band < D / 32; ++band) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(to + band * 32, o);
+          if (band == D / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
+          }
+          if (use_tma) {
+            if (leader) bulk_wait_read0();  // the previous band's store has read the buffer
+            named_bar_sync(1 + t, kBlockM);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(to + c0, o);
-        float x[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = u2f(o[i]) * inv_l;
-        if (valid) {
-          if (a.out_fp32) {
-            float* op = static_cast<float*>(a.out) + b * a.so_b + row * a.so_m + h * a.so_h + c0;
+            for (int c = 0; c < 32; c += 4) {
+              const int chunk = (c / 4) ^ (row_in_tile & 7);  // 128-byte swizzle
+              *reinterpret_cast<float4*>(stage + chunk * 16) =
+                  make_float4(u2f(o[c]) * inv_l, u2f(o[c + 1]) * inv_l, u2f(o[c + 2]) * inv_l,
+                              u2f(o[c + 3]) * inv_l);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + t, kBlockM);
+            if (leader) {
+              tma_store_4d(&tm_o, stage_base, band * 32, u.q_base + row_first, u.h, u.b);
+              bulk_commit();
+            }
+          } else if (valid) {
+            float* op = static_cast<float*>(a.out) + u.b * a.so_b + row * a.so_m + u.h * a.so_h + band * 32;
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(op + c) = make_float4(x[c], x[c + 1], x[c + 2], x[c + 3]);
-          } else {
-            __nv_bfloat16* op =
-                static_cast<__nv_bfloat16*>(a.out) + b * a.so_b + row * a.so_m + h * a.so_h + c0;
+              *reinterpret_cast<float4*>(op + c) =
+                  make_float4(u2f(o[c]) * inv_l, u2f(o[c + 1]) * inv_l, u2f(o[c + 2]) * inv_l,
+                              u2f(o[c + 3]) * inv_l);
+          }
+        }
+      } else {
+        // bf16 outputs: bands of 64 columns
+#pragma unroll 1
+        for (int band = 0; band < D / 64; ++band) {
+          uint32_t o[64];
+          tmem_ld_32x32b_x64(to + band * 64, o);
+          if (band == D / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
+          }
+          uint4 w[8];
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              uint4 w;
-              w.x = pack_bf16x2(x[c], x[c + 1]);
-              w.y = pack_bf16x2(x[c + 2], x[c + 3]);
-              w.z = pack_bf16x2(x[c + 4], x[c + 5]);
-              w.w = pack_bf16x2(x[c + 6], x[c + 7]);
-              *reinterpret_cast<uint4*>(op + c) = w;
+          for (int c = 0; c < 64; c += 8) {
+            w[c / 8].x = pack_bf16x2(u2f(o[c]) * inv_l, u2f(o[c + 1]) * inv_l);
+            w[c / 8].y = pack_bf16x2(u2f(o[c + 2]) * inv_l, u2f(o[c + 3]) * inv_l);
+            w[c / 8].z = pack_bf16x2(u2f(o[c + 4]) * inv_l, u2f(o[c + 5]) * inv_l);
+            w[c / 8].w = pack_bf16x2(u2f(o[c + 6]) * inv_l, u2f(o[c + 7]) * inv_l);
+          }
+          if (use_tma) {
+            if (leader) bulk_wait_read0();  // the previous band's store has read the buffer
+            named_bar_sync(1 + t, kBlockM);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(stage + ((ch ^ (row_in_tile & 7)) * 16)) = w[ch];
+            fence_proxy_async_smem();
+            named_bar_sync(1 + t, kBlockM);
+            if (leader) {
+              tma_store_4d(&tm_o, stage_base, band * 64, u.q_base + row_first, u.h, u.b);
+              bulk_commit();
             }
+          } else if (valid) {
+            __nv_bfloat16* op =
+                static_cast<__nv_bfloat16*>(a.out) + u.b * a.so_b + row * a.so_m + u.h * a.so_h + band * 64;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) *reinterpret_cast<uint4*>(op + ch * 8) = w[ch];
           }
         }
       }
-      if (valid && a.lse != nullptr)
-        a.lse[(static_cast<long long>(b) * a.H + h) * a.M + row] =
-            (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
+      if (valid) {
+        if (a.lse != nullptr)
+          a.lse[(static_cast<long long>(u.b) * a.H + u.h) * a.M + row] =
+              (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
+      }
+      ++uc;
     }
   }
 
   // ---------------------------------------------------------------- teardown
+  if (warp < 8 && (warp % 4) == 0 && lane == 0) bulk_wait0();  // output stores complete
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -499,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 }
+
 
 // ------------------------------------------------------------------ host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -543,6 +732,41 @@ bool encode_bhmd(EncodeTiledFn enc, CUtensorMap* map, const void* base, int D, l
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int num_sms() {
+  constexpr int kMaxDevices = 64;
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+// Output [batch, rows, heads, D] (bf16 or fp32) for TMA stores of 128-byte column bands.
+bool encode_out(EncodeTiledFn enc, CUtensorMap* map, void* base, bool fp32, int D, long long rows,
+                long long heads, long long batch, long long s_m, long long s_h, long long s_b) {
+  const long long elt = fp32 ? 4 : 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
+  long long st_m = s_m * elt;
+  long long st_h = heads > 1 ? s_h * elt : st_m * rows;
+  long long st_b = batch > 1 ? s_b * elt : st_h * heads;
+  if (rows == 1) st_m = 16;
+  if (st_h <= 0 || st_h % 16) st_h = 16;
+  if (st_b <= 0 || st_b % 16) st_b = 16;
+  if (st_m <= 0 || st_m % 16) return false;
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st_m), static_cast<cuuint64_t>(st_h),
+                           static_cast<cuuint64_t>(st_b)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), kBlockM, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
                      const char** why) {
@@ -560,6 +784,9 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
     *why = "cuTensorMapEncodeTiled rejected a q/k/v layout";
     return cudaErrorInvalidValue;
   }
+  // Output tiles: bands of 128 bytes (64 bf16 / 32 fp32 columns) x 128 rows.
+  CUtensorMap to{};
+  const bool tma_store = encode_out(enc, &to, p.out, p.out_fp32, D, p.M, p.H, p.B, p.so.m, p.so.h, p.so.b);
   TcArgs a{};
   a.M = p.M;
   a.Mkv = p.Mkv;
@@ -579,17 +806,26 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.so_m = p.so.m;
   a.so_h = p.so.h;
   a.lse = p.lse;
+  a.tma_store = tma_store ? 1 : 0;
   a.err = ctl.err;
   a.timeout_ns = ctl.timeout_ns;
-  const dim3 grid(a.units_m, p.H, a.varlen ? p.n_seqs : p.B);
-  if (grid.x == 0) return cudaSuccess;
+  a.Z = a.varlen ? p.n_seqs : p.B;
+  const long long total = static_cast<long long>(a.units_m) * p.H * a.Z;
+  if (total == 0) return cudaSuccess;
+  if (total > 0x7fffffffLL) {
+    *why = "too many work units";
+    return cudaErrorInvalidValue;
+  }
+  a.total_units = static_cast<int>(total);
+  // Persistent: one CTA per SM (or fewer when there are fewer units).
+  const dim3 grid(static_cast<unsigned>(std::min<long long>(total, num_sms())));
   cudaError_t e = cudaFuncSetAttribute(fmha_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Lt::kAlloc);
   if (e != cudaSuccess) {
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  fmha_tc_kernel<D><<<grid, kThreads, Lt::kAlloc, stream>>>(tq, tk, tv, a);
+  fmha_tc_kernel<D><<<grid, kThreads, Lt::kAlloc, stream>>>(tq, tk, tv, to, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     static thread_local char msg[160];
