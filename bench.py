@@ -442,6 +442,63 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
     return res
 
 
+def run_profile_other(args):
+    """Warm-up + timed steps of one secondary kernel's workload (for ncu captures)."""
+    import torch
+
+    import attention_fmha_fwd_gb300 as fa
+    from attention_fmha_fwd_gb300 import build, inputs
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.workload == "merge":
+        n, B, M, H, Kv = 8, 2, 2048, 32, 128
+        g = torch.Generator(device=dev).manual_seed(0)
+        outs = torch.randn((n, B, M, H, Kv), generator=g, device=dev)
+        lses = torch.randn((n, B, H, M), generator=g, device=dev)
+        mo = torch.empty((B, M, H, Kv), dtype=torch.bfloat16, device=dev)
+        ml = torch.empty((B, H, M), dtype=torch.float32, device=dev)
+
+        def step():
+            fa.merge_attentions(outs, lses, out=mo, lse=ml)
+    elif args.workload == "decode_split_kv":
+        w = inputs.WORKLOADS["decode_split_kv"]
+        q, k, v = inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        bounds = inputs.equal_chunks(w.Mkv, 16)
+        po = torch.empty((16, w.B, w.M, w.H, w.Kv), dtype=torch.float32, device=dev)
+        pl = torch.empty((16, w.B, w.H, w.M), dtype=torch.float32, device=dev)
+
+        def step():
+            for c, (a, b) in enumerate(bounds):
+                fa.attn_partial(qd, kd[:, a:b], vd[:, a:b], scale=w.scale, out=po[c], lse=pl[c])
+            fa.merge_attentions(po, pl)
+    else:
+        w = inputs.WORKLOADS["varlen_packed"]
+        lens = inputs.varlen_seqlens(w.n_seqs, w.M, seed=0)
+        cu = torch.tensor(inputs.cu_seqlens(lens), dtype=torch.int32, device=dev)
+        q, k, v = inputs.qkv(1, w.M, w.Mkv, w.H, w.K, seed=0)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+
+        def step():
+            fa.attn_fwd(qd, kd, vd, mask="blockdiag_causal", scale=w.scale, cu_seqlens_q=cu,
+                        cu_seqlens_k=cu, max_seqlen_q=max(lens), max_seqlen_k=max(lens))
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_mode": True, "workload": args.workload,
+                      "ms_per_step": a.elapsed_time(b) / args.steps}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,11 +510,16 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--profile-mode", action="store_true",
                     help="only the warm-up and timed steps (for ncu); prints a short line")
+    ap.add_argument("--workload", default="causal_fwd",
+                    choices=["causal_fwd", "merge", "decode_split_kv", "varlen_packed"],
+                    help="with --profile-mode: which kernel's workload to run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_mode and args.workload != "causal_fwd":
+        return run_profile_other(args)
     return run_gpu(args)
 
 
