@@ -83,6 +83,8 @@ _lock = threading.Lock()
 def load(path: str | None = None) -> ctypes.CDLL:
     """Load libmslk_attn.so (once) and declare its functions."""
     global _lib
+    if _lib is not None and path is None:
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib

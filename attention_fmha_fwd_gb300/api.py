@@ -34,21 +34,32 @@ def _mask_kind(mask) -> int:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream_handle(stream) -> ctypes.c_void_p:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+# The raw handle of the current stream without building a torch.cuda.Stream object
+# (a few microseconds per call); torch.cuda.current_stream() where that is unavailable.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream, device=None) -> int:
+    if stream is not None:
+        return stream.cuda_stream
+    index = device.index if device is not None else None
+    if index is None:
+        index = torch.cuda.current_device()
+    if _raw_stream is not None:
+        return _raw_stream(index)
+    return torch.cuda.current_stream(index).cuda_stream
 
 
 def _bmhk_strides(t: torch.Tensor, name: str) -> Strides:
-    if t.dim() != 4:
+    st = t.stride()
+    if len(st) != 4:
         raise ValueError(f"{name} must be [B, M, H, D], got shape {tuple(t.shape)}")
-    if t.shape[3] > 1 and t.stride(3) != 1:
+    if st[3] != 1 and t.shape[3] > 1:
         raise ValueError(f"{name}: the last dimension must have stride 1")
-    return Strides(t.stride(0), t.stride(1), t.stride(2))
+    return Strides(st[0], st[1], st[2])
 
 
 def _as_bmhk(t: torch.Tensor) -> torch.Tensor:
@@ -59,6 +70,9 @@ def _as_bmhk(t: torch.Tensor) -> torch.Tensor:
 
 
 def _check_inputs(q, k, v):
+    bf16 = torch.bfloat16
+    if q.dtype is bf16 and k.dtype is bf16 and v.dtype is bf16 and q.is_cuda and k.is_cuda and v.is_cuda:
+        return
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor (the library reads device memory)")
@@ -104,12 +118,13 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", 
     elif lse is False:
         lse = None
     sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
-    sq, sk, sv, so = (_bmhk_strides(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
+    sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
+    so = _bmhk_strides(out, "out")
     lib = _capi.load()
-    check(lib.mslk_attn_fwd(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(sq), ctypes.byref(sk),
-                            ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H, K, Kv,
-                            0.0 if scale is None else float(scale), mk, sl, _ptr(out),
-                            _ptr(lse), _stream_handle(stream)))
+    check(lib.mslk_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
+                            ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H, K,
+                            Kv, 0.0 if scale is None else float(scale), mk, sl, out.data_ptr(),
+                            _ptr(lse), _stream_handle(stream, q.device)))
     return out, lse
 
 
@@ -135,13 +150,14 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
     if lse is None:
         lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
     sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
-    sq, sk, sv, so = (_bmhk_strides(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")))
+    sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
+    so = _bmhk_strides(out, "out")
     lib = _capi.load()
-    check(lib.mslk_attn_partial(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(sq), ctypes.byref(sk),
-                                ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H, K, Kv,
-                                0.0 if scale is None else float(scale), mk, sl, int(kv_offset),
-                                _ptr(out), _DTYPES[out_dtype], _ptr(lse),
-                                _stream_handle(stream)))
+    check(lib.mslk_attn_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
+                                ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H,
+                                K, Kv, 0.0 if scale is None else float(scale), mk, sl,
+                                int(kv_offset), out.data_ptr(), _DTYPES[out_dtype], lse.data_ptr(),
+                                _stream_handle(stream, q.device)))
     return out, lse
 
 
@@ -192,9 +208,9 @@ def merge_attentions(out_split, lse_split, *, write_lse=True, output_dtype=torch
     ss = _bmhk_strides(o0, "out_split")
     so = _bmhk_strides(out, "out")
     lib = _capi.load()
-    check(lib.mslk_merge_attentions(_ptr(o0), _ptr(l0), n, cs_o, cs_l, B, M, H, Kv,
-                                    ctypes.byref(ss), ctypes.byref(so), _ptr(out),
-                                    _DTYPES[out.dtype], _ptr(lse), _stream_handle(stream)))
+    check(lib.mslk_merge_attentions(o0.data_ptr(), l0.data_ptr(), n, cs_o, cs_l, B, M, H, Kv,
+                                    ctypes.byref(ss), ctypes.byref(so), out.data_ptr(),
+                                    _DTYPES[out.dtype], _ptr(lse), _stream_handle(stream, o0.device)))
     return out, lse
 
 

@@ -3,13 +3,17 @@
 //
 // With one query row per head each K/V element is used once, so the work is a stream
 // of K and V from HBM (about 1 FLOP per byte); tensor-core tiles would be 128-fold
-// padding.  Each CTA owns one (batch, head) and streams all its keys: 8 warps take
-// contiguous key ranges; lane l holds head-dim elements [l*V, l*V+V) of every row
-// (V = D/32), loads 32 (or 16) keys of K and V per step with 8-byte (D=128) / 4-byte
-// (D=64) coalesced loads (a 256/128-byte row per warp instruction), forms the scores
-// with a halving butterfly (each lane ends up with one key's full score), and runs the
-// base-2 online softmax.  The 8 warp states (max, sum, accumulator) are then merged through shared
-// memory by the same LSE rule as the split-KV merge.
+// padding.  The keys of one (batch, head) are split over a thread-block cluster of CS
+// CTAs (CS = 1..8, chosen so the grid fits in one wave); inside a CTA one producer warp
+// streams tiles of T keys (T * D = 4096 elements: 8 KiB of K plus 8 KiB of V) through a
+// ring of shared-memory stages with TMA, so up to 192 KiB per SM are in flight whatever
+// the register budget.  Eight consumer warps take the tiles round robin.  Lane l holds
+// head-dim elements [l*V, l*V+V) of every row (V = D/32) and reads them from shared
+// memory (one 256/128-byte row per warp instruction); a halving butterfly leaves key l's
+// full score on lane l, followed by the base-2 online softmax and one pass over the V
+// rows for all query rows.  Warp states (max, sum, accumulator) merge through shared
+// memory and the CTAs of a cluster merge through distributed shared memory, by the same
+// LSE rule as the split-KV merge; no global scratch memory is used.
 //
 // Semantics follow MSLK's memory_efficient_attention / _partial ("Attention - Core
 // fMHA"): out = softmax(scale q.k^T + mask) v over the allowed keys; lse = ln sum exp;
@@ -17,34 +21,52 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace mslk {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 8;                      // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;    // + one producer warp
+constexpr int kMaxCluster = 8;
+constexpr int kStages = 12;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+template <int D>
+struct DecLayout {
+  static constexpr int kT = 4096 / D;              // keys per tile: 32 (D=128), 64 (D=64)
+  static constexpr int kTileBytes = kT * D * 2;    // one tensor's tile: 8 KiB
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kFullOff = kRingBytes;      // full[kStages] mbarriers
+  static constexpr int kEmptyOff = kFullOff + 8 * kStages;
+  static constexpr int kAbortOff = kEmptyOff + 8 * kStages;
+  static constexpr int kIssuedOff = kAbortOff + 4;  // tiles issued so far (producer-written)
+  static constexpr int kBytes = kAbortOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;     // slack for 1024-byte alignment
+};
+
 struct DecArgs {
   const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
   long long sq_b, sq_m, sq_h;
-  long long sk_b, sk_m, sk_h;
-  long long sv_b, sv_m, sv_h;
   int M, Mkv, H;
   int hk_shared, causal;
+  int cs;  // CTAs per (batch, head): the cluster size
   long long kv_offset;
   float scale_log2;
   void* out;
   int out_fp32;
   long long so_b, so_m, so_h;
   float* lse;
+  unsigned int* err;
+  unsigned long long timeout_ns;
 };
 
 template <int V>
@@ -68,11 +90,6 @@ struct Vec<2> {
   }
 };
 
-template <typename T>
-MSLK_DEV T ldg_stream(const T* p) {
-  return __ldg(p);
-}
-
 MSLK_DEV float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -84,212 +101,416 @@ MSLK_DEV float warp_sum(float x) {
   return x;
 }
 
-// v[0..N-1] (N = 16 or 32) are one lane's partial sums for N keys.  Returns on lane l
-// the full sum over all 32 lanes for key l / (32 / N).  Each halving step keeps the half
-// of the values selected by one lane bit and adds the partner lane's other half.
-template <int N>
-MSLK_DEV float butterfly_reduce(float (&v)[N], int lane) {
-  int n = N;
+// v[0..31] are one lane's partial sums for 32 keys.  Returns on lane l the full sum over
+// all 32 lanes for key l.  Each halving step keeps the half of the values selected by one
+// lane bit and adds the partner lane's other half.
+MSLK_DEV float butterfly_reduce32(float (&v)[32], int lane) {
+  int n = 32;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
-    if (n > 1) {
-      n /= 2;
+    n /= 2;
+    const bool up = lane & o;
 #pragma unroll
-      for (int i = 0; i < N / 2; ++i) {
-        if (i < n) {
-          const bool up = lane & o;
-          const float send = up ? v[i] : v[i + n];
-          const float keep = up ? v[i + n] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
+    for (int i = 0; i < 16; ++i) {
+      if (i < n) {
+        const float send = up ? v[i] : v[i + n];
+        const float keep = up ? v[i + n] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
     }
   }
   return v[0];
 }
 
+// Bounded mbarrier wait: false on timeout (recorded in the error word and the CTA's abort
+// flag) or when another warp of the CTA has already given up.
+MSLK_DEV bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DecArgs& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(a.err, kErrWaitTimeout);
+      return false;
+    }
+  }
+}
+
+// Bounded wait until the producer has issued more than `i` tiles.  Tile i is issued only
+// after tile i - kStages (same stage, possibly another warp's) has been consumed, so the
+// stage's previous full-barrier phase has completed and a parity wait on it cannot be
+// satisfied by that older phase.
+MSLK_DEV bool wait_issued(const volatile int* issued, int i, volatile int* abort_flag, const DecArgs& a) {
+  if (*issued > i) {
+    __threadfence_block();
+    return true;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  while (*issued <= i) {
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(a.err, kErrWaitTimeout);
+      return false;
+    }
+  }
+  __threadfence_block();
+  return true;
+}
+
 template <int D, int MQ>
-__global__ void __launch_bounds__(kThreads, 1) fmha_decode_kernel(const DecArgs a) {
-  constexpr int VE = D / 32;  // head-dim elements per lane
-  // Keys per step: 32 (a key per lane) unless the registers of several query rows
-  // need the smaller step (16 keys, each score held by a lane pair).
-  constexpr int KB = (D == 128 && MQ > 1) ? 16 : 32;
-  constexpr int kDup = 32 / KB;
+struct DecodeState {
+  float m_run[MQ], l_run[MQ], acc[MQ][D / 32];
+};
+
+// Folds one tile of keys (in shared memory, row-major [T][D]) into the warp's
+// online-softmax state, 32 keys at a time.
+template <int D, int MQ>
+MSLK_DEV void fold_tile(const DecArgs& a, const float (&qf)[MQ][D / 32], const uint8_t* sK,
+                        const uint8_t* sV, int key0, int kb1, int lane, DecodeState<D, MQ>& st) {
+  constexpr int VE = D / 32;
+  constexpr int T = DecLayout<D>::kT;
   using VT = typename Vec<VE>::T;
-  const int h = blockIdx.x;
-  const int b = blockIdx.y;
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  const int hk = a.hk_shared ? 0 : h;
-
-  // Query rows, pre-multiplied by scale * log2(e): scores come out in base 2.
-  float qf[MQ][VE];
-#pragma unroll
-  for (int m = 0; m < MQ; ++m) {
-    if (m < a.M) {
-      const VT x = *reinterpret_cast<const VT*>(a.q + b * a.sq_b + m * a.sq_m + h * a.sq_h + lane * VE);
-      Vec<VE>::to_float(x, qf[m]);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) qf[m][e] *= a.scale_log2;
-    } else {
-#pragma unroll
-      for (int e = 0; e < VE; ++e) qf[m][e] = 0.f;
-    }
-  }
-
-  // Keys this warp owns: contiguous, a multiple of 32 long.
-  int n_keys = a.Mkv;
-  if (a.causal) {  // key j allowed iff kv_offset + j <= row; the last row sees the most
-    const long long kmax = static_cast<long long>(a.M - 1) - a.kv_offset;
-    n_keys = kmax < 0 ? 0 : static_cast<int>(min(static_cast<long long>(n_keys), kmax + 1));
-  }
-  const int blocks = (n_keys + KB - 1) / KB;
-  const int per_warp = (blocks + kWarps - 1) / kWarps;
-  const int kb0 = warp * per_warp * KB;
-  const int kb1 = min(n_keys, (warp + 1) * per_warp * KB);
-
-  float m_run[MQ], l_run[MQ], acc[MQ][VE];
-#pragma unroll
-  for (int m = 0; m < MQ; ++m) {
-    m_run[m] = -INFINITY;
-    l_run[m] = 0.f;
-#pragma unroll
-    for (int e = 0; e < VE; ++e) acc[m][e] = 0.f;
-  }
-
-  const __nv_bfloat16* kbase = a.k + b * a.sk_b + hk * a.sk_h + lane * VE;
-  const __nv_bfloat16* vbase = a.v + b * a.sv_b + hk * a.sv_h + lane * VE;
-  for (int k0 = kb0; k0 < kb1; k0 += KB) {
-    VT kr[KB], vr[KB];
-#pragma unroll
-    for (int j = 0; j < KB; ++j) {
-      const int key = k0 + j;
-      if (key < kb1) {
-        kr[j] = ldg_stream(reinterpret_cast<const VT*>(kbase + static_cast<long long>(key) * a.sk_m));
-        vr[j] = ldg_stream(reinterpret_cast<const VT*>(vbase + static_cast<long long>(key) * a.sv_m));
-      } else {
-        kr[j] = VT{};
-        vr[j] = VT{};
-      }
-    }
-    const int my_key = k0 + lane / kDup;
+#pragma unroll 1
+  for (int sb = 0; sb < T; sb += 32) {
+    const int my_key = key0 + sb + lane;
+    const VT* kp = reinterpret_cast<const VT*>(sK + (sb * D + lane * VE) * 2);
+    const VT* vp = reinterpret_cast<const VT*>(sV + (sb * D + lane * VE) * 2);
+    float p[MQ];
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
-      if (m >= a.M) break;
-      float part[KB];
+      p[m] = 0.f;
+      if (m >= a.M) continue;
+      float part[32];
 #pragma unroll
-      for (int j = 0; j < KB; ++j) {
+      for (int j = 0; j < 32; ++j) {
         float kf[VE];
-        Vec<VE>::to_float(kr[j], kf);
+        Vec<VE>::to_float(kp[j * (D / VE)], kf);
         float d = 0.f;
 #pragma unroll
         for (int e = 0; e < VE; ++e) d = fmaf(qf[m][e], kf[e], d);
         part[j] = d;
       }
-      float sc = butterfly_reduce<KB>(part, lane);
+      float sc = butterfly_reduce32(part, lane);
       const bool allowed = my_key < kb1 && (!a.causal || a.kv_offset + my_key <= m);
       sc = allowed ? sc : -INFINITY;
-      const float m_new = fmaxf(m_run[m], warp_max(sc));
+      const float m_new = fmaxf(st.m_run[m], warp_max(sc));
       const float msub = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run[m] - msub);  // m_run = -inf -> 0
-      const float p = ex2_approx(sc - msub);
-      // With lane pairs holding the same key, count each key once in the sum.
-      l_run[m] = l_run[m] * alpha + warp_sum((lane % kDup == 0) ? p : 0.f);
-      m_run[m] = m_new;
+      const float alpha = ex2_approx(st.m_run[m] - msub);  // m_run = -inf -> 0
+      p[m] = ex2_approx(sc - msub);
+      st.l_run[m] = st.l_run[m] * alpha + warp_sum(p[m]);
+      st.m_run[m] = m_new;
 #pragma unroll
-      for (int e = 0; e < VE; ++e) acc[m][e] *= alpha;
+      for (int e = 0; e < VE; ++e) st.acc[m][e] *= alpha;
+    }
+    // One pass over the V rows for every query row.
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j) {
+      float vf[VE];
+      Vec<VE>::to_float(vp[j * (D / VE)], vf);
 #pragma unroll
-      for (int j = 0; j < KB; ++j) {
-        const float pj = __shfl_sync(0xffffffffu, p, j * kDup);
-        float vf[VE];
-        Vec<VE>::to_float(vr[j], vf);
+      for (int m = 0; m < MQ; ++m) {
+        if (m >= a.M) continue;
+        const float pj = __shfl_sync(0xffffffffu, p[m], j);
 #pragma unroll
-        for (int e = 0; e < VE; ++e) acc[m][e] = fmaf(pj, vf[e], acc[m][e]);
+        for (int e = 0; e < VE; ++e) st.acc[m][e] = fmaf(pj, vf[e], st.acc[m][e]);
       }
     }
   }
+}
 
-  // Merge the warps' states: M* = max_w m_w; L = sum_w 2^(m_w - M*) l_w;
-  // out = sum_w 2^(m_w - M*) acc_w / L.
-  __shared__ float s_m[kWarps][MQ];
-  __shared__ float s_l[kWarps][MQ];
-  __shared__ float s_acc[kWarps][MQ][D];
-#pragma unroll
-  for (int m = 0; m < MQ; ++m) {
-    if (lane == 0) {
-      s_m[warp][m] = m_run[m];
-      s_l[warp][m] = l_run[m];
+template <int D, int MQ>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const DecArgs a) {
+  using L = DecLayout<D>;
+  constexpr int VE = D / 32;  // head-dim elements per lane
+  constexpr int T = L::kT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbortOff);
+  volatile int* issued_ctr = reinterpret_cast<volatile int*>(smem + L::kIssuedOff);
+
+  const int rank = static_cast<int>(blockIdx.x) % a.cs;  // CTA rank inside the cluster
+  const int h = static_cast<int>(blockIdx.x) / a.cs;
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int hk = a.hk_shared ? 0 : h;
+
+  // Keys of this (batch, head): the causal limit of the last row, split over the
+  // cluster's CTAs in whole tiles.
+  int n_keys = a.Mkv;
+  if (a.causal) {  // key j allowed iff kv_offset + j <= row; the last row sees the most
+    const long long kmax = static_cast<long long>(a.M - 1) - a.kv_offset;
+    n_keys = kmax < 0 ? 0 : static_cast<int>(min(static_cast<long long>(n_keys), kmax + 1));
+  }
+  const int tiles_all = (n_keys + T - 1) / T;
+  const int per_cta = (tiles_all + a.cs - 1) / a.cs;
+  const int t0 = min(tiles_all, rank * per_cta);
+  const int n_tiles = max(0, min(tiles_all, t0 + per_cta) - t0);
+  const int key_base = t0 * T;
+  const int kb1 = min(n_keys, (t0 + n_tiles) * T);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(sbase + L::kFullOff + 8 * s, 1);
+      mbar_init(sbase + L::kEmptyOff + 8 * s, 1);
     }
-#pragma unroll
-    for (int e = 0; e < VE; ++e) s_acc[warp][m][lane * VE + e] = acc[m][e];
+    *abort_flag = 0;
+    *issued_ctr = 0;
+    fence_mbar_init();
   }
   __syncthreads();
-  // Warp w finalises rows w, w + 8, ... (MQ <= 8: one row per warp).
-  for (int m = warp; m < a.M && m < MQ; m += kWarps) {
+
+  DecodeState<D, MQ> st;
+#pragma unroll
+  for (int m = 0; m < MQ; ++m) {
+    st.m_run[m] = -INFINITY;
+    st.l_run[m] = 0.f;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) st.acc[m][e] = 0.f;
+  }
+
+  if (warp == kWarps) {
+    // Producer: tile i -> stage i % kStages, after the consumer of tile i - kStages has
+    // released the stage; the issued count it publishes tells consumers when a stage's
+    // barrier is on the phase of their tile.  Afterwards it waits (bounded) for every copy it issued, so no
+    // copy is still writing shared memory when the stages are reused below.
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % kStages;
+        if (i >= kStages &&
+            !wait_bounded(sbase + L::kEmptyOff + 8 * s, ((i / kStages) - 1) & 1, abort_flag, a))
+          break;
+        const uint32_t full = sbase + L::kFullOff + 8 * s;
+        const uint32_t dst = sbase + s * L::kStageBytes;
+        mbar_arrive_expect_tx(full, L::kStageBytes);
+        tma_load_4d(dst, &tm_k, full, 0, key_base + i * T, hk, b);
+        tma_load_4d(dst + L::kTileBytes, &tm_v, full, 0, key_base + i * T, hk, b);
+        ++issued;
+        __threadfence_block();
+        *issued_ctr = issued;
+      }
+      const uint64_t t_start = globaltimer_ns();
+      for (int i = max(0, issued - kStages); i < issued; ++i) {
+        const uint32_t full = sbase + L::kFullOff + 8 * (i % kStages);
+        while (!mbar_try_wait(full, (i / kStages) & 1)) {
+          if (globaltimer_ns() - t_start > a.timeout_ns) {
+            *abort_flag = 1;
+            atomicOr(a.err, kErrWaitTimeout);
+            break;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // Query rows, pre-multiplied by scale * log2(e): scores come out in base 2.
+    using VT = typename Vec<VE>::T;
+    float qf[MQ][VE];
+#pragma unroll
+    for (int m = 0; m < MQ; ++m) {
+      if (m < a.M) {
+        const VT x = *reinterpret_cast<const VT*>(a.q + b * a.sq_b + m * a.sq_m + h * a.sq_h + lane * VE);
+        Vec<VE>::to_float(x, qf[m]);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) qf[m][e] *= a.scale_log2;
+      } else {
+#pragma unroll
+        for (int e = 0; e < VE; ++e) qf[m][e] = 0.f;
+      }
+    }
+    for (int i = warp; i < n_tiles; i += kWarps) {
+      const int s = i % kStages;
+      const bool ok = __all_sync(0xffffffffu,
+                                 wait_issued(issued_ctr, i, abort_flag, a) &&
+                                     wait_bounded(sbase + L::kFullOff + 8 * s, (i / kStages) & 1, abort_flag, a));
+      if (!ok) break;
+      const uint8_t* sK = smem + s * L::kStageBytes;
+      fold_tile<D, MQ>(a, qf, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sbase + L::kEmptyOff + 8 * s);
+    }
+  }
+  __syncthreads();  // every copy has landed and every tile has been read: the ring is free
+
+  // Merge the warps' states: M* = max_w m_w; L = sum_w 2^(m_w - M*) l_w;
+  // acc = sum_w 2^(m_w - M*) acc_w.  The CTA's merged state goes to c_* for the cluster.
+  // These arrays reuse the ring's shared memory.
+  float(*s_m)[MQ] = reinterpret_cast<float(*)[MQ]>(smem);
+  float(*s_l)[MQ] = reinterpret_cast<float(*)[MQ]>(smem + kWarps * MQ * 4);
+  float(*s_acc)[MQ][D] = reinterpret_cast<float(*)[MQ][D]>(smem + 2 * kWarps * MQ * 4);
+  float* c_m = reinterpret_cast<float*>(smem + 2 * kWarps * MQ * 4 + kWarps * MQ * D * 4);
+  float* c_l = c_m + MQ;
+  float(*c_acc)[D] = reinterpret_cast<float(*)[D]>(c_l + MQ);
+  if (warp < kWarps) {
+#pragma unroll
+    for (int m = 0; m < MQ; ++m) {
+      if (lane == 0) {
+        s_m[warp][m] = st.m_run[m];
+        s_l[warp][m] = st.l_run[m];
+      }
+#pragma unroll
+      for (int e = 0; e < VE; ++e) s_acc[warp][m][lane * VE + e] = st.acc[m][e];
+    }
+  }
+  __syncthreads();
+  // Warp w merges row w (MQ <= 8: at most one row per warp).
+  for (int m = warp; m < a.M && m < MQ; m += kWarps + 1) {
     float mstar = -INFINITY;
     for (int w = 0; w < kWarps; ++w) mstar = fmaxf(mstar, s_m[w][m]);
     const float msub = (mstar == -INFINITY) ? 0.f : mstar;
-    float L = 0.f;
+    float Ls = 0.f;
     float o[VE];
 #pragma unroll
     for (int e = 0; e < VE; ++e) o[e] = 0.f;
     for (int w = 0; w < kWarps; ++w) {
       const float c = ex2_approx(s_m[w][m] - msub);
-      L = fmaf(c, s_l[w][m], L);
+      Ls = fmaf(c, s_l[w][m], Ls);
 #pragma unroll
       for (int e = 0; e < VE; ++e) o[e] = fmaf(c, s_acc[w][m][lane * VE + e], o[e]);
     }
-    const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    if (a.out_fp32) {
-      float* op = static_cast<float*>(a.out) + b * a.so_b + m * a.so_m + h * a.so_h + lane * VE;
-#pragma unroll
-      for (int e = 0; e < VE; ++e) op[e] = o[e] * inv;
-    } else {
-      __nv_bfloat16* op =
-          static_cast<__nv_bfloat16*>(a.out) + b * a.so_b + m * a.so_m + h * a.so_h + lane * VE;
-#pragma unroll
-      for (int e = 0; e < VE; e += 2)
-        *reinterpret_cast<uint32_t*>(op + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
+    if (lane == 0) {
+      c_m[m] = mstar;
+      c_l[m] = Ls;
     }
-    if (lane == 0 && a.lse != nullptr)
-      a.lse[(static_cast<long long>(b) * a.H + h) * a.M + m] =
-          (L > 0.f) ? (mstar + lg2_approx(L)) * kLn2 : -INFINITY;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) c_acc[m][lane * VE + e] = o[e];
   }
+
+  // Cluster merge: rank 0 reads every rank's (c_m, c_l, c_acc) through distributed shared
+  // memory and writes the row; the second barrier keeps the other CTAs (and their shared
+  // memory) alive until rank 0 has read them.
+  if (a.cs > 1) cluster_sync(); else __syncthreads();
+  if (rank == 0) {
+    for (int m = warp; m < a.M && m < MQ; m += kWarps + 1) {
+      float mstar = -INFINITY;
+      for (int r = 0; r < a.cs; ++r)
+        mstar = fmaxf(mstar, a.cs > 1 ? ld_shared_cluster_f32(mapa_shared(smem_u32(&c_m[m]), r)) : c_m[m]);
+      const float msub = (mstar == -INFINITY) ? 0.f : mstar;
+      float Ls = 0.f;
+      float o[VE];
+#pragma unroll
+      for (int e = 0; e < VE; ++e) o[e] = 0.f;
+      for (int r = 0; r < a.cs; ++r) {
+        const float mr = a.cs > 1 ? ld_shared_cluster_f32(mapa_shared(smem_u32(&c_m[m]), r)) : c_m[m];
+        const float lr = a.cs > 1 ? ld_shared_cluster_f32(mapa_shared(smem_u32(&c_l[m]), r)) : c_l[m];
+        const float c = ex2_approx(mr - msub);
+        Ls = fmaf(c, lr, Ls);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          const float x = a.cs > 1 ? ld_shared_cluster_f32(mapa_shared(smem_u32(&c_acc[m][lane * VE + e]), r))
+                                   : c_acc[m][lane * VE + e];
+          o[e] = fmaf(c, x, o[e]);
+        }
+      }
+      const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
+      if (a.out_fp32) {
+        float* op = static_cast<float*>(a.out) + b * a.so_b + m * a.so_m + h * a.so_h + lane * VE;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) op[e] = o[e] * inv;
+      } else {
+        __nv_bfloat16* op =
+            static_cast<__nv_bfloat16*>(a.out) + b * a.so_b + m * a.so_m + h * a.so_h + lane * VE;
+#pragma unroll
+        for (int e = 0; e < VE; e += 2)
+          *reinterpret_cast<uint32_t*>(op + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
+      }
+      if (lane == 0 && a.lse != nullptr)
+        a.lse[(static_cast<long long>(b) * a.H + h) * a.M + m] =
+            (Ls > 0.f) ? (mstar + lg2_approx(Ls)) * kLn2 : -INFINITY;
+    }
+  }
+  if (a.cs > 1) cluster_sync();
 }
 
 template <int D, int MQ>
-cudaError_t launch_dm(const DecArgs& a, int B, int H, cudaStream_t stream) {
-  fmha_decode_kernel<D, MQ><<<dim3(H, B), kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, const DecArgs& a, int B, int H,
+                      cudaStream_t stream) {
+  using L = DecLayout<D>;
+  static_assert(L::kAlloc <= 227 * 1024, "shared memory");
+  static_assert(2 * kWarps * MQ * 4 + kWarps * MQ * D * 4 + 2 * MQ * 4 + MQ * D * 4 <= L::kRingBytes,
+                "merge arrays must fit in the ring");
+  // The shared-memory opt-in is per device; set it once on each.
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> opted_in[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(fmha_decode_kernel<D, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kAlloc);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(1, std::memory_order_release);
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(H * a.cs), static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(a.cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fmha_decode_kernel<D, MQ>, tk, tv, a);
 }
 
 template <int D>
-cudaError_t launch_d(const DecArgs& a, int B, int H, cudaStream_t stream) {
-  if (a.M <= 1) return launch_dm<D, 1>(a, B, H, stream);
-  if (a.M <= 2) return launch_dm<D, 2>(a, B, H, stream);
-  if (a.M <= 4) return launch_dm<D, 4>(a, B, H, stream);
-  return launch_dm<D, 8>(a, B, H, stream);
+cudaError_t launch_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecArgs& a, int B, int H,
+                     cudaStream_t stream) {
+  if (a.M <= 1) return launch_dm<D, 1>(tk, tv, a, B, H, stream);
+  if (a.M <= 2) return launch_dm<D, 2>(tk, tv, a, B, H, stream);
+  if (a.M <= 4) return launch_dm<D, 4>(tk, tv, a, B, H, stream);
+  return launch_dm<D, 8>(tk, tv, a, B, H, stream);
+}
+
+int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
 }
 
 }  // namespace
 
-cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream) {
-  (void)ctl;  // no waits in this kernel
+cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
+                               const char** why) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) {
+    *why = "cuTensorMapEncodeTiled is not available from the driver";
+    return cudaErrorNotSupported;
+  }
+  const int D = p.K;
+  const int T = 4096 / D;
+  const long long hk = p.kv_head_shared ? 1 : p.H;
+  CUtensorMap tk, tv;
+  if (!encode_rows_plain(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, D, T) ||
+      !encode_rows_plain(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, D, T)) {
+    *why = "cuTensorMapEncodeTiled rejected a k/v layout";
+    return cudaErrorInvalidValue;
+  }
   DecArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(p.q);
-  a.k = static_cast<const __nv_bfloat16*>(p.k);
-  a.v = static_cast<const __nv_bfloat16*>(p.v);
   a.sq_b = p.sq.b;
   a.sq_m = p.sq.m;
   a.sq_h = p.sq.h;
-  a.sk_b = p.sk.b;
-  a.sk_m = p.sk.m;
-  a.sk_h = p.sk.h;
-  a.sv_b = p.sv.b;
-  a.sv_m = p.sv.m;
-  a.sv_h = p.sv.h;
   a.M = p.M;
   a.Mkv = p.Mkv;
   a.H = p.H;
@@ -303,8 +524,18 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   a.so_m = p.so.m;
   a.so_h = p.so.h;
   a.lse = p.lse;
-  if (p.K == 128) return launch_d<128>(a, p.B, p.H, stream);
-  return launch_d<64>(a, p.B, p.H, stream);
+  a.err = ctl.err;
+  a.timeout_ns = ctl.timeout_ns;
+  // Cluster size: the grid stays within one wave of one CTA per SM, and every CTA keeps
+  // at least two tiles per consumer warp.
+  const long long units = static_cast<long long>(p.B) * p.H;
+  const long long tiles = (static_cast<long long>(p.Mkv) + T - 1) / T;
+  int cs = 1;
+  while (cs < kMaxCluster && units * cs * 2 <= sm_count() && tiles / (cs * 2) >= 2 * kWarps) cs *= 2;
+  a.cs = cs;
+  *why = "decode kernel launch failed";
+  if (D == 128) return launch_d<128>(tk, tv, a, p.B, p.H, stream);
+  return launch_d<64>(tk, tv, a, p.B, p.H, stream);
 }
 
 }  // namespace mslk

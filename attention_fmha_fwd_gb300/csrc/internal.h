@@ -63,7 +63,8 @@ constexpr int kDecodeMaxRows = 8;
 cudaError_t launch_fmha_tc(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
                            const char** why);
 // CUDA-core streaming kernel for M <= kDecodeMaxRows with dense masks.
-cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream);
+cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
+                               const char** why);
 // out = 0, lse = -inf for every row (no keys at all).
 cudaError_t launch_fill_empty(const AttnProblem& p, cudaStream_t stream);
 // LSE merge.

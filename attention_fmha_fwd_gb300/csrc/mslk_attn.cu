@@ -209,7 +209,7 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   cudaError_t e;
   const char* why = "launch failed";
   if (decode_ok && policy != 1) {
-    e = launch_fmha_decode(p, ctl, stream);
+    e = launch_fmha_decode(p, ctl, stream, &why);
   } else {
     e = launch_fmha_tc(p, ctl, stream, &why);
   }

@@ -77,6 +77,17 @@ def test_fwd_decode_rows(M, D, mask):
     _fwd_case(3, M, 1000, 4, D, mask, policy=1)
 
 
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_decode_cluster_split_long_keys(M):
+    """Few heads and many keys: the decode kernel splits each head's keys over a cluster
+    of 8 CTAs and merges them through distributed shared memory."""
+    _fwd_case(1, M, 20000, 2, 128, "none", seed=21)
+    q, k, v = inputs.qkv(1, M, 20000, 2, 128, seed=22)
+    o, l_ = fa.attn_partial(*to_dev(q, k, v), mask="causal", kv_offset=-19990)
+    ro, rl = oracle.attention_partial(f32(q), f32(k), f32(v), 1 / 128 ** 0.5, 1, kv_offset=-19990)
+    compare(o.double().cpu().numpy(), l_.double().cpu().numpy(), ro, rl, "cluster causal partial")
+
+
 def test_fwd_strided_views_and_shared_head():
     """q/k/v as views into packed buffers (free strides) and K/V expanded with head stride 0."""
     B, M, Mkv, H, D = 2, 200, 260, 4, 128
