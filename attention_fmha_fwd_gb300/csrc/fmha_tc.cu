@@ -18,7 +18,7 @@
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D),
 // fp32 accumulators, row r of a tile in lane r.  The bf16 probabilities P_t overwrite the
 // first 64 columns of S_t (two values per column) and feed the PV MMA from tensor memory.
-// Shared memory: Q0, Q1 and a 5-stage ring of K/V tiles, in the 128-byte-swizzled
+// Shared memory: Q0, Q1 and a ring of K/V tiles (4 stages at D=128), in the 128-byte-swizzled
 // K-major layout TMA writes (V is read MN-major by the PV MMA).
 // The MMA and TMA roles run as whole converged warps that issue through one elected lane:
 // their operands stay warp-uniform, so they need few issue slots while the softmax
@@ -474,41 +474,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (a.causal) lim = min(lim, static_cast<long long>(r) - a.kv_offset - key0);
           lim_c = static_cast<int>(max(-1LL, min(lim, static_cast<long long>(kBlockN - 1))));
         }
-        // Two passes over the S row in tensor memory: pass 1 takes the row max, pass 2
-        // forms p = 2^(s*scale*log2e - m) (bf16, packed in pairs over S's first 64
-        // columns; quarter q of P lands in columns [16q, 16q+16), all of which pass 2 has
-        // already read) and the row sum.  Interior tiles (every column allowed) run fully
-        // unrolled code; tiles crossing a mask limit classify 32/64-column bands
-        // warp-uniformly so only the band(s) holding a row's limit test each column.
+        // The whole S row comes out of tensor memory in one load (128 registers): mask it
+        // (only tiles crossing a mask limit), take the row max, then form
+        // p = 2^(s*scale*log2e - m) and the row sum and write P as bf16 pairs over S's first
+        // 64 columns, a quarter (16 columns) at a time.
+        uint32_t sr[128];
+        tmem_ld_32x32b_x128(ts, sr);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c)
+            if (c > lim_c) sr[c] = 0xFF800000u;  // -inf: excluded from the max, 2^-inf = 0
+        }
         float mx8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-        if (!need_mask) {
+        for (int e = 0; e < 8; ++e) mx8[e] = fmax3(u2f(sr[e]), u2f(sr[8 + e]), u2f(sr[16 + e]));
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t sr[64];
-            tmem_ld_32x32b_x64(ts + half * 64, sr);
+        for (int c = 24; c < 120; c += 16)
 #pragma unroll
-            for (int c = 0; c < 64; c += 16)
+          for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], u2f(sr[c + e]), u2f(sr[c + 8 + e]));
 #pragma unroll
-              for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], u2f(sr[c + e]), u2f(sr[c + 8 + e]));
-          }
-        } else {
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            const int c0 = half * 64;
-            if (__all_sync(0xffffffffu, lim_c < c0)) continue;
-            uint32_t sr[64];
-            tmem_ld_32x32b_x64(ts + c0, sr);
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (c0 + c > lim_c) sr[c] = 0xFF800000u;  // -inf
-#pragma unroll
-            for (int c = 0; c < 64; c += 16)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], u2f(sr[c + e]), u2f(sr[c + 8 + e]));
-          }
-        }
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], u2f(sr[120 + e]));
         const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7])));
         const float m_new = fmaxf(m_run, mx * sl2);
         const bool rescale = m_new > m_run + kRescaleThreshold;
@@ -519,48 +504,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l_run *= alpha;
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-        float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
-        // p for 32 columns (in sr) -> 16 packed bf16 pairs
         const uint64_t sl2x2 = pack_f2(sl2, sl2);
         const uint64_t nmx2 = pack_f2(-msub, -msub);
-        auto exp_band = [&](const uint32_t (&sr)[32], uint32_t (&pk)[16]) {
+        uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // 8 independent partial sums, in pairs
+#pragma unroll
+        for (int qtr = 0; qtr < 4; ++qtr) {
+          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[2 * e]), u2f(sr[2 * e + 1])), sl2x2, nmx2));
+            const int c = qtr * 32 + 2 * e;
+            const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
             const float p0 = ex2_approx(x.x);
             const float p1 = ex2_approx(x.y);
-            rs8[(2 * e) % 8] += p0;
-            rs8[(2 * e + 1) % 8] += p1;
+            rs2[e % 4] = fadd2(rs2[e % 4], pack_f2(p0, p1));
             pk[e] = pack_bf16x2(p0, p1);
           }
-        };
-        if (!need_mask) {
-#pragma unroll
-          for (int qtr = 0; qtr < 4; ++qtr) {
-            uint32_t sr[32], pk[16];
-            tmem_ld_32x32b_x32(ts + qtr * 32, sr);
-            exp_band(sr, pk);
-            tmem_st_32x32b_x16(ts + qtr * 16, pk);
-          }
-        } else {
-#pragma unroll 1
-          for (int qtr = 0; qtr < 4; ++qtr) {
-            const int c0 = qtr * 32;
-            uint32_t sr[32], pk[16];
-            if (__all_sync(0xffffffffu, lim_c < c0)) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) pk[e] = 0u;
-            } else {
-              tmem_ld_32x32b_x32(ts + c0, sr);
-#pragma unroll
-              for (int c = 0; c < 32; ++c)
-                if (c0 + c > lim_c) sr[c] = 0xFF800000u;  // -inf: 2^-inf = 0
-              exp_band(sr, pk);
-            }
-            tmem_st_32x32b_x16(ts + qtr * 16, pk);
-          }
+          tmem_st_32x32b_x16(ts + qtr * 16, pk);
         }
-        l_run += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        {
+          const float2 r0 = unpack_f2(fadd2(rs2[0], rs2[1]));
+          const float2 r1 = unpack_f2(fadd2(rs2[2], rs2[3]));
+          l_run += (r0.x + r0.y) + (r1.x + r1.y);
+        }
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
           // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled, and
           // PV_t(j) is not issued before this warpgroup arrives on p_full.
