@@ -19,7 +19,10 @@
 // fp32 accumulators, row r of a tile in lane r.  The bf16 probabilities P_t overwrite the
 // first 64 columns of S_t (two values per column) and feed the PV MMA from tensor memory.
 // Shared memory: Q0, Q1 and a ring of K/V tiles (4 stages at D=128), in the 128-byte-swizzled
-// K-major layout TMA writes (V is read MN-major by the PV MMA).
+// K-major layout TMA writes (V is read MN-major by the PV MMA).  Each Q tile has its own
+// full/empty barriers: the next unit's Q0 loads as soon as this unit's last S0 MMA has
+// run (a tile earlier than Q1 under a causal mask), and the next unit's S0_0 is issued
+// right behind this unit's last PV1.
 // The MMA and TMA roles run as whole converged warps that issue through one elected lane:
 // their operands stay warp-uniform, so they need few issue slots while the softmax
 // warpgroups keep the SM's schedulers busy.
@@ -78,8 +81,9 @@ struct Layout {
   static constexpr int kStageOutBytes = kBlockM * 128;
   static constexpr int kOutOff = kKVOff + kStages * kTileBytes;
   static constexpr int kBarOff = kOutOff + kQTiles * kStageOutBytes;
-  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], o_free[2], drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1;
+  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2],
+  // o_free[2], drain
+  static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // abort flag, tmem slot
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
@@ -248,15 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- setup
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0;
-  const uint32_t q_empty = bar0 + 8u;
-  auto kv_full = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (2 + L::kStages + s); };
-  auto s_full = [&](int t) { return bar0 + 8u * (2 + 2 * L::kStages + t); };
-  auto p_full = [&](int t) { return bar0 + 8u * (4 + 2 * L::kStages + t); };
-  auto o_done = [&](int t) { return bar0 + 8u * (6 + 2 * L::kStages + t); };
-  auto o_free = [&](int t) { return bar0 + 8u * (8 + 2 * L::kStages + t); };
-  const uint32_t bar_drain = bar0 + 8u * (10 + 2 * L::kStages);
+  auto q_full = [&](int t) { return bar0 + 8u * t; };        // Q tile t loaded
+  auto q_empty = [&](int t) { return bar0 + 8u * (2 + t); };  // Q tile t's last S MMA done
+  auto kv_full = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (4 + L::kStages + s); };
+  auto s_full = [&](int t) { return bar0 + 8u * (4 + 2 * L::kStages + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (6 + 2 * L::kStages + t); };
+  auto o_done = [&](int t) { return bar0 + 8u * (8 + 2 * L::kStages + t); };
+  auto o_free = [&](int t) { return bar0 + 8u * (10 + 2 * L::kStages + t); };
+  const uint32_t bar_drain = bar0 + 8u * (12 + 2 * L::kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff + 8);
   const WaitCtl wc{abort_flag, a.err, a.timeout_ns};
@@ -266,8 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto kv_addr = [&](int s) { return s_base + L::kKVOff + s * L::kTileBytes; };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(q_full(t), 1);
+      mbar_init(q_empty(t), 1);
+    }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
@@ -300,38 +306,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer (whole warp)
+    // Order per unit: Q0, K_0, Q1, V_0, K_1, V_1, ...  Each Q tile waits only for its own
+    // tile's last S MMA of the previous unit, so the next unit's Q0 (and K_0) arrive in
+    // time for the MMA warp to start S0_0 before the current unit's last tile-1 step.
     int uc = 0, it = 0;
-    bool ok = true, q_pending = false;
+    int q_issued[kQTiles] = {0, 0};
+    bool ok = true;
+    auto load_q = [&](int t, const Unit& u) {
+      if (!(ok = wait_bar_warp(q_empty(t), (uc & 1) ^ 1, wc))) return;
+      mbar_arrive_expect_tx_elect(q_full(t), L::kTileBytes);
+      for (int kb = 0; kb < L::kKBlocks; ++kb)
+        tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, q_full(t), kb * 64,
+                          u.q_base + u.r0 + t * kBlockM, u.h, u.b);
+      ++q_issued[t];
+    };
+    auto load_kv = [&](int j, int which, const Unit& u) {  // K_j (which = 0) or V_j
+      const int s = it % L::kStages;
+      if (!(ok = wait_bar_warp(kv_empty(s), ((it / L::kStages) & 1) ^ 1, wc))) return;
+      mbar_arrive_expect_tx_elect(kv_full(s), L::kTileBytes);
+      const CUtensorMap* tm = which ? &tm_v : &tm_k;
+      for (int kb = 0; kb < L::kKBlocks; ++kb)
+        tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64,
+                          u.k_base + j * kBlockN, u.hk, u.b);
+      ++it;
+    };
     for (int k = 0; k < n_rounds && ok; ++k) {
       const int i = unit_at(k, cta, G);
       Unit u;
       if (i >= a.total_units || !decode_unit(a, i, u) || u.n_tiles == 0) continue;
-      // Q of this unit may overwrite the previous unit's Q once its last S MMA was issued.
-      if (!(ok = wait_bar_warp(q_empty, (uc & 1) ^ 1, wc))) break;
-      mbar_arrive_expect_tx_elect(q_full, kQTiles * L::kTileBytes);
-      for (int t = 0; t < kQTiles; ++t)
-        for (int kb = 0; kb < L::kKBlocks; ++kb)
-          tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, q_full, kb * 64,
-                            u.q_base + u.r0 + t * kBlockM, u.h, u.b);
-      q_pending = true;
-      for (int j = 0; j < u.n_tiles && ok; ++j) {
-        for (int which = 0; which < 2; ++which, ++it) {  // K_j then V_j
-          const int s = it % L::kStages;
-          if (!(ok = wait_bar_warp(kv_empty(s), ((it / L::kStages) & 1) ^ 1, wc))) break;
-          mbar_arrive_expect_tx_elect(kv_full(s), L::kTileBytes);
-          const CUtensorMap* tm = which ? &tm_v : &tm_k;
-          for (int kb = 0; kb < L::kKBlocks; ++kb)
-            tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64,
-                              u.k_base + j * kBlockN, u.hk, u.b);
-        }
+      load_q(0, u);
+      if (ok) load_kv(0, 0, u);
+      if (ok) load_q(1, u);
+      if (ok) load_kv(0, 1, u);
+      for (int j = 1; j < u.n_tiles && ok; ++j) {
+        load_kv(j, 0, u);
+        if (ok) load_kv(j, 1, u);
       }
-      if (ok) {
-        ++uc;
-        q_pending = false;
-      }
+      if (ok) ++uc;
     }
     if (!ok) {  // let every copy this warp issued land before the CTA exits
-      if (q_pending) wait_bar_warp(q_full, uc & 1, wc, false);
+      for (int t = 0; t < kQTiles; ++t)
+        if (q_issued[t] > 0) wait_bar_warp(q_full(t), (q_issued[t] - 1) & 1, wc, false);
       for (int k = max(0, it - L::kStages); k < it; ++k)
         wait_bar_warp(kv_full(k % L::kStages), (k / L::kStages) & 1, wc, false);
     }
@@ -348,33 +363,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     // uc: units; uc_t / jg_t: units and key tiles of Q tile t (its barrier phases).
     int uc = 0, it = 0, uc0 = 0, uc1 = 0, jg0 = 0, jg1 = 0;
     bool ok = true;
-    for (int k = 0; k < n_rounds && ok; ++k) {
-      const int i = unit_at(k, cta, G);
-      Unit u;
-      if (i >= a.total_units || !decode_unit(a, i, u) || u.n_tiles == 0) continue;
+    // The next unit with work at or after round k (k_out = its round), false if none.
+    auto next_unit = [&](int k, int& k_out, Unit& uo) {
+      for (; k < n_rounds; ++k) {
+        const int i = unit_at(k, cta, G);
+        if (i < a.total_units && decode_unit(a, i, uo) && uo.n_tiles > 0) {
+          k_out = k;
+          return true;
+        }
+      }
+      return false;
+    };
+    Unit u;
+    int ku = 0;
+    bool have = next_unit(0, ku, u);
+    bool s0_issued = false;  // S0_0 of unit u was issued at the end of the previous unit
+    while (have && ok) {
+      Unit un;
+      int kn = 0;
+      const bool have_next = next_unit(ku + 1, kn, un);
       const int n = u.n_tiles;
       const int n0 = u.n0;
-      if (!(ok = wait_bar_warp(q_full, uc & 1, wc))) break;
-      const int sk0 = it % L::kStages;
-      if (!(ok = wait_bar_warp(kv_full(sk0), (it / L::kStages) & 1, wc))) break;
-      ++it;
-      tc_fence_after();
+      const int ik0 = it++;  // K_0's ring position
+      const int sk0 = ik0 % L::kStages;
       // S_t(0): S_t is free (its last P was consumed by the previous unit's PV_t, which
       // was issued before this and executes first).
-      if (n0 > 0) {
-        issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk0));
-        mma_commit_elect(s_full(0));
+      if (!s0_issued) {
+        if (!(ok = wait_bar_warp(q_full(0), uc & 1, wc))) break;
+        if (!(ok = wait_bar_warp(kv_full(sk0), (ik0 / L::kStages) & 1, wc))) break;
+        tc_fence_after();
+        if (n0 > 0) {
+          issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk0));
+          mma_commit_elect(s_full(0));
+        }
+        if (n0 <= 1) mma_commit_elect(q_empty(0));  // Q0's last S MMA was issued
       }
+      s0_issued = false;
+      if (!(ok = wait_bar_warp(q_full(1), uc & 1, wc))) break;
+      if (!(ok = wait_bar_warp(kv_full(sk0), (ik0 / L::kStages) & 1, wc))) break;
+      tc_fence_after();
       issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk0));
       mma_commit_elect(s_full(1));
       mma_commit_elect(kv_empty(sk0));
-      if (n == 1) mma_commit_elect(q_empty);
+      if (n == 1) mma_commit_elect(q_empty(1));
       for (int j = 0; j < n && ok; ++j) {
-        const int sv = it % L::kStages;
-        if (!(ok = wait_bar_warp(kv_full(sv), (it / L::kStages) & 1, wc))) break;
-        ++it;
         const bool more = j + 1 < n;
-        int sk = 0;
+        const int iv = it;       // V_j's ring position
+        const int ik = it + 1;   // K_{j+1}'s
+        it += more ? 2 : 1;
+        const int sv = iv % L::kStages;
+        const int sk = ik % L::kStages;
+        if (!(ok = wait_bar_warp(kv_full(sv), (iv / L::kStages) & 1, wc))) break;
         // Q tile 0 (only while its rows still see keys): PV0_j, then S0_{j+1}
         if (j < n0) {
           if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
@@ -385,13 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++jg0;
         }
         if (more) {
-          sk = it % L::kStages;
-          if (!(ok = wait_bar_warp(kv_full(sk), (it / L::kStages) & 1, wc))) break;
-          ++it;
+          if (!(ok = wait_bar_warp(kv_full(sk), (ik / L::kStages) & 1, wc))) break;
           tc_fence_after();
           if (j + 1 < n0) {
             issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk));
             mma_commit_elect(s_full(0));
+            if (j + 2 == n0) mma_commit_elect(q_empty(0));
           }
         }
         // Q tile 1: PV1_j, then S1_{j+1}
@@ -404,17 +442,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk));
           mma_commit_elect(s_full(1));
           mma_commit_elect(kv_empty(sk));
-          if (j + 2 == n) mma_commit_elect(q_empty);  // the unit's last S MMA was issued
+          if (j + 2 == n) mma_commit_elect(q_empty(1));  // the unit's last S1 MMA was issued
         } else {
           mma_commit_elect(o_done(1));
+          if (have_next && un.n0 > 0) {
+            // The next unit's S0_0 right behind this unit's last PV1 (its Q0 was loaded
+            // after this unit's last S0 MMA), before this warp decodes units and waits
+            // for Q1.  S0 is free: this unit's last PV0 precedes it in issue order.
+            const int ikn = it;  // the next unit's K_0 follows V_{n-1} in the ring
+            if (!(ok = wait_bar_warp(q_full(0), (uc + 1) & 1, wc))) break;
+            if (!(ok = wait_bar_warp(kv_full(ikn % L::kStages), (ikn / L::kStages) & 1, wc))) break;
+            tc_fence_after();
+            issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(ikn % L::kStages));
+            mma_commit_elect(s_full(0));
+            if (un.n0 <= 1) mma_commit_elect(q_empty(0));
+            s0_issued = true;
+          }
         }
         ++jg1;
       }
-      if (ok) {
-        ++uc;
-        ++uc1;
-        if (n0 > 0) ++uc0;
-      }
+      if (!ok) break;
+      ++uc;
+      ++uc1;
+      if (n0 > 0) ++uc0;
+      u = un;
+      ku = kn;
+      have = have_next;
     }
     if (!ok) {  // wait for every MMA this warp issued
       mma_commit_elect(bar_drain);
