@@ -4,10 +4,11 @@
 // With one query row per head each K/V element is used once, so the work is a stream
 // of K and V from HBM (about 1 FLOP per byte); tensor-core tiles would be 128-fold
 // padding.  The keys of one (batch, head) are split over a thread-block cluster of CS
-// CTAs (CS = 1..8, chosen so the grid fits in one wave); inside a CTA one producer warp
-// streams tiles of T keys (T * D = 4096 elements: 8 KiB of K plus 8 KiB of V) through a
-// ring of shared-memory stages with TMA, so up to 192 KiB per SM are in flight whatever
-// the register budget.  Eight consumer warps take the tiles round robin.  Lane l holds
+// CTAs (CS = 1..16, above 8 only where the device schedules it, chosen from how many such
+// clusters stay resident, to minimise waves x keys per CTA); inside a CTA one
+// producer warp streams tiles of T keys (T * D = 4096 elements: 8 KiB of K plus 8 KiB of
+// V) through a ring of shared-memory stages with TMA, so up to 192 KiB per SM are in
+// flight whatever the register budget.  Eight consumer warps take the tiles round robin.  Lane l holds
 // head-dim elements [l*V, l*V+V) of every row (V = D/32) and reads them from shared
 // memory (one 256/128-byte row per warp instruction); a halving butterfly leaves key l's
 // full score on lane l, followed by the base-2 online softmax and one pass over the V
@@ -34,7 +35,6 @@ namespace {
 
 constexpr int kWarps = 8;                      // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;    // + one producer warp
-constexpr int kMaxCluster = 8;
 constexpr int kStages = 12;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, int MQ>
-cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, const DecArgs& a, int B, int H,
+cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, int B, int H,
                       cudaStream_t stream) {
   using L = DecLayout<D>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory");
@@ -445,11 +445,57 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, const DecArg
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
+  // Per cluster size c = 1..16: how many clusters the device keeps resident at once (0: c
+  // not schedulable).  Sizes above 8 are non-portable and opted into explicitly.
+  constexpr int kSizes = 16;
+  static std::atomic<int> resident[kMaxDevices][kSizes];
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(fmha_decode_kernel<D, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kAlloc);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(1, std::memory_order_release);
+    const bool big_ok = cudaFuncSetAttribute(fmha_decode_kernel<D, MQ>,
+                                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    for (int si = 0; si < kSizes; ++si) {
+      const int c = si + 1;
+      int n = 0;
+      if (c <= 8 || big_ok) {
+        cudaLaunchConfig_t q{};
+        q.gridDim = dim3(static_cast<unsigned>(c));
+        q.blockDim = dim3(kThreads);
+        q.dynamicSmemBytes = L::kAlloc;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = static_cast<unsigned>(c);
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, fmha_decode_kernel<D, MQ>, &q) != cudaSuccess) n = 0;
+      }
+      resident[dev][si].store(n, std::memory_order_relaxed);
+    }
+    (void)cudaGetLastError();  // a refused query only removes that size
+    opted_in[dev].store(1, std::memory_order_release);
+  }
+  // Cluster size: fewest waves x keys per CTA, i.e. the smallest ceil(units / resident) / c,
+  // with every CTA keeping at least two tiles per consumer warp (ties: the smaller c).
+  {
+    const long long units = static_cast<long long>(B) * H;
+    const long long tiles = (static_cast<long long>(a.Mkv) + L::kT - 1) / L::kT;
+    int best = 1;
+    double best_cost = 1e300;
+    for (int si = 0; si < kSizes; ++si) {
+      const int c = si + 1;
+      const int n = resident[dev][si].load(std::memory_order_relaxed);
+      if (n <= 0 || (c > 1 && tiles / c < 2 * kWarps)) continue;
+      const double cost = static_cast<double>((units + n - 1) / n) / c;
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best = c;
+      }
+    }
+    a.cs = best;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(H * a.cs), static_cast<unsigned>(B));
@@ -475,18 +521,6 @@ cudaError_t launch_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecArgs
   return launch_dm<D, 8>(tk, tv, a, B, H, stream);
 }
 
-int sm_count() {
-  constexpr int kMaxDevices = 64;
-  static int cache[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-  if (cache[dev] == 0) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = n > 0 ? n : 148;
-  }
-  return cache[dev];
-}
 
 }  // namespace
 
@@ -526,13 +560,7 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   a.lse = p.lse;
   a.err = ctl.err;
   a.timeout_ns = ctl.timeout_ns;
-  // Cluster size: the grid stays within one wave of one CTA per SM, and every CTA keeps
-  // at least two tiles per consumer warp.
-  const long long units = static_cast<long long>(p.B) * p.H;
-  const long long tiles = (static_cast<long long>(p.Mkv) + T - 1) / T;
-  int cs = 1;
-  while (cs < kMaxCluster && units * cs * 2 <= sm_count() && tiles / (cs * 2) >= 2 * kWarps) cs *= 2;
-  a.cs = cs;
+  a.cs = 1;  // chosen per kernel instantiation from the device's cluster residency
   *why = "decode kernel launch failed";
   if (D == 128) return launch_d<128>(tk, tv, a, p.B, p.H, stream);
   return launch_d<64>(tk, tv, a, p.B, p.H, stream);

@@ -513,6 +513,29 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
                                       "eager_partial_GB/s": kv_bytes / t_eager / 1e9,
                                       "launches": 17}
     del graph
+    # the same step as one call over all 32768 keys (the kernel splits keys on-chip)
+    fo32 = torch.empty((w.B, w.M, w.H, w.Kv), dtype=torch.float32, device=dev)
+    one = lambda: fa.attn_partial(qd, kd, vd, scale=w.scale, out=fo32, lse=fl)  # noqa: E731
+    for _ in range(3):
+        one()
+    t_one = _time_it(one, 10, stream, flush)
+    res["decode_single_launch_16x32768"] = {"us": t_one * 1e6, "GB/s": kv_bytes / t_one / 1e9,
+                                            "frac_hbm": kv_bytes / t_one / 1e9 / peaks["hbm_gbs"],
+                                            "launches": 1}
+    # few heads: 1 x 1 query, 131072 keys, 8 heads (the keys of each head split over a cluster)
+    q1, k1, v1 = inputs.qkv(1, 1, 131072, 8, 128, seed=5)
+    q1, k1, v1 = q1.to(dev), k1.to(dev), v1.to(dev)
+    o1 = torch.empty((1, 1, 8, 128), dtype=torch.float32, device=dev)
+    l1 = torch.empty((1, 8, 1), dtype=torch.float32, device=dev)
+    few = lambda: fa.attn_partial(q1, k1, v1, scale=w.scale, out=o1, lse=l1)  # noqa: E731
+    for _ in range(3):
+        few()
+    t_few = _time_it(few, 10, stream, flush)
+    b_few = (k1.numel() + v1.numel()) * 2
+    res["decode_single_launch_1x131072x8"] = {"us": t_few * 1e6, "GB/s": b_few / t_few / 1e9,
+                                              "frac_hbm": b_few / t_few / 1e9 / peaks["hbm_gbs"],
+                                              "launches": 1}
+    del q1, k1, v1
     del kd, vd, k, v
     # varlen packed block-diagonal causal
     w = inputs.WORKLOADS["varlen_packed"]

@@ -80,12 +80,19 @@ def test_fwd_decode_rows(M, D, mask):
 @pytest.mark.parametrize("M", [1, 3, 8])
 def test_decode_cluster_split_long_keys(M):
     """Few heads and many keys: the decode kernel splits each head's keys over a cluster
-    of 8 CTAs and merges them through distributed shared memory."""
+    of CTAs (16 where the device schedules it, else 8) and merges them through distributed
+    shared memory."""
     _fwd_case(1, M, 20000, 2, 128, "none", seed=21)
     q, k, v = inputs.qkv(1, M, 20000, 2, 128, seed=22)
     o, l_ = fa.attn_partial(*to_dev(q, k, v), mask="causal", kv_offset=-19990)
     ro, rl = oracle.attention_partial(f32(q), f32(k), f32(v), 1 / 128 ** 0.5, 1, kv_offset=-19990)
     compare(o.double().cpu().numpy(), l_.double().cpu().numpy(), ro, rl, "cluster causal partial")
+
+
+@pytest.mark.parametrize("B,H,Mkv,D", [(1, 8, 20000, 128), (2, 2, 33000, 128), (1, 4, 40000, 64)])
+def test_decode_cluster_sizes(B, H, Mkv, D):
+    """Cluster sizes 8 and 16 (and D = 64) over long key ranges, one query row."""
+    _fwd_case(B, 1, Mkv, H, D, "none", seed=23)
 
 
 def test_fwd_strided_views_and_shared_head():
