@@ -30,6 +30,20 @@ Allowed sets (MSLK kernel reference, "Attention - Biases & masks"):
                             inside each block, on positions relative to the block
                             starts (kv_offset added to the key position).
 
+Alignment and local windows (same page: ``LowerTriangularFromBottomRightMask``,
+``LowerTriangularFromBottomRightLocalAttentionMask``, ``LocalAttentionFromBottomRightMask``,
+``BlockDiagonalCausalFromBottomRightMask``, ``BlockDiagonalCausalLocalAttentionMask``,
+``BlockDiagonalCausalLocalAttentionFromBottomRightMask``).  The pages name these without
+formulas; the reading used here is the plainest one, on positions p_i (query) and p_j
+(key, kv_offset added) inside a block of Lq queries and Lk keys:
+  * ``bottom_right``: the diagonal is moved so that the last query lines up with the last
+    key: shift = Lk - Lq (0 for top-left alignment);
+  * causal kinds keep p_j - p_i <= shift;
+  * ``window_left`` = wl keeps p_j - p_i >= shift - wl (a causal local window of
+    ``window_size`` w keeps the w keys ending at the diagonal: wl = w - 1);
+  * ``window_right`` = wr (non-causal kinds only) keeps p_j - p_i <= shift + wr.
+So every mask is a band  lo <= p_j - p_i <= hi  (either side possibly unbounded).
+
 Partial attention (``memory_efficient_attention_partial``) is the same definition over
 one disjoint key/value chunk; ``kv_offset`` is the chunk's first key position, used only
 by the causal masks.
@@ -80,20 +94,40 @@ def _scale64(scale: float) -> float:
     return float(np.float32(scale))
 
 
-def _block(qb, kb, vb, scale64, causal, q_pos0, k_pos0):
+def _band(mask_kind, bottom_right, window_left, window_right, Lq, Lk):
+    """(lo, hi) bounds on p_j - p_i for a block of Lq queries and Lk keys (None = open)."""
+    if window_left is not None and window_left < 0:
+        raise ValueError("window_left must be >= 0")
+    if window_right is not None and window_right < 0:
+        raise ValueError("window_right must be >= 0")
+    causal = mask_kind in (MASK_CAUSAL, MASK_BLOCKDIAG_CAUSAL)
+    if causal and window_right not in (None, 0):
+        raise ValueError("causal masks have no right window")
+    shift = (Lk - Lq) if bottom_right else 0
+    if causal:
+        hi = shift
+    else:
+        hi = None if window_right is None else shift + window_right
+    lo = None if window_left is None else shift - window_left
+    return lo, hi
+
+
+def _block(qb, kb, vb, scale64, lo, hi, q_pos0, k_pos0):
     """Attention of one query block against one key block (one batch, one head).
 
-    qb [Lq, K], kb [Lk, K], vb [Lk, Kv] in float64.  ``q_pos0``/``k_pos0`` are the
-    positions of the first query/key used by the causal comparison (key j is allowed
-    for query i iff k_pos0 + j <= q_pos0 + i).
+    qb [Lq, K], kb [Lk, K], vb [Lk, Kv] in float64.  Key j is allowed for query i iff
+    lo <= (k_pos0 + j) - (q_pos0 + i) <= hi (a None bound is open).
     Returns out [Lq, Kv] and lse [Lq].
     """
     Lq, Lk = qb.shape[0], kb.shape[0]
     x = scale64 * (qb @ kb.T)                                   # [Lq, Lk]
-    if causal:
-        qi = q_pos0 + np.arange(Lq)[:, None]
-        kj = k_pos0 + np.arange(Lk)[None, :]
-        allowed = kj <= qi
+    if lo is not None or hi is not None:
+        d = (k_pos0 + np.arange(Lk)[None, :]) - (q_pos0 + np.arange(Lq)[:, None])
+        allowed = np.ones((Lq, Lk), dtype=bool)
+        if hi is not None:
+            allowed &= d <= hi
+        if lo is not None:
+            allowed &= d >= lo
         x = np.where(allowed, x, -np.inf)
     if Lk == 0:
         m = np.full(Lq, -np.inf)
@@ -124,12 +158,14 @@ def _check_shapes(q, k, v):
 
 
 def attention_head(q, k, v, b, h, scale, mask_kind=MASK_NONE, cu_seqlens_q=None,
-                   cu_seqlens_k=None, kv_offset=0, rows=None):
+                   cu_seqlens_k=None, kv_offset=0, rows=None, bottom_right=False,
+                   window_left=None, window_right=None):
     """out [M, Kv] and lse [M] (float64) for one (batch b, head h).
 
     ``rows`` (optional, dense masks only) restricts the result to those query rows;
     each row is independent of the others in the definition, so this is the same
-    arithmetic on fewer rows.
+    arithmetic on fewer rows.  ``bottom_right`` / ``window_left`` / ``window_right``
+    select the alignment and local window described in the module docstring.
     """
     B, M, H, K, Mkv, Kv = _check_shapes(q, k, v)
     hk = h if k.shape[2] == H else 0
@@ -152,29 +188,31 @@ def attention_head(q, k, v, b, h, scale, mask_kind=MASK_NONE, cu_seqlens_q=None,
             qs, qe, ks, ke = cq[s], cq[s + 1], ck[s], ck[s + 1]
             if qe == qs:
                 continue
-            o_s, l_s = _block(qb_all[qs:qe], kb_all[ks:ke], vb_all[ks:ke], s64,
-                              mask_kind == MASK_BLOCKDIAG_CAUSAL, 0, kv_offset)
+            lo, hi = _band(mask_kind, bottom_right, window_left, window_right, qe - qs, ke - ks)
+            o_s, l_s = _block(qb_all[qs:qe], kb_all[ks:ke], vb_all[ks:ke], s64, lo, hi, 0,
+                              kv_offset)
             out[qs:qe] = o_s
             lse[qs:qe] = l_s
         return out, lse
     if mask_kind not in (MASK_NONE, MASK_CAUSAL):
         raise ValueError(f"unknown mask kind {mask_kind}")
+    lo, hi = _band(mask_kind, bottom_right, window_left, window_right, M, Mkv)
     if rows is None:
         qb = np.asarray(q[b, :, h, :], dtype=np.float64)
-        return _block(qb, kb_all, vb_all, s64, mask_kind == MASK_CAUSAL, 0, kv_offset)
+        return _block(qb, kb_all, vb_all, s64, lo, hi, 0, kv_offset)
     rows = np.asarray(rows, dtype=np.int64)
     out = np.empty((len(rows), Kv))
     lse = np.empty(len(rows))
     for n, i in enumerate(rows):
         qb = np.asarray(q[b, i:i + 1, h, :], dtype=np.float64)
-        o_i, l_i = _block(qb, kb_all, vb_all, s64, mask_kind == MASK_CAUSAL, int(i), kv_offset)
+        o_i, l_i = _block(qb, kb_all, vb_all, s64, lo, hi, int(i), kv_offset)
         out[n] = o_i[0]
         lse[n] = l_i[0]
     return out, lse
 
 
 def attention(q, k, v, scale, mask_kind=MASK_NONE, cu_seqlens_q=None, cu_seqlens_k=None,
-              kv_offset=0):
+              kv_offset=0, bottom_right=False, window_left=None, window_right=None):
     """Full forward: out [B, M, H, Kv] and lse [B, H, M], float64.
 
     ``memory_efficient_attention_forward_requires_grad`` returns exactly this pair.
@@ -185,21 +223,24 @@ def attention(q, k, v, scale, mask_kind=MASK_NONE, cu_seqlens_q=None, cu_seqlens
     for b in range(B):
         for h in range(H):
             o, l = attention_head(q, k, v, b, h, scale, mask_kind, cu_seqlens_q,
-                                  cu_seqlens_k, kv_offset)
+                                  cu_seqlens_k, kv_offset, None, bottom_right, window_left,
+                                  window_right)
             out[b, :, h, :] = o
             lse[b, h, :] = l
     return out, lse
 
 
 def attention_partial(q, k_chunk, v_chunk, scale, mask_kind=MASK_NONE, cu_seqlens_q=None,
-                      cu_seqlens_k=None, kv_offset=0):
+                      cu_seqlens_k=None, kv_offset=0, window_left=None, window_right=None):
     """Partial attention over one disjoint K/V chunk (same definition, chunk keys only).
 
     ``kv_offset`` is the position of the chunk's first key in the full key sequence
-    (inside each packed sequence, for the block-diagonal masks); only causal masks use it.
+    (inside each packed sequence, for the block-diagonal masks); masks compare it with the
+    query position (top-left alignment: a bottom-right alignment over the full key
+    sequence is expressed by folding Lk_full - Lq into kv_offset).
     """
     return attention(q, k_chunk, v_chunk, scale, mask_kind, cu_seqlens_q, cu_seqlens_k,
-                     kv_offset)
+                     kv_offset, False, window_left, window_right)
 
 
 def merge_attentions(out_split, lse_split):

@@ -41,31 +41,47 @@ def _seq_of(pos, cu):
     raise IndexError(pos)
 
 
-def materialize_bias(kind, M, Mkv, kv_offset=0, cu_q=None, cu_k=None):
-    """Dense additive bias [M][Mkv] of 0.0 / -inf, one element at a time."""
+def materialize_bias(kind, M, Mkv, kv_offset=0, cu_q=None, cu_k=None, bottom_right=False,
+                     window_left=None, window_right=None):
+    """Dense additive bias [M][Mkv] of 0.0 / -inf, one element at a time.
+
+    Alignment and windows follow the mask classes' one-line descriptions: a bottom-right
+    mask lines the last query up with the last key of its block (query row i of a block
+    of Lq rows is paired with key row i + Lk - Lq); a causal local window of w keys keeps
+    the w keys ending at the paired key; a non-causal local window keeps the keys from
+    window_left before to window_right after the paired key.
+    """
     bias = [[0.0] * Mkv for _ in range(M)]
     for i in range(M):
         for j in range(Mkv):
-            if kind == 0:                                   # no mask
+            if kind in (0, 1):
+                qi, kj, Lq, Lk = i, kv_offset + j, M, Mkv
                 keep = True
-            elif kind == 1:                                 # top-left causal
-                keep = (kv_offset + j) <= i
             else:                                           # block-diagonal (+ causal)
                 si, sj = _seq_of(i, cu_q), _seq_of(j, cu_k)
                 keep = si == sj
-                if keep and kind == 3:
-                    keep = (kv_offset + j - cu_k[sj]) <= (i - cu_q[si])
+                qi, kj = i - cu_q[si], kv_offset + j - cu_k[sj]
+                Lq, Lk = cu_q[si + 1] - cu_q[si], cu_k[sj + 1] - cu_k[sj]
+            paired = qi + (Lk - Lq if bottom_right else 0)   # the key row query qi lines up with
+            if keep and kind in (1, 3):
+                keep = kj <= paired
+            if keep and window_right is not None:
+                keep = kj <= paired + window_right
+            if keep and window_left is not None:
+                keep = kj >= paired - window_left
             bias[i][j] = 0.0 if keep else NEG_INF
     return bias
 
 
-def brute_attention(q, k, v, scale, kind=0, cu_q=None, cu_k=None, kv_offset=0):
+def brute_attention(q, k, v, scale, kind=0, cu_q=None, cu_k=None, kv_offset=0,
+                    bottom_right=False, window_left=None, window_right=None):
     """Loops over (b, h, i, j, d) with Python floats. Returns out [B][M][H][Kv], lse [B][H][M]."""
     q, k, v = (np.asarray(t, dtype=np.float64).tolist() for t in (q, k, v))
     B, M, H, K = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
     Mkv, Hk, Kv = len(k[0]), len(k[0][0]), len(v[0][0][0])
     s = float(np.float32(scale))
-    bias = materialize_bias(kind, M, Mkv, kv_offset, cu_q, cu_k)
+    bias = materialize_bias(kind, M, Mkv, kv_offset, cu_q, cu_k, bottom_right, window_left,
+                            window_right)
     out = [[[[0.0] * Kv for _ in range(H)] for _ in range(M)] for _ in range(B)]
     lse = [[[NEG_INF] * M for _ in range(H)] for _ in range(B)]
     for b in range(B):
@@ -491,7 +507,116 @@ def pin_widen_bf16(orc):
     assert np.array_equal(np.isnan(got), np.isnan(ref)), "bf16 NaN patterns"
 
 
+# --------------------------------------------------------------------------------------
+# alignment and local windows
+# --------------------------------------------------------------------------------------
+
+def pin_window_single_key(orc):
+    """A window of one key (causal window_left = 0, or non-causal 0/0) leaves query i the
+    single paired key i + shift: out_i = v[paired], lse_i = scale * q_i . k[paired]; a
+    query whose paired key falls outside the keys has an empty row."""
+    rng = np.random.default_rng(41)
+    for M, Mkv in ((5, 9), (7, 4), (6, 6)):
+        q = _bf16_round(_rand(rng, (1, M, 2, 8)))
+        k = _bf16_round(_rand(rng, (1, Mkv, 2, 8)))
+        v = _bf16_round(_rand(rng, (1, Mkv, 2, 8)))
+        s = 0.3
+        for br in (False, True):
+            shift = (Mkv - M) if br else 0
+            want_o = np.zeros((1, M, 2, 8))
+            want_l = np.full((1, 2, M), NEG_INF)
+            for i in range(M):
+                j = i + shift
+                if 0 <= j < Mkv:
+                    want_o[0, i] = v[0, j]
+                    for h in range(2):
+                        want_l[0, h, i] = float(np.float32(s)) * float(np.dot(q[0, i, h], k[0, j, h]))
+            for kind, wr in ((orc.MASK_CAUSAL, None), (orc.MASK_NONE, 0)):
+                o, l_ = orc.attention(q, k, v, s, kind, bottom_right=br, window_left=0,
+                                      window_right=wr)
+                _close(o, want_o, 1e-12, f"single-key window out M{M} Mkv{Mkv} br{br} kind{kind}")
+                _close(l_, want_l, 1e-12, f"single-key window lse M{M} Mkv{Mkv} br{br} kind{kind}")
+
+
+def pin_bottom_right_reductions(orc):
+    """Bottom-right causal equals top-left causal when M = Mkv, and with one query it keeps
+    every key (PyTorch's unmasked SDPA); a causal window wider than the keys changes
+    nothing; a non-causal window wider on both sides is no mask."""
+    rng = np.random.default_rng(42)
+    q = _bf16_round(_rand(rng, (2, 6, 2, 16)))
+    k = _bf16_round(_rand(rng, (2, 6, 2, 16)))
+    v = _bf16_round(_rand(rng, (2, 6, 2, 16)))
+    a = orc.attention(q, k, v, 0.25, orc.MASK_CAUSAL, bottom_right=True)
+    b = orc.attention(q, k, v, 0.25, orc.MASK_CAUSAL)
+    _close(a[0], b[0], 0.0, "br == tl causal at M = Mkv (out)")
+    _close(a[1], b[1], 0.0, "br == tl causal at M = Mkv (lse)")
+    q1 = q[:, :1]
+    k9 = _bf16_round(_rand(rng, (2, 9, 2, 16)))
+    v9 = _bf16_round(_rand(rng, (2, 9, 2, 16)))
+    o, l_ = orc.attention(q1, k9, v9, 0.25, orc.MASK_CAUSAL, bottom_right=True)
+    tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(t.transpose(0, 2, 1, 3))) for t in (q1, k9, v9))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=float(np.float32(0.25)))
+    _close(o, ref.transpose(1, 2).numpy(), 1e-12, "br causal, one query = no mask")
+    x = torch.einsum("bhik,bhjk->bhij", tq, tk) * float(np.float32(0.25))
+    _close(l_, torch.logsumexp(x, dim=-1).numpy(), 1e-12, "br causal, one query lse")
+    wide = orc.attention(q, k9, v9, 0.25, orc.MASK_CAUSAL, window_left=20)
+    base = orc.attention(q, k9, v9, 0.25, orc.MASK_CAUSAL)
+    _close(wide[0], base[0], 0.0, "wide causal window (out)")
+    both = orc.attention(q, k9, v9, 0.25, orc.MASK_NONE, bottom_right=True, window_left=20,
+                         window_right=20)
+    none = orc.attention(q, k9, v9, 0.25, orc.MASK_NONE)
+    _close(both[0], none[0], 0.0, "wide local window = no mask (out)")
+    _close(both[1], none[1], 0.0, "wide local window = no mask (lse)")
+
+
+def pin_band_bruteforce(orc):
+    """Windows and bottom-right alignment against the element-by-element brute force,
+    dense and block-diagonal (blocks of unequal query and key lengths)."""
+    rng = np.random.default_rng(43)
+    q = _bf16_round(_rand(rng, (1, 7, 2, 8)))
+    k = _bf16_round(_rand(rng, (1, 10, 2, 8)))
+    v = _bf16_round(_rand(rng, (1, 10, 2, 8)))
+    dense = [(1, True, None, None), (1, False, 2, None), (1, True, 3, None),
+             (0, True, 2, 1), (0, False, 0, 3), (0, True, 4, 0)]
+    for kind, br, wl, wr in dense:
+        o, l_ = orc.attention(q, k, v, 0.5, kind, bottom_right=br, window_left=wl,
+                              window_right=wr)
+        bo, bl = brute_attention(q, k, v, 0.5, kind, bottom_right=br, window_left=wl,
+                                 window_right=wr)
+        _close(o, bo, 1e-12, f"band out kind{kind} br{br} wl{wl} wr{wr}")
+        _close(l_, bl, 1e-12, f"band lse kind{kind} br{br} wl{wl} wr{wr}")
+    cu_q, cu_k = [0, 3, 7], [0, 6, 10]
+    for kind, br, wl in ((3, True, None), (3, False, 1), (3, True, 2), (2, True, None)):
+        kw = {} if kind == 3 else {"window_left": 1, "window_right": 1}
+        if kind == 3:
+            kw = {"window_left": wl}
+        o, l_ = orc.attention(q, k, v, 0.5, kind, cu_q, cu_k, bottom_right=br, **kw)
+        bo, bl = brute_attention(q, k, v, 0.5, kind, cu_q, cu_k, bottom_right=br, **kw)
+        _close(o, bo, 1e-12, f"blockdiag band out kind{kind} br{br} {kw}")
+        _close(l_, bl, 1e-12, f"blockdiag band lse kind{kind} br{br} {kw}")
+
+
+def pin_window_split_merge(orc):
+    """A windowed causal forward equals the merge of windowed partials over any chunking
+    (each chunk's kv_offset carries its key positions)."""
+    rng = np.random.default_rng(44)
+    q = _bf16_round(_rand(rng, (1, 9, 2, 8)))
+    k = _bf16_round(_rand(rng, (1, 9, 2, 8)))
+    v = _bf16_round(_rand(rng, (1, 9, 2, 8)))
+    full = orc.attention(q, k, v, 0.4, orc.MASK_CAUSAL, window_left=3)
+    for bounds in (((0, 4), (4, 9)), ((0, 2), (2, 5), (5, 9))):
+        parts = [orc.attention_partial(q, k[:, a:b], v[:, a:b], 0.4, orc.MASK_CAUSAL,
+                                       kv_offset=a, window_left=3) for a, b in bounds]
+        o, l_ = orc.merge_attentions([p[0] for p in parts], [p[1] for p in parts])
+        _close(o, full[0], 1e-12, f"windowed split {bounds} (out)")
+        _close(l_, full[1], 1e-12, f"windowed split {bounds} (lse)")
+
+
 PINS = [
+    pin_window_single_key,
+    pin_bottom_right_reductions,
+    pin_band_bruteforce,
+    pin_window_split_merge,
     pin_bruteforce,
     pin_torch_sdpa,
     pin_single_key,

@@ -17,9 +17,18 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "attention.py")
 
 MUTANTS = {
-    "causal_strict_diagonal": ("allowed = kj <= qi", "allowed = kj < qi"),
-    "causal_ignores_offset": ("kj = k_pos0 + np.arange(Lk)[None, :]",
-                              "kj = np.arange(Lk)[None, :]"),
+    "causal_strict_diagonal": ("allowed &= d <= hi", "allowed &= d < hi"),
+    "causal_ignores_offset": ("d = (k_pos0 + np.arange(Lk)[None, :])", "d = (np.arange(Lk)[None, :])"),
+    "window_left_off_by_one": ("allowed &= d >= lo", "allowed &= d > lo"),
+    "window_left_ignored": ("allowed &= d >= lo", "allowed &= d >= d"),
+    "bottom_right_shift_sign": ("shift = (Lk - Lq) if bottom_right else 0",
+                                "shift = (Lq - Lk) if bottom_right else 0"),
+    "window_right_ignored": ("hi = None if window_right is None else shift + window_right", "hi = None"),
+    "window_left_ignores_shift": ("lo = None if window_left is None else shift - window_left",
+                                  "lo = None if window_left is None else -window_left"),
+    "blockdiag_bottom_right_global_lengths": (
+        "_band(mask_kind, bottom_right, window_left, window_right, qe - qs, ke - ks)",
+        "_band(mask_kind, bottom_right, window_left, window_right, M, Mkv)"),
     "scale_dropped": ("x = scale64 * (qb @ kb.T)", "x = (qb @ kb.T)"),
     "scores_use_values": ("x = scale64 * (qb @ kb.T)", "x = scale64 * (qb @ vb.T)"),
     "lse_wrong_sign": ("lse = m + np.log(l)", "lse = m - np.log(l)"),
@@ -30,8 +39,8 @@ MUTANTS = {
     "shared_head_always_zero": ("hk = h if k.shape[2] == H else 0", "hk = 0"),
     "blockdiag_sees_all_keys": ("_block(qb_all[qs:qe], kb_all[ks:ke], vb_all[ks:ke], s64,",
                                 "_block(qb_all[qs:qe], kb_all, vb_all, s64,"),
-    "blockdiag_absolute_positions": ("mask_kind == MASK_BLOCKDIAG_CAUSAL, 0, kv_offset)",
-                                     "mask_kind == MASK_BLOCKDIAG_CAUSAL, qs, ks + kv_offset)"),
+    "blockdiag_absolute_positions": ("s64, lo, hi, 0,\n                              kv_offset)",
+                                     "s64, lo, hi, qs,\n                              ks + kv_offset)"),
     "merge_averages": ("coef = w / sum_w[None]", "coef = np.ones_like(w) / w.shape[0]"),
     "merge_lse_drops_shift": ("lse = m_star + np.log(sum_w)", "lse = np.log(sum_w)"),
     "merge_unnormalised": ("coef = w / sum_w[None]", "coef = w"),
