@@ -27,6 +27,8 @@ MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_BLOCKDIAG = 2
 MASK_BLOCKDIAG_CAUSAL = 3
+MASK_CAUSAL_BOTTOM_RIGHT = 4
+MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT = 5
 DTYPE_BF16 = 0
 DTYPE_FP32 = 1
 
@@ -43,6 +45,11 @@ class Seqlens(ctypes.Structure):
         ("max_seqlen_q", ctypes.c_int32),
         ("max_seqlen_k", ctypes.c_int32),
     ]
+
+
+class Band(ctypes.Structure):
+    _fields_ = [("bottom_right", ctypes.c_int32), ("window_left", ctypes.c_int32),
+                ("window_right", ctypes.c_int32)]
 
 
 class MslkError(RuntimeError):
@@ -66,6 +73,12 @@ SIGNATURES = {
     "mslk_attn_partial": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32, _i32,
                                  ctypes.c_float, _i32, ctypes.POINTER(Seqlens), _i64, _P, _i32,
                                  _P, _P]),
+    "mslk_attn_fwd_band": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32, _i32,
+                                  ctypes.c_float, _i32, ctypes.POINTER(Seqlens), ctypes.POINTER(Band),
+                                  _P, _P, _P]),
+    "mslk_attn_partial_band": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32,
+                                      _i32, ctypes.c_float, _i32, ctypes.POINTER(Seqlens),
+                                      ctypes.POINTER(Band), _i64, _P, _i32, _P, _P]),
     "mslk_merge_attentions": (_i32, [_P, _P, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _S, _S,
                                      _P, _i32, _P, _P]),
     "mslk_last_error": (ctypes.c_char_p, []),

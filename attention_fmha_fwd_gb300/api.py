@@ -21,7 +21,10 @@ MASKS = {
     "causal": _capi.MASK_CAUSAL,
     "blockdiag": _capi.MASK_BLOCKDIAG,
     "blockdiag_causal": _capi.MASK_BLOCKDIAG_CAUSAL,
+    "causal_bottom_right": _capi.MASK_CAUSAL_BOTTOM_RIGHT,
+    "blockdiag_causal_bottom_right": _capi.MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT,
 }
+_BLOCKDIAG = (_capi.MASK_BLOCKDIAG, _capi.MASK_BLOCKDIAG_CAUSAL, _capi.MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT)
 _DTYPES = {torch.bfloat16: _capi.DTYPE_BF16, torch.float32: _capi.DTYPE_FP32}
 
 
@@ -80,8 +83,16 @@ def _check_inputs(q, k, v):
             raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
 
 
+def _band(bottom_right, window_left, window_right):
+    """mslk_band for the *_band entry points, or None when the plain call suffices."""
+    if not bottom_right and window_left is None and window_right is None:
+        return None
+    return _capi.Band(1 if bottom_right else 0, -1 if window_left is None else int(window_left),
+                      -1 if window_right is None else int(window_right))
+
+
 def _seqlens(mask_kind, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k):
-    if mask_kind not in (_capi.MASK_BLOCKDIAG, _capi.MASK_BLOCKDIAG_CAUSAL):
+    if mask_kind not in _BLOCKDIAG:
         return None, ()
     if cu_seqlens_q is None or cu_seqlens_k is None:
         raise ValueError("block-diagonal masks need cu_seqlens_q and cu_seqlens_k")
@@ -100,11 +111,16 @@ def _seqlens(mask_kind, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k):
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", scale=None,
              cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
-             out=None, lse=True, stream=None):
+             out=None, lse=True, stream=None, bottom_right=False, window_left=None,
+             window_right=None):
     """Fused attention forward; returns (out, lse) with lse None when ``lse=False``.
 
     q [B,M,H,K], k [B,Mkv,H,K], v [B,Mkv,H,Kv] bf16 CUDA tensors (BMK inputs are viewed
     as one head).  ``lse`` may be True (allocate), False (skip) or an fp32 [B,H,M] tensor.
+    ``bottom_right`` / ``window_left`` / ``window_right`` (keys before / after the paired
+    key; None = unbounded) select a bottom-right alignment and a local window (the pages'
+    ``...FromBottomRight...`` and ``...LocalAttention...`` masks; a causal window of
+    ``window_size`` w keys is ``window_left=w - 1``).
     """
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
     _check_inputs(q, k, v)
@@ -121,20 +137,29 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", 
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")
     lib = _capi.load()
-    check(lib.mslk_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
-                            ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H, K,
-                            Kv, 0.0 if scale is None else float(scale), mk, sl, out.data_ptr(),
-                            _ptr(lse), _stream_handle(stream, q.device)))
+    band = _band(bottom_right, window_left, window_right)
+    sc = 0.0 if scale is None else float(scale)
+    if band is None:
+        check(lib.mslk_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
+                                ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H,
+                                K, Kv, sc, mk, sl, out.data_ptr(), _ptr(lse),
+                                _stream_handle(stream, q.device)))
+    else:
+        check(lib.mslk_attn_fwd_band(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
+                                     ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M,
+                                     Mkv, H, K, Kv, sc, mk, sl, ctypes.byref(band), out.data_ptr(),
+                                     _ptr(lse), _stream_handle(stream, q.device)))
     return out, lse
 
 
 def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none",
                  scale=None, kv_offset: int = 0, cu_seqlens_q=None, cu_seqlens_k=None,
                  max_seqlen_q=None, max_seqlen_k=None, out_dtype=torch.float32, out=None,
-                 lse=None, stream=None):
+                 lse=None, stream=None, window_left=None, window_right=None):
     """Attention over one disjoint K/V chunk; returns (out, lse) for merge_attentions.
 
-    ``kv_offset`` is the position of the chunk's first key (causal masks only).
+    ``kv_offset`` is the position of the chunk's first key (read by causal masks and
+    windows; a bottom-right alignment over the full keys is folded into it).
     """
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
     _check_inputs(q, k, v)
@@ -153,11 +178,21 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")
     lib = _capi.load()
-    check(lib.mslk_attn_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
-                                ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H,
-                                K, Kv, 0.0 if scale is None else float(scale), mk, sl,
-                                int(kv_offset), out.data_ptr(), _DTYPES[out_dtype], lse.data_ptr(),
-                                _stream_handle(stream, q.device)))
+    band = _band(False, window_left, window_right)
+    sc = 0.0 if scale is None else float(scale)
+    if band is None:
+        check(lib.mslk_attn_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
+                                    ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M,
+                                    Mkv, H, K, Kv, sc, mk, sl, int(kv_offset), out.data_ptr(),
+                                    _DTYPES[out_dtype], lse.data_ptr(),
+                                    _stream_handle(stream, q.device)))
+    else:
+        check(lib.mslk_attn_partial_band(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                         ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv),
+                                         ctypes.byref(so), B, M, Mkv, H, K, Kv, sc, mk, sl,
+                                         ctypes.byref(band), int(kv_offset), out.data_ptr(),
+                                         _DTYPES[out_dtype], lse.data_ptr(),
+                                         _stream_handle(stream, q.device)))
     return out, lse
 
 

@@ -57,9 +57,11 @@ struct DecArgs {
   const __nv_bfloat16* q;
   long long sq_b, sq_m, sq_h;
   int M, Mkv, H;
-  int hk_shared, causal;
+  int hk_shared;
   int cs;  // CTAs per (batch, head): the cluster size
-  long long kv_offset;
+  // Key j is allowed for query row m iff m + lo <= j <= m + hi (kv_offset folded in;
+  // +-kBandOpen: open).
+  long long lo, hi;
   float scale_log2;
   void* out;
   int out_fp32;
@@ -194,7 +196,7 @@ MSLK_DEV void fold_tile(const DecArgs& a, const float (&qf)[MQ][D / 32], const u
         part[j] = d;
       }
       float sc = butterfly_reduce32(part, lane);
-      const bool allowed = my_key < kb1 && (!a.causal || a.kv_offset + my_key <= m);
+      const bool allowed = my_key < kb1 && my_key <= m + a.hi && my_key >= m + a.lo;
       sc = allowed ? sc : -INFINITY;
       const float m_new = fmaxf(st.m_run[m], warp_max(sc));
       const float msub = (m_new == -INFINITY) ? 0.f : m_new;
@@ -242,19 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
   const int hk = a.hk_shared ? 0 : h;
 
-  // Keys of this (batch, head): the causal limit of the last row, split over the
-  // cluster's CTAs in whole tiles.
-  int n_keys = a.Mkv;
-  if (a.causal) {  // key j allowed iff kv_offset + j <= row; the last row sees the most
-    const long long kmax = static_cast<long long>(a.M - 1) - a.kv_offset;
-    n_keys = kmax < 0 ? 0 : static_cast<int>(min(static_cast<long long>(n_keys), kmax + 1));
-  }
-  const int tiles_all = (n_keys + T - 1) / T;
+  // Keys of this (batch, head) that some row may see: from row 0's lower band edge to
+  // row M-1's upper edge, split over the cluster's CTAs in whole tiles.
+  const long long k_first = max(0LL, a.lo);
+  const long long k_last = min(static_cast<long long>(a.Mkv) - 1, static_cast<long long>(a.M - 1) + a.hi);
+  const int tile_first = k_first <= k_last ? static_cast<int>(k_first / T) : 0;
+  const int tiles_all = k_first <= k_last ? static_cast<int>(k_last / T) + 1 - tile_first : 0;
   const int per_cta = (tiles_all + a.cs - 1) / a.cs;
   const int t0 = min(tiles_all, rank * per_cta);
   const int n_tiles = max(0, min(tiles_all, t0 + per_cta) - t0);
-  const int key_base = t0 * T;
-  const int kb1 = min(n_keys, (t0 + n_tiles) * T);
+  const int key_base = (tile_first + t0) * T;
+  const int kb1 = static_cast<int>(min(k_last + 1, static_cast<long long>(tile_first + t0 + n_tiles) * T));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -482,7 +482,10 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, i
   // with every CTA keeping at least two tiles per consumer warp (ties: the smaller c).
   {
     const long long units = static_cast<long long>(B) * H;
-    const long long tiles = (static_cast<long long>(a.Mkv) + L::kT - 1) / L::kT;
+    // key tiles some row may see (the band's reach, as in the kernel)
+    const long long k_first = std::max(0LL, a.lo);
+    const long long k_last = std::min(static_cast<long long>(a.Mkv) - 1, static_cast<long long>(a.M - 1) + a.hi);
+    const long long tiles = k_first <= k_last ? k_last / L::kT + 1 - k_first / L::kT : 0;
     int best = 1;
     double best_cost = 1e300;
     for (int si = 0; si < kSizes; ++si) {
@@ -549,8 +552,8 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   a.Mkv = p.Mkv;
   a.H = p.H;
   a.hk_shared = p.kv_head_shared ? 1 : 0;
-  a.causal = is_causal(p.mask_kind) ? 1 : 0;
-  a.kv_offset = p.kv_offset;
+  a.lo = p.band_lo <= -kBandOpen ? -kBandOpen : p.band_lo - p.kv_offset;
+  a.hi = p.band_hi >= kBandOpen ? kBandOpen : p.band_hi - p.kv_offset;
   a.scale_log2 = p.scale * kLog2e;
   a.out = p.out;
   a.out_fp32 = p.out_fp32 ? 1 : 0;

@@ -13,25 +13,27 @@
 // Per CTA (320 threads):
 //   warps 0-3   softmax for Q tile 0 (thread t owns row t = TMEM lane t)
 //   warps 4-7   softmax for Q tile 1
-//   warp  8     tcgen05.mma issue (one thread) + TMEM allocation
-//   warp  9     TMA producer (one thread)
+//   warp  8     tcgen05.mma issue (one elected thread) + TMEM allocation
+//   warp  9     TMA producer (one elected thread)
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D),
 // fp32 accumulators, row r of a tile in lane r.  The bf16 probabilities P_t overwrite the
 // first 64 columns of S_t (two values per column) and feed the PV MMA from tensor memory.
 // Shared memory: Q0, Q1 and a ring of K/V tiles (4 stages at D=128), in the 128-byte-swizzled
 // K-major layout TMA writes (V is read MN-major by the PV MMA).  Each Q tile has its own
 // full/empty barriers: the next unit's Q0 loads as soon as this unit's last S0 MMA has
-// run (a tile earlier than Q1 under a causal mask), and the next unit's S0_0 is issued
-// right behind this unit's last PV1.
+// run (a tile earlier than Q1 under a causal mask), and the next unit's first S0 is
+// issued right behind this unit's last PV.
 // The MMA and TMA roles run as whole converged warps that issue through one elected lane:
 // their operands stay warp-uniform, so they need few issue slots while the softmax
 // warpgroups keep the SM's schedulers busy.
 //
 // MMA order (ping-pong: the tensor core works on one tile while the other tile's
-// softmax runs):  S0_0 S1_0 | PV0_j S0_{j+1} PV1_j S1_{j+1} | ...
-// S_t(j+1) is committed after PV_t(j), so when a softmax warpgroup sees S_t(j+1) its
-// O_t is stable (it may rescale it) and PV_t(j) has finished reading P_t; MMAs issued by
-// one thread execute in order, so S_t(j+1) overwrites P_t(j) only after PV_t(j) read it.
+// softmax runs):  S0_lo S1_lo | PV0_j S0_{j+1} PV1_j S1_{j+1} | ...  (each tile only over
+// its own key tiles).  S_t(j+1) is committed after PV_t(j), so when a softmax warpgroup
+// sees S_t(j+1) its O_t is stable (it may rescale it) and PV_t(j) has finished reading
+// P_t; MMAs issued by one thread execute in order, so S_t(j+1) overwrites P_t(j) only
+// after PV_t(j) read it.  Measured: issuing each tile's MMAs from its own warp instead
+// was slower (the two streams interleave worse on the tensor core).
 //
 // Online softmax in base 2: m2 = running max of scale*log2(e)*s; p = 2^(scale*log2e*s - m2);
 // l = running sum of p.  The running max used for p is only raised when the row max
@@ -94,10 +96,14 @@ struct TcArgs {
   int Z;            // batches, or packed sequences
   int total_units;  // units_m * H * Z
   int hk_shared;
-  int causal, varlen;
+  int varlen;
   int units_m;
   float scale_log2;
-  long long kv_offset;
+  // Key j of a sequence/chunk is allowed for its query row r iff r + lo <= j <= r + hi
+  // (kv_offset already folded in; +-kBandOpen: open), plus Lk - Lq per packed sequence
+  // when band_seq is set.
+  long long lo, hi;
+  int band_seq;
   const int* cu_q;
   const int* cu_k;
   void* out;
@@ -180,8 +186,14 @@ struct Unit {
   int b, h, hk;
   int q_base, Lq, k_base, Lk;
   int r0;
-  int n_tiles;  // key tiles of the unit (= of Q tile 1)
-  int n0;       // key tiles Q tile 0 needs (fewer under a causal mask); n0 <= n_tiles
+  int lo, hi;  // the band of this unit's sequence (see TcArgs), clamped to +-2^30
+  // Key tiles [tlo[t], thi[t]) hold every key some row of Q tile t may see (empty:
+  // tlo == thi); the unit streams [jlo, jhi), their union, which has no gaps because
+  // the band's lower edge never passes its upper edge.
+  int tlo[2], thi[2];
+  int jlo, jhi;
+  MSLK_DEV bool has(int t) const { return tlo[t] < thi[t]; }
+  MSLK_DEV bool act(int t, int j) const { return tlo[t] <= j && j < thi[t]; }
 };
 
 // Unit i of the heavy-first order: unit rows descend level by level (causal units late in
@@ -214,16 +226,36 @@ MSLK_DEV bool decode_unit(const TcArgs& a, int i, Unit& u) {
   }
   u.r0 = unit_m * kUnitRows;
   if (u.r0 >= u.Lq) return false;
-  u.n_tiles = (u.Lk + kBlockN - 1) / kBlockN;
-  u.n0 = u.n_tiles;
-  if (a.causal) {
-    const long long all = u.n_tiles;
-    const long long last_row = min(u.r0 + kUnitRows - 1, u.Lq - 1);
-    const long long kmax = last_row - a.kv_offset;  // last allowed key of the unit
-    u.n_tiles = kmax < 0 ? 0 : static_cast<int>(min(all, kmax / kBlockN + 1));
-    const long long last0 = min(u.r0 + kBlockM - 1, u.Lq - 1);
-    const long long kmax0 = last0 - a.kv_offset;  // last allowed key of Q tile 0
-    u.n0 = kmax0 < 0 ? 0 : static_cast<int>(min(all, kmax0 / kBlockN + 1));
+  {
+    long long lo = a.lo, hi = a.hi;
+    if (a.band_seq) {
+      const long long shift = static_cast<long long>(u.Lk) - u.Lq;
+      if (lo > -kBandOpen) lo += shift;
+      if (hi < kBandOpen) hi += shift;
+    }
+    // Row and key positions are below 2^31, so bounds beyond +-2^30 of any difference
+    // that matters act as open; clamping keeps the per-row arithmetic in 32 bits.
+    constexpr long long kClamp = 1LL << 30;
+    u.lo = static_cast<int>(max(-kClamp, min(kClamp, lo)));
+    u.hi = static_cast<int>(max(-kClamp, min(kClamp, hi)));
+  }
+  for (int t = 0; t < kQTiles; ++t) {
+    const long long row0 = u.r0 + t * kBlockM;
+    u.tlo[t] = u.thi[t] = 0;
+    if (row0 >= u.Lq) continue;  // rows past the sequence: nothing to compute
+    const long long row1 = min(row0 + kBlockM, static_cast<long long>(u.Lq)) - 1;
+    const long long k_first = max(0LL, row0 + u.lo);
+    const long long k_last = min(static_cast<long long>(u.Lk) - 1, row1 + u.hi);
+    if (k_first > k_last) continue;
+    u.tlo[t] = static_cast<int>(k_first / kBlockN);
+    u.thi[t] = static_cast<int>(k_last / kBlockN) + 1;
+  }
+  if (u.has(0) && u.has(1)) {
+    u.jlo = min(u.tlo[0], u.tlo[1]);
+    u.jhi = max(u.thi[0], u.thi[1]);
+  } else {
+    u.jlo = u.has(0) ? u.tlo[0] : u.tlo[1];
+    u.jhi = u.has(0) ? u.thi[0] : u.thi[1];
   }
   return true;
 }
@@ -234,7 +266,9 @@ MSLK_DEV int unit_at(int round, int c, int G) {
   return round * G + ((round & 1) ? (G - 1 - c) : c);
 }
 
-template <int D>
+// kLowerEdge: the band has a lower edge (a local window), so masked tiles test both
+// edges; without it the per-row lower limit is compiled out of the softmax.
+template <int D, bool kLowerEdge>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -306,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer (whole warp)
-    // Order per unit: Q0, K_0, Q1, V_0, K_1, V_1, ...  Each Q tile waits only for its own
+    // Order per unit: Q0, K_lo, Q1, V_lo, K_lo+1, V_lo+1, ...  Each Q tile waits only for its own
     // tile's last S MMA of the previous unit, so the next unit's Q0 (and K_0) arrive in
     // time for the MMA warp to start S0_0 before the current unit's last tile-1 step.
     int uc = 0, it = 0;
@@ -333,12 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < n_rounds && ok; ++k) {
       const int i = unit_at(k, cta, G);
       Unit u;
-      if (i >= a.total_units || !decode_unit(a, i, u) || u.n_tiles == 0) continue;
+      if (i >= a.total_units || !decode_unit(a, i, u) || u.jhi <= u.jlo) continue;
       load_q(0, u);
-      if (ok) load_kv(0, 0, u);
+      if (ok) load_kv(u.jlo, 0, u);
       if (ok) load_q(1, u);
-      if (ok) load_kv(0, 1, u);
-      for (int j = 1; j < u.n_tiles && ok; ++j) {
+      if (ok) load_kv(u.jlo, 1, u);
+      for (int j = u.jlo + 1; j < u.jhi && ok; ++j) {
         load_kv(j, 0, u);
         if (ok) load_kv(j, 1, u);
       }
@@ -360,14 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t vdesc0 = desc_mnmajor(kv_addr(0));
     auto kv_kdesc = [&](int st) { return kdesc0 + static_cast<uint32_t>(st * (L::kTileBytes >> 4)); };
     auto kv_vdesc = [&](int st) { return vdesc0 + static_cast<uint32_t>(st * (L::kTileBytes >> 4)); };
-    // uc: units; uc_t / jg_t: units and key tiles of Q tile t (its barrier phases).
+    // uc: units; uc_t: units in which Q tile t has keys (o_free phases); jg_t: its key tiles.
     int uc = 0, it = 0, uc0 = 0, uc1 = 0, jg0 = 0, jg1 = 0;
     bool ok = true;
     // The next unit with work at or after round k (k_out = its round), false if none.
     auto next_unit = [&](int k, int& k_out, Unit& uo) {
       for (; k < n_rounds; ++k) {
         const int i = unit_at(k, cta, G);
-        if (i < a.total_units && decode_unit(a, i, uo) && uo.n_tiles > 0) {
+        if (i < a.total_units && decode_unit(a, i, uo) && uo.jhi > uo.jlo) {
           k_out = k;
           return true;
         }
@@ -377,94 +411,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit u;
     int ku = 0;
     bool have = next_unit(0, ku, u);
-    bool s0_issued = false;  // S0_0 of unit u was issued at the end of the previous unit
+    bool s0_issued = false;  // the unit's first S0 was issued at the end of the previous unit
     while (have && ok) {
       Unit un;
       int kn = 0;
       const bool have_next = next_unit(ku + 1, kn, un);
-      const int n = u.n_tiles;
-      const int n0 = u.n0;
-      const int ik0 = it++;  // K_0's ring position
+      const int jlo = u.jlo;
+      const int jhi = u.jhi;
+      const int lo0 = u.tlo[0], hi0 = u.thi[0], lo1 = u.tlo[1], hi1 = u.thi[1];
+      const int ik0 = it++;  // K_jlo's ring position
       const int sk0 = ik0 % L::kStages;
-      // S_t(0): S_t is free (its last P was consumed by the previous unit's PV_t, which
-      // was issued before this and executes first).
+      // S_t(jlo): S_t is free (its last P was consumed by the previous unit's PV_t, which
+      // was issued before this and executes first).  Q tile 0 starts at jlo whenever it
+      // has keys (its rows come first, so its key range starts first).
       if (!s0_issued) {
         if (!(ok = wait_bar_warp(q_full(0), uc & 1, wc))) break;
         if (!(ok = wait_bar_warp(kv_full(sk0), (ik0 / L::kStages) & 1, wc))) break;
         tc_fence_after();
-        if (n0 > 0) {
+        if ((lo0 <= jlo && jlo < hi0)) {
           issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk0));
           mma_commit_elect(s_full(0));
         }
-        if (n0 <= 1) mma_commit_elect(q_empty(0));  // Q0's last S MMA was issued
+        if (lo0 >= hi0 || hi0 == jlo + 1) mma_commit_elect(q_empty(0));  // Q0's last S issued
       }
       s0_issued = false;
       if (!(ok = wait_bar_warp(q_full(1), uc & 1, wc))) break;
       if (!(ok = wait_bar_warp(kv_full(sk0), (ik0 / L::kStages) & 1, wc))) break;
       tc_fence_after();
-      issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk0));
-      mma_commit_elect(s_full(1));
+      if ((lo1 <= jlo && jlo < hi1)) {
+        issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk0));
+        mma_commit_elect(s_full(1));
+      }
       mma_commit_elect(kv_empty(sk0));
-      if (n == 1) mma_commit_elect(q_empty(1));
-      for (int j = 0; j < n && ok; ++j) {
-        const bool more = j + 1 < n;
+      if (lo1 >= hi1 || hi1 == jlo + 1) mma_commit_elect(q_empty(1));
+      for (int j = jlo; j < jhi && ok; ++j) {
+        const bool more = j + 1 < jhi;
         const int iv = it;       // V_j's ring position
         const int ik = it + 1;   // K_{j+1}'s
         it += more ? 2 : 1;
         const int sv = iv % L::kStages;
         const int sk = ik % L::kStages;
         if (!(ok = wait_bar_warp(kv_full(sv), (iv / L::kStages) & 1, wc))) break;
-        // Q tile 0 (only while its rows still see keys): PV0_j, then S0_{j+1}
-        if (j < n0) {
+        // Q tile 0 (while key tile j is in its range): PV0_j, then S0_{j+1}
+        if ((lo0 <= j && j < hi0)) {
           if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
-          if (j == 0 && !(ok = wait_bar_warp(o_free(0), (uc0 & 1) ^ 1, wc))) break;
+          if (j == lo0 && !(ok = wait_bar_warp(o_free(0), (uc0 & 1) ^ 1, wc))) break;
           tc_fence_after();
-          issue_pv<D>(tm_o[0], tm_s[0], kv_vdesc(sv), j > 0 ? 1u : 0u);
-          if (j == n0 - 1) mma_commit_elect(o_done(0));
+          issue_pv<D>(tm_o[0], tm_s[0], kv_vdesc(sv), j > lo0 ? 1u : 0u);
+          if (j == hi0 - 1) mma_commit_elect(o_done(0));
           ++jg0;
         }
         if (more) {
           if (!(ok = wait_bar_warp(kv_full(sk), (ik / L::kStages) & 1, wc))) break;
           tc_fence_after();
-          if (j + 1 < n0) {
+          if ((lo0 <= j + 1 && j + 1 < hi0)) {
             issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk));
             mma_commit_elect(s_full(0));
-            if (j + 2 == n0) mma_commit_elect(q_empty(0));
+            if (j + 2 == hi0) mma_commit_elect(q_empty(0));
           }
         }
         // Q tile 1: PV1_j, then S1_{j+1}
-        if (!(ok = wait_bar_warp(p_full(1), jg1 & 1, wc))) break;
-        if (j == 0 && !(ok = wait_bar_warp(o_free(1), (uc1 & 1) ^ 1, wc))) break;
-        tc_fence_after();
-        issue_pv<D>(tm_o[1], tm_s[1], kv_vdesc(sv), j > 0 ? 1u : 0u);
+        if ((lo1 <= j && j < hi1)) {
+          if (!(ok = wait_bar_warp(p_full(1), jg1 & 1, wc))) break;
+          if (j == lo1 && !(ok = wait_bar_warp(o_free(1), (uc1 & 1) ^ 1, wc))) break;
+          tc_fence_after();
+          issue_pv<D>(tm_o[1], tm_s[1], kv_vdesc(sv), j > lo1 ? 1u : 0u);
+          if (j == hi1 - 1) mma_commit_elect(o_done(1));
+          ++jg1;
+        }
         mma_commit_elect(kv_empty(sv));
         if (more) {
-          issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk));
-          mma_commit_elect(s_full(1));
-          mma_commit_elect(kv_empty(sk));
-          if (j + 2 == n) mma_commit_elect(q_empty(1));  // the unit's last S1 MMA was issued
-        } else {
-          mma_commit_elect(o_done(1));
-          if (have_next && un.n0 > 0) {
-            // The next unit's S0_0 right behind this unit's last PV1 (its Q0 was loaded
-            // after this unit's last S0 MMA), before this warp decodes units and waits
-            // for Q1.  S0 is free: this unit's last PV0 precedes it in issue order.
-            const int ikn = it;  // the next unit's K_0 follows V_{n-1} in the ring
-            if (!(ok = wait_bar_warp(q_full(0), (uc + 1) & 1, wc))) break;
-            if (!(ok = wait_bar_warp(kv_full(ikn % L::kStages), (ikn / L::kStages) & 1, wc))) break;
-            tc_fence_after();
-            issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(ikn % L::kStages));
-            mma_commit_elect(s_full(0));
-            if (un.n0 <= 1) mma_commit_elect(q_empty(0));
-            s0_issued = true;
+          if ((lo1 <= j + 1 && j + 1 < hi1)) {
+            issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk));
+            mma_commit_elect(s_full(1));
+            if (j + 2 == hi1) mma_commit_elect(q_empty(1));  // the unit's last S1 MMA was issued
           }
+          mma_commit_elect(kv_empty(sk));
+        } else if (have_next && un.has(0)) {
+          // The next unit's first S0 right behind this unit's last PV (its Q0 was loaded
+          // after this unit's last S0 MMA), before this warp decodes units and waits for
+          // Q1.  S0 is free: this unit's last PV0 precedes it in issue order.
+          const int ikn = it;  // the next unit's first K follows V_{jhi-1} in the ring
+          if (!(ok = wait_bar_warp(q_full(0), (uc + 1) & 1, wc))) break;
+          if (!(ok = wait_bar_warp(kv_full(ikn % L::kStages), (ikn / L::kStages) & 1, wc))) break;
+          tc_fence_after();
+          issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(ikn % L::kStages));
+          mma_commit_elect(s_full(0));
+          if (un.thi[0] == un.jlo + 1) mma_commit_elect(q_empty(0));
+          s0_issued = true;
         }
-        ++jg1;
       }
       if (!ok) break;
       ++uc;
-      ++uc1;
-      if (n0 > 0) ++uc0;
+      if (lo0 < hi0) ++uc0;
+      if (lo1 < hi1) ++uc1;
       u = un;
       ku = kn;
       have = have_next;
@@ -491,8 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = row_first + row_in_tile;
       const bool valid = r < u.Lq;
       const long long row = static_cast<long long>(u.q_base) + r;
-      const int n_t = (t == 0) ? u.n0 : u.n_tiles;  // key tiles this Q tile sees
-      if (n_t == 0) {  // no allowed key for any row of this Q tile
+      // this Q tile's key tiles (selects, not a runtime index, keep u in registers)
+      const int tlo_t = t == 0 ? u.tlo[0] : u.tlo[1];
+      const int n_t = (t == 0 ? u.thi[0] : u.thi[1]) - tlo_t;
+      if (n_t <= 0) {  // no allowed key for any row of this Q tile
         if (valid) {
           for (int c = 0; c < D; c += 4) {
             if (a.out_fp32) {
@@ -516,16 +558,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         __syncwarp();
         tc_fence_after();
-        const int key0 = j * kBlockN;
-        const bool need_mask =
-            (key0 + kBlockN > u.Lk) || (a.causal && (a.kv_offset + key0 + kBlockN - 1 > row_first));
-        // Column c of this tile is allowed iff c <= lim_c (key < Lk, and for causal masks
-        // kv_offset + key <= r); lim_c = 127 when the whole tile is allowed.
-        int lim_c = kBlockN - 1;
+        const int key0 = (tlo_t + j) * kBlockN;
+        // The tile is allowed whole for every row iff its last key is below Lk and within
+        // the first row's upper band edge and its first key is within the last row's lower
+        // edge; otherwise column c is allowed iff lim_lo <= c <= lim_c (this row's band
+        // edges, and key < Lk).
+        const bool need_mask = (key0 + kBlockN > u.Lk) ||
+                               (key0 + kBlockN - 1 > row_first + u.hi) ||
+                               (kLowerEdge && key0 < row_first + kBlockM - 1 + u.lo);
+        int lim_c = kBlockN - 1, lim_lo = 0;
         if (need_mask) {
-          long long lim = static_cast<long long>(u.Lk) - 1 - key0;
-          if (a.causal) lim = min(lim, static_cast<long long>(r) - a.kv_offset - key0);
-          lim_c = static_cast<int>(max(-1LL, min(lim, static_cast<long long>(kBlockN - 1))));
+          lim_c = max(-1, min(min(u.Lk - 1, r + u.hi) - key0, kBlockN - 1));
+          if constexpr (kLowerEdge) lim_lo = max(0, min(max(0, r + u.lo) - key0, kBlockN));
         }
         // The whole S row comes out of tensor memory in one load (128 registers): mask it
         // (only tiles crossing a mask limit), take the row max, then form
@@ -534,9 +578,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[128];
         tmem_ld_32x32b_x128(ts, sr);
         if (need_mask) {
+          if (kLowerEdge && __any_sync(0xffffffffu, lim_lo > 0)) {  // a lower window edge here
 #pragma unroll
-          for (int c = 0; c < kBlockN; ++c)
-            if (c > lim_c) sr[c] = 0xFF800000u;  // -inf: excluded from the max, 2^-inf = 0
+            for (int c = 0; c < kBlockN; ++c)
+              if (c > lim_c || c < lim_lo) sr[c] = 0xFF800000u;  // -inf: excluded from the max
+          } else {
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c)
+              if (c > lim_c) sr[c] = 0xFF800000u;  // -inf: excluded from the max, 2^-inf = 0
+          }
         }
         float mx8[8];
 #pragma unroll
@@ -810,12 +860,13 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.Mkv = p.Mkv;
   a.H = p.H;
   a.hk_shared = p.kv_head_shared ? 1 : 0;
-  a.causal = is_causal(p.mask_kind) ? 1 : 0;
+  a.lo = p.band_lo <= -kBandOpen ? -kBandOpen : p.band_lo - p.kv_offset;
+  a.hi = p.band_hi >= kBandOpen ? kBandOpen : p.band_hi - p.kv_offset;
+  a.band_seq = p.band_seq_shift ? 1 : 0;
   a.varlen = is_blockdiag(p.mask_kind) ? 1 : 0;
   const int rows = a.varlen ? p.max_seqlen_q : p.M;
   a.units_m = (rows + kUnitRows - 1) / kUnitRows;
   a.scale_log2 = p.scale * kLog2e;
-  a.kv_offset = p.kv_offset;
   a.cu_q = p.cu_q;
   a.cu_k = p.cu_k;
   a.out = p.out;
@@ -837,18 +888,18 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.total_units = static_cast<int>(total);
   // Persistent: one CTA per SM (or fewer when there are fewer units).
   const dim3 grid(static_cast<unsigned>(std::min<long long>(total, num_sms())));
-  cudaError_t e = cudaFuncSetAttribute(fmha_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Lt::kAlloc);
+  auto kernel = a.lo > -kBandOpen ? fmha_tc_kernel<D, true> : fmha_tc_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lt::kAlloc);
   if (e != cudaSuccess) {
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  fmha_tc_kernel<D><<<grid, kThreads, Lt::kAlloc, stream>>>(tq, tk, tv, to, a);
+  kernel<<<grid, kThreads, Lt::kAlloc, stream>>>(tq, tk, tv, to, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     static thread_local char msg[160];
     cudaFuncAttributes fa{};
-    cudaFuncGetAttributes(&fa, fmha_tc_kernel<D>);
+    cudaFuncGetAttributes(&fa, kernel);
     snprintf(msg, sizeof(msg),
              "fmha_tc_kernel launch failed (regs/thread %d, max threads/block %d, dyn smem %d)",
              fa.numRegs, fa.maxThreadsPerBlock, Lt::kAlloc);

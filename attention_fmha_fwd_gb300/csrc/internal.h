@@ -22,6 +22,11 @@ struct AttnProblem {
   const int32_t* cu_k;
   int n_seqs, max_seqlen_q, max_seqlen_k;
   int64_t kv_offset;    // 0 for the forward call
+  // Band of allowed keys: key position j (kv_offset added) is allowed for query row i
+  // iff band_lo <= j - i <= band_hi (kBandOpen: that side open), plus, for block-diagonal
+  // kinds with band_seq_shift, each sequence's Lk - Lq added to both bounds.
+  int64_t band_lo, band_hi;
+  bool band_seq_shift;
   void* out;
   bool out_fp32;
   float* lse;           // may be null (forward without lse)
@@ -50,11 +55,18 @@ struct DeviceCtl {
 constexpr unsigned int kErrWaitTimeout = 1u;
 
 constexpr bool is_causal(int mask_kind) {
-  return mask_kind == MSLK_MASK_CAUSAL || mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL;
+  return mask_kind == MSLK_MASK_CAUSAL || mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL ||
+         mask_kind == MSLK_MASK_CAUSAL_BOTTOM_RIGHT || mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT;
 }
 constexpr bool is_blockdiag(int mask_kind) {
-  return mask_kind == MSLK_MASK_BLOCKDIAG || mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL;
+  return mask_kind == MSLK_MASK_BLOCKDIAG || mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL ||
+         mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT;
 }
+constexpr bool is_bottom_right(int mask_kind) {
+  return mask_kind == MSLK_MASK_CAUSAL_BOTTOM_RIGHT || mask_kind == MSLK_MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT;
+}
+// An open side of the key band (far beyond any int32 position difference).
+constexpr int64_t kBandOpen = int64_t(1) << 40;
 
 // Largest query-row count the CUDA-core decode kernel takes.
 constexpr int kDecodeMaxRows = 8;

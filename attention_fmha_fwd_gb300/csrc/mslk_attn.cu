@@ -79,11 +79,24 @@ mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const vo
                           const mslk_strides* sq, const mslk_strides* sk, const mslk_strides* sv,
                           const mslk_strides* so, int32_t B, int32_t M, int32_t Mkv, int32_t H,
                           int32_t K, int32_t Kv, float scale, int32_t mask_kind,
-                          const mslk_seqlens* seqlens, int64_t kv_offset, void* out,
-                          int32_t out_dtype, float* lse, bool lse_required, const char* who) {
+                          const mslk_seqlens* seqlens, const mslk_band* band, int64_t kv_offset,
+                          void* out, int32_t out_dtype, float* lse, bool lse_required,
+                          bool partial, const char* who) {
   if (B < 0 || M < 0 || Mkv < 0 || H < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative size", who);
-  if (mask_kind < MSLK_MASK_NONE || mask_kind > MSLK_MASK_BLOCKDIAG_CAUSAL)
+  if (mask_kind < MSLK_MASK_NONE || mask_kind > MSLK_MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT)
     return fail(MSLK_ERR_INVALID_ARG, "%s: unknown mask_kind %d", who, mask_kind);
+  const int32_t wl = band ? band->window_left : -1;
+  const int32_t wr = band ? band->window_right : -1;
+  if (band && band->bottom_right != 0 && band->bottom_right != 1)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: band.bottom_right must be 0 or 1", who);
+  if (wl < -1 || wr < -1)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: window sizes must be >= 0 (or -1 for unbounded)", who);
+  if (is_causal(mask_kind) && wr > 0)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: causal masks have no right window (window_right %d)", who, wr);
+  const bool bottom_right = is_bottom_right(mask_kind) || (band && band->bottom_right);
+  if (partial && bottom_right)
+    return fail(MSLK_ERR_INVALID_ARG,
+                "%s: bottom-right alignment is forward only; fold Lk_full - M into kv_offset", who);
   if (out_dtype != MSLK_DTYPE_BF16 && out_dtype != MSLK_DTYPE_FP32)
     return fail(MSLK_ERR_INVALID_ARG, "%s: unknown out_dtype %d", who, out_dtype);
   if (sq == nullptr || sk == nullptr || sv == nullptr || so == nullptr)
@@ -109,6 +122,17 @@ mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const vo
   p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : 1.0f / std::sqrt(static_cast<float>(K));
   p.mask_kind = mask_kind;
   p.kv_offset = kv_offset;
+  // Band on (key position - query row): causal kinds close it at 0, windows at -wl / +wr;
+  // a dense bottom-right alignment shifts both bounds by Mkv - M, a block-diagonal one by
+  // each sequence's Lk - Lq (added in the kernels).
+  p.band_hi = is_causal(mask_kind) ? 0 : (wr >= 0 ? wr : kBandOpen);
+  p.band_lo = wl >= 0 ? -static_cast<int64_t>(wl) : -kBandOpen;
+  p.band_seq_shift = bottom_right && is_blockdiag(mask_kind);
+  if (bottom_right && !is_blockdiag(mask_kind)) {
+    const int64_t shift = static_cast<int64_t>(Mkv) - M;
+    if (p.band_hi != kBandOpen) p.band_hi += shift;
+    if (p.band_lo != -kBandOpen) p.band_lo += shift;
+  }
   p.out = out;
   p.out_fp32 = out_dtype == MSLK_DTYPE_FP32;
   p.lse = lse;
@@ -231,8 +255,8 @@ mslk_status mslk_attn_fwd(const void* q, const void* k, const void* v, const msl
                           float* lse, void* stream) {
   AttnProblem p;
   const mslk_status s = validate_attn(p, q, k, v, sq, sk, sv, so, B, M, Mkv, H, K, Kv, scale,
-                                      mask_kind, seqlens, 0, out, MSLK_DTYPE_BF16, lse, false,
-                                      "mslk_attn_fwd");
+                                      mask_kind, seqlens, nullptr, 0, out, MSLK_DTYPE_BF16, lse,
+                                      false, false, "mslk_attn_fwd");
   if (s != MSLK_OK) return s;
   return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_fwd");
 }
@@ -245,10 +269,38 @@ mslk_status mslk_attn_partial(const void* q, const void* k, const void* v, const
                               void* stream) {
   AttnProblem p;
   const mslk_status s = validate_attn(p, q, k, v, sq, sk, sv, so, B, M, Mkv, H, K, Kv, scale,
-                                      mask_kind, seqlens, kv_offset, out, out_dtype, lse, true,
-                                      "mslk_attn_partial");
+                                      mask_kind, seqlens, nullptr, kv_offset, out, out_dtype, lse,
+                                      true, true, "mslk_attn_partial");
   if (s != MSLK_OK) return s;
   return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_partial");
+}
+
+mslk_status mslk_attn_fwd_band(const void* q, const void* k, const void* v, const mslk_strides* sq,
+                               const mslk_strides* sk, const mslk_strides* sv, const mslk_strides* so,
+                               int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv,
+                               float scale, int32_t mask_kind, const mslk_seqlens* seqlens,
+                               const mslk_band* band, void* out, float* lse, void* stream) {
+  AttnProblem p;
+  const mslk_status s = validate_attn(p, q, k, v, sq, sk, sv, so, B, M, Mkv, H, K, Kv, scale,
+                                      mask_kind, seqlens, band, 0, out, MSLK_DTYPE_BF16, lse, false,
+                                      false, "mslk_attn_fwd_band");
+  if (s != MSLK_OK) return s;
+  return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_fwd_band");
+}
+
+mslk_status mslk_attn_partial_band(const void* q, const void* k, const void* v,
+                                   const mslk_strides* sq, const mslk_strides* sk,
+                                   const mslk_strides* sv, const mslk_strides* so, int32_t B,
+                                   int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv,
+                                   float scale, int32_t mask_kind, const mslk_seqlens* seqlens,
+                                   const mslk_band* band, int64_t kv_offset, void* out,
+                                   int32_t out_dtype, float* lse, void* stream) {
+  AttnProblem p;
+  const mslk_status s = validate_attn(p, q, k, v, sq, sk, sv, so, B, M, Mkv, H, K, Kv, scale,
+                                      mask_kind, seqlens, band, kv_offset, out, out_dtype, lse,
+                                      true, true, "mslk_attn_partial_band");
+  if (s != MSLK_OK) return s;
+  return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_partial_band");
 }
 
 mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split, int32_t n_chunks,

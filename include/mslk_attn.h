@@ -63,8 +63,33 @@ typedef enum {
   MSLK_MASK_NONE = 0,              /* every key */
   MSLK_MASK_CAUSAL = 1,            /* LowerTriangularMask: top-left, key position <= query row */
   MSLK_MASK_BLOCKDIAG = 2,         /* BlockDiagonalMask: packed sequences, B = 1 */
-  MSLK_MASK_BLOCKDIAG_CAUSAL = 3   /* BlockDiagonalCausalMask: top-left causal inside each block */
+  MSLK_MASK_BLOCKDIAG_CAUSAL = 3,  /* BlockDiagonalCausalMask: top-left causal inside each block */
+  /* LowerTriangularFromBottomRightMask: query i pairs with key i + Mkv - M, keys after it are
+   * masked (forward only; a split-KV chunk expresses this through kv_offset). */
+  MSLK_MASK_CAUSAL_BOTTOM_RIGHT = 4,
+  /* BlockDiagonalCausalFromBottomRightMask: the same inside every packed block (forward only). */
+  MSLK_MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT = 5
 } mslk_mask_kind;
+
+/*
+ * Alignment and local window of a mask (same page: LowerTriangularFromBottomRight-
+ * LocalAttentionMask, LocalAttentionFromBottomRightMask, BlockDiagonalCausalLocal-
+ * AttentionMask, BlockDiagonalCausalLocalAttentionFromBottomRightMask; the pages name
+ * them without formulas, this is the reading the library implements).  Query row i of a
+ * block of Lq rows and Lk keys (the whole tensor for dense kinds, one packed sequence for
+ * block-diagonal kinds) is PAIRED with key position p = i + (bottom_right ? Lk - Lq : 0);
+ * key position j (kv_offset + chunk index for partials) is allowed iff
+ *     j <= p                       for causal kinds (window_right must be -1 or 0),
+ *     j <= p + window_right        for other kinds when window_right >= 0,
+ *     j >= p - window_left         when window_left >= 0,
+ * on top of the kind's own rule (same block for block-diagonal kinds).  -1 leaves that side
+ * open.  A causal local window of w keys (the pages' window_size) is window_left = w - 1.
+ */
+typedef struct {
+  int32_t bottom_right;  /* 0 or 1; kinds 4 and 5 imply 1.  Forward only. */
+  int32_t window_left;   /* >= 0, or -1: unbounded */
+  int32_t window_right;  /* >= 0, or -1: unbounded */
+} mslk_band;
 
 typedef enum { MSLK_DTYPE_BF16 = 0, MSLK_DTYPE_FP32 = 1 } mslk_dtype;
 
@@ -116,8 +141,9 @@ mslk_status mslk_attn_fwd(const void* q, const void* k, const void* v,
  *
  * Arguments as mslk_attn_fwd, with k/v (and Mkv) describing the chunk only, plus:
  *   kv_offset  position of the chunk's first key in the full key sequence (inside each
- *              packed sequence for the block-diagonal kinds).  Only causal kinds read
- *              it: key j of the chunk is allowed for row i iff kv_offset + j <= i.
+ *              packed sequence for the block-diagonal kinds).  Causal kinds and windows
+ *              read it: key j of the chunk is at position kv_offset + j (causal: allowed
+ *              for row i iff kv_offset + j <= i).  Bottom-right kinds are forward only.
  *   out_dtype  MSLK_DTYPE_FP32 (recommended: keeps the merge exact to fp32) or
  *              MSLK_DTYPE_BF16.  out strides `so` are in elements of that type.
  *   lse        required, fp32 [B,H,M] contiguous.  Rows with no allowed key in this chunk
@@ -130,6 +156,30 @@ mslk_status mslk_attn_partial(const void* q, const void* k, const void* v,
                               int32_t Kv, float scale, int32_t mask_kind,
                               const mslk_seqlens* seqlens, int64_t kv_offset, void* out,
                               int32_t out_dtype, float* lse, void* stream);
+
+/*
+ * mslk_attn_fwd_band / mslk_attn_partial_band — as mslk_attn_fwd / mslk_attn_partial with a
+ * mask alignment and local window (mslk_band, read during the call; NULL = no window,
+ * top-left unless the kind says otherwise).  Windows work with every mask kind; for the
+ * partial call bottom_right must be 0 (fold Lk_full - Lq into kv_offset instead).
+ * Key tiles outside every row's window are skipped, so a window of W keys costs
+ * O(M * W) instead of O(M * Mkv).
+ */
+mslk_status mslk_attn_fwd_band(const void* q, const void* k, const void* v,
+                               const mslk_strides* sq, const mslk_strides* sk,
+                               const mslk_strides* sv, const mslk_strides* so,
+                               int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K,
+                               int32_t Kv, float scale, int32_t mask_kind,
+                               const mslk_seqlens* seqlens, const mslk_band* band, void* out,
+                               float* lse, void* stream);
+mslk_status mslk_attn_partial_band(const void* q, const void* k, const void* v,
+                                   const mslk_strides* sq, const mslk_strides* sk,
+                                   const mslk_strides* sv, const mslk_strides* so,
+                                   int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K,
+                                   int32_t Kv, float scale, int32_t mask_kind,
+                                   const mslk_seqlens* seqlens, const mslk_band* band,
+                                   int64_t kv_offset, void* out, int32_t out_dtype, float* lse,
+                                   void* stream);
 
 /*
  * mslk_merge_attentions — exact log-sum-exp merge of n chunk results into preallocated

@@ -115,6 +115,46 @@ def test_partial_requires_lse(lib):
     assert st == _capi.MSLK_ERR_INVALID_ARG
 
 
+def _band_call(lib, band, mask=0, partial=False):
+    s = S(8 * 128 * 64, 8 * 128, 128)
+    r = ctypes.byref
+    if partial:
+        st = lib.mslk_attn_partial_band(FAKE, FAKE, FAKE, r(s), r(s), r(s), r(s), 2, 64, 64, 8, 128,
+                                        128, 0.0, mask, None, r(band), 0, FAKE, _capi.DTYPE_FP32,
+                                        FAKE, None)
+    else:
+        st = lib.mslk_attn_fwd_band(FAKE, FAKE, FAKE, r(s), r(s), r(s), r(s), 2, 64, 64, 8, 128, 128,
+                                    0.0, mask, None, r(band), FAKE, FAKE, None)
+    return st, lib.mslk_last_error().decode()
+
+
+@pytest.mark.parametrize("band,mask,partial,needle", [
+    ((0, -1, 3), 1, False, "right window"),         # causal kinds have no right window
+    ((0, -2, -1), 0, False, "window sizes"),
+    ((0, 4, -7), 0, True, "window sizes"),
+    ((2, -1, -1), 0, False, "bottom_right"),
+    ((1, 3, -1), 1, True, "forward only"),           # partials fold alignment into kv_offset
+    ((0, -1, -1), 4, True, "forward only"),          # bottom-right kinds are forward only
+])
+def test_band_rejects(lib, band, mask, partial, needle):
+    st, why = _band_call(lib, _capi.Band(*band), mask, partial)
+    assert st == _capi.MSLK_ERR_INVALID_ARG, why
+    assert needle in why
+
+
+def test_band_kinds_pass_validation(lib):
+    """Bottom-right kinds and windows get past validation (then fail at the CUDA layer
+    here, without a device)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for band, mask in (((1, 7, -1), 1), ((0, 3, 5), 0), ((1, -1, 0), 0), ((0, -1, -1), 4)):
+        st, why = _band_call(lib, _capi.Band(*band), mask)
+        assert st == _capi.MSLK_ERR_CUDA, why
+    st, why = _fwd(lib, mask=4)
+    assert st == _capi.MSLK_ERR_CUDA, why
+
+
 def _merge(lib, n=2, Kv=128, cs_out=2 * 64 * 8 * 128, out_split=FAKE, out=FAKE, dtype=0):
     s = S(64 * 8 * 128, 8 * 128, 128)
     st = lib.mslk_merge_attentions(out_split, FAKE, n, cs_out, 2 * 8 * 64, 2, 64, 8, Kv,
