@@ -397,7 +397,7 @@ def run_gpu(args):
 
     if rank == 0:
         achieved = flops / t_step / 1e12
-        traffic = traffic_for("fmha_tc_kernel<128> causal_fwd")
+        traffic = traffic_for("fmha_tc_kernel<128, false> causal_fwd")
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
@@ -410,7 +410,7 @@ def run_gpu(args):
             "roofline": {"bound": "tensor", "achieved": achieved,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
-                         "kernel": "fmha_tc_kernel<128>", "peak_source": peak_src + " bf16 burst"},
+                         "kernel": "fmha_tc_kernel<128, false>", "peak_source": peak_src + " bf16 burst"},
             "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
                     "pipeline": "pinned host q/k/v -> device (3 copy streams), attn_fwd, "
@@ -558,6 +558,34 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
     res["varlen_packed_12seq_16384"] = {"us": t_v * 1e6, "TFLOP/s": vflops / t_v / 1e12,
                                         "frac_bf16": vflops / t_v / 1e12 / peaks["bf16_tflops"],
                                         "seqlens": lens}
+    del qd, kd, vd
+    # local window and bottom-right alignment (key tiles outside every row's band skipped)
+    import numpy as np
+
+    def band_pairs(M, Mkv, shift, wl):
+        i = np.arange(M, dtype=np.int64)
+        hi = np.minimum(i + shift, Mkv - 1)
+        lo = np.zeros_like(i) if wl is None else np.maximum(i + shift - wl, 0)
+        return int(np.maximum(hi - lo + 1, 0).sum())
+
+    for name, (M, Mkv, br, wl) in (("causal_window1024_1x8192x32x128", (8192, 8192, False, 1023)),
+                                    ("causal_bottom_right_1x2048x8192x32x128", (2048, 8192, True, None))):
+        q, k, v = inputs.qkv(1, M, Mkv, 32, 128, seed=6)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        bo = torch.empty((1, M, 32, 128), dtype=torch.bfloat16, device=dev)
+        bl = torch.empty((1, 32, M), dtype=torch.float32, device=dev)
+
+        def bstep():
+            fa.attn_fwd(qd, kd, vd, mask="causal", scale=w.scale, out=bo, lse=bl, bottom_right=br,
+                        window_left=wl)
+
+        for _ in range(3):
+            bstep()
+        t_b = _time_it(bstep, 10, stream, flush)
+        bflops = band_pairs(M, Mkv, Mkv - M if br else 0, wl) * 2 * 256 * 32
+        res[name] = {"us": t_b * 1e6, "TFLOP/s": bflops / t_b / 1e12,
+                     "frac_bf16": bflops / t_b / 1e12 / peaks["bf16_tflops"]}
+        del qd, kd, vd
     return res
 
 
