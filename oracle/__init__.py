@@ -10,8 +10,10 @@ from .attention import (  # noqa: F401
     MASK_NONE,
     attention,
     attention_head,
+    attention_lanes,
     attention_partial,
     default_scale,
+    lane_rows,
     merge_attentions,
     widen_bf16_bits,
 )

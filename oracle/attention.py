@@ -44,6 +44,16 @@ formulas; the reading used here is the plainest one, on positions p_i (query) an
   * ``window_right`` = wr (non-causal kinds only) keeps p_j - p_i <= shift + wr.
 So every mask is a band  lo <= p_j - p_i <= hi  (either side possibly unbounded).
 
+Padded and paged key lanes (same page: ``BlockDiagonalPaddedKeysMask``,
+``BlockDiagonalCausalWithOffsetPaddedKeysMask``, ``PagedBlockDiagonalPaddedKeysMask`` and
+their local variants; again named without formulas, plainest reading): queries are packed
+as for the block-diagonal masks; sequence s owns a key lane holding its ``seqlen_k[s]``
+valid keys, logical key p of the lane living at K/V row ``seqstart_k[s] + p`` (padded
+lanes) or, paged, at row ``block_table[s][p // page_size] * page_size + p % page_size`` of
+a pool of pages.  Rows beyond a lane's valid keys are never read.  The masks then act on
+the logical positions as for the block-diagonal kinds (``...CausalWithOffset...`` is the
+bottom-right alignment).
+
 Partial attention (``memory_efficient_attention_partial``) is the same definition over
 one disjoint key/value chunk; ``kv_offset`` is the chunk's first key position, used only
 by the causal masks.
@@ -227,6 +237,52 @@ def attention(q, k, v, scale, mask_kind=MASK_NONE, cu_seqlens_q=None, cu_seqlens
                                   window_right)
             out[b, :, h, :] = o
             lse[b, h, :] = l
+    return out, lse
+
+
+def lane_rows(s, seqlen_k, seqstart_k=None, block_table=None, page_size=None):
+    """K/V row index of every logical key of lane s (padded start or page table)."""
+    n = int(seqlen_k[s])
+    p = np.arange(n, dtype=np.int64)
+    if block_table is not None:
+        pages = np.asarray(block_table[s], dtype=np.int64)
+        return pages[p // page_size] * page_size + p % page_size
+    return int(seqstart_k[s]) + p
+
+
+def attention_lanes(q, k, v, scale, mask_kind, cu_seqlens_q, seqlen_k, seqstart_k=None,
+                    block_table=None, page_size=None, bottom_right=False, window_left=None,
+                    window_right=None):
+    """Packed queries (B = 1) against per-sequence key lanes, padded or paged.
+
+    q [1, total_q, H, K]; k, v [1, rows, Hk, D] holding the lanes (or the page pool).
+    ``mask_kind`` is MASK_BLOCKDIAG or MASK_BLOCKDIAG_CAUSAL.  Returns out
+    [1, total_q, H, Kv] and lse [1, H, total_q].
+    """
+    if mask_kind not in _BLOCKDIAG_KINDS:
+        raise ValueError("key lanes take a block-diagonal mask kind")
+    if q.shape[0] != 1 or k.shape[0] != 1:
+        raise ValueError("key lanes use packed tensors (B = 1)")
+    _, M, H, K = q.shape
+    Kv = v.shape[3]
+    s64 = _scale64(scale)
+    cq = [int(t) for t in cu_seqlens_q]
+    out = np.zeros((1, M, H, Kv))
+    lse = np.full((1, H, M), -np.inf)
+    for s in range(len(cq) - 1):
+        qs, qe = cq[s], cq[s + 1]
+        if qe == qs:
+            continue
+        rows = lane_rows(s, seqlen_k, seqstart_k, block_table, page_size)
+        lo, hi = _band(mask_kind, bottom_right, window_left, window_right, qe - qs, len(rows))
+        for h in range(H):
+            hk = 0 if k.shape[2] == 1 else h
+            qb = np.asarray(q[0, qs:qe, h, :], dtype=np.float64)
+            kb = np.asarray(k[0, rows, hk, :], dtype=np.float64)
+            vb = np.asarray(v[0, rows, hk, :], dtype=np.float64)
+            o_s, l_s = _block(qb, kb, vb, s64, lo, hi, 0, 0)
+            out[0, qs:qe, h] = o_s
+            lse[0, h, qs:qe] = l_s
     return out, lse
 
 

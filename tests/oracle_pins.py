@@ -612,7 +612,91 @@ def pin_window_split_merge(orc):
         _close(l_, full[1], 1e-12, f"windowed split {bounds} (lse)")
 
 
+# --------------------------------------------------------------------------------------
+# padded and paged key lanes
+# --------------------------------------------------------------------------------------
+
+def _lane_case(rng):
+    lq, lk = [3, 1, 5, 2], [7, 9, 4, 11]
+    pad = 12
+    H, D = 2, 8
+    q = _bf16_round(_rand(rng, (1, sum(lq), H, D)))
+    k = np.zeros((1, pad * len(lk), H, D))
+    v = np.zeros((1, pad * len(lk), H, D))
+    for s, n in enumerate(lk):
+        k[0, s * pad:s * pad + n] = _bf16_round(_rand(rng, (n, H, D)))
+        v[0, s * pad:s * pad + n] = _bf16_round(_rand(rng, (n, H, D)))
+    return lq, lk, pad, q, k, v
+
+
+def pin_lanes_contiguous_equal_blockdiag(orc):
+    """Lanes packed back to back (seqstart = previous ends) are the block-diagonal masks
+    with cu_seqlens_k; bottom-right and windows included."""
+    rng = np.random.default_rng(51)
+    lq, lk, pad, q, k, v = _lane_case(rng)
+    cu_q = [0] + list(np.cumsum(lq))
+    cu_k = [0] + list(np.cumsum(lk))
+    kc = np.concatenate([k[:, s * pad:s * pad + n] for s, n in enumerate(lk)], axis=1)
+    vc = np.concatenate([v[:, s * pad:s * pad + n] for s, n in enumerate(lk)], axis=1)
+    for kind, br, wl in ((orc.MASK_BLOCKDIAG, False, None), (orc.MASK_BLOCKDIAG_CAUSAL, True, None),
+                         (orc.MASK_BLOCKDIAG_CAUSAL, False, 2), (orc.MASK_BLOCKDIAG_CAUSAL, True, 1)):
+        a = orc.attention_lanes(q, kc, vc, 0.5, kind, cu_q, lk, seqstart_k=cu_k[:-1],
+                                bottom_right=br, window_left=wl)
+        b = orc.attention(q, kc, vc, 0.5, kind, cu_q, cu_k, bottom_right=br, window_left=wl)
+        _close(a[0], b[0], 0.0, f"contiguous lanes = blockdiag out kind{kind} br{br} wl{wl}")
+        _close(a[1], b[1], 0.0, f"contiguous lanes = blockdiag lse kind{kind} br{br} wl{wl}")
+
+
+def pin_lanes_padding_unread(orc):
+    """Rows past a lane's valid keys never reach the result (NaN there changes nothing)."""
+    rng = np.random.default_rng(52)
+    lq, lk, pad, q, k, v = _lane_case(rng)
+    cu_q = [0] + list(np.cumsum(lq))
+    starts = [s * pad for s in range(len(lk))]
+    kn, vn = k.copy(), v.copy()
+    for s, n in enumerate(lk):
+        kn[0, s * pad + n:(s + 1) * pad] = np.nan
+        vn[0, s * pad + n:(s + 1) * pad] = np.nan
+    a = orc.attention_lanes(q, k, v, 0.5, orc.MASK_BLOCKDIAG_CAUSAL, cu_q, lk, seqstart_k=starts,
+                            bottom_right=True)
+    b = orc.attention_lanes(q, kn, vn, 0.5, orc.MASK_BLOCKDIAG_CAUSAL, cu_q, lk, seqstart_k=starts,
+                            bottom_right=True)
+    _close(a[0], b[0], 0.0, "padding unread (out)")
+    _close(a[1], b[1], 0.0, "padding unread (lse)")
+
+
+def pin_paged_equals_padded(orc):
+    """Scattering every lane's logical pages to a random permutation of physical pages
+    (and recording it in a block table) leaves the result unchanged."""
+    rng = np.random.default_rng(53)
+    lq, lk, pad, q, k, v = _lane_case(rng)
+    cu_q = [0] + list(np.cumsum(lq))
+    starts = [s * pad for s in range(len(lk))]
+    ps = 4
+    pages_per_lane = (pad + ps - 1) // ps
+    n_pages = pages_per_lane * len(lk) + 3
+    perm = rng.permutation(n_pages)
+    table = perm[:pages_per_lane * len(lk)].reshape(len(lk), pages_per_lane)
+    kp = np.full((1, n_pages * ps, 2, 8), np.nan)
+    vp = np.full((1, n_pages * ps, 2, 8), np.nan)
+    for s, n in enumerate(lk):
+        for p in range(n):
+            row = table[s][p // ps] * ps + p % ps
+            kp[0, row] = k[0, starts[s] + p]
+            vp[0, row] = v[0, starts[s] + p]
+    for kind, br, wl in ((orc.MASK_BLOCKDIAG, False, None), (orc.MASK_BLOCKDIAG_CAUSAL, True, 2)):
+        a = orc.attention_lanes(q, k, v, 0.5, kind, cu_q, lk, seqstart_k=starts, bottom_right=br,
+                                window_left=wl)
+        b = orc.attention_lanes(q, kp, vp, 0.5, kind, cu_q, lk, block_table=table, page_size=ps,
+                                bottom_right=br, window_left=wl)
+        _close(a[0], b[0], 0.0, f"paged = padded out kind{kind}")
+        _close(a[1], b[1], 0.0, f"paged = padded lse kind{kind}")
+
+
 PINS = [
+    pin_lanes_contiguous_equal_blockdiag,
+    pin_lanes_padding_unread,
+    pin_paged_equals_padded,
     pin_window_single_key,
     pin_bottom_right_reductions,
     pin_band_bruteforce,

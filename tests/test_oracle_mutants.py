@@ -41,6 +41,14 @@ MUTANTS = {
                                 "_block(qb_all[qs:qe], kb_all, vb_all, s64,"),
     "blockdiag_absolute_positions": ("s64, lo, hi, 0,\n                              kv_offset)",
                                      "s64, lo, hi, qs,\n                              ks + kv_offset)"),
+    "paged_index_swapped": ("return pages[p // page_size] * page_size + p % page_size",
+                            "return pages[p % page_size] * page_size + p // page_size"),
+    "lane_shared_head_always_zero": ("hk = 0 if k.shape[2] == 1 else h", "hk = 0"),
+    "lane_start_ignored": ("return int(seqstart_k[s]) + p", "return p"),
+    "lane_reads_padding": ("n = int(seqlen_k[s])", "n = int(seqlen_k[s]) + 1"),
+    "lane_bottom_right_uses_padding": (
+        "_band(mask_kind, bottom_right, window_left, window_right, qe - qs, len(rows))",
+        "_band(mask_kind, bottom_right, window_left, window_right, qe - qs, len(rows) + 1)"),
     "merge_averages": ("coef = w / sum_w[None]", "coef = np.ones_like(w) / w.shape[0]"),
     "merge_lse_drops_shift": ("lse = m_star + np.log(sum_w)", "lse = np.log(sum_w)"),
     "merge_unnormalised": ("coef = w / sum_w[None]", "coef = w"),
