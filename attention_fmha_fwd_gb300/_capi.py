@@ -52,6 +52,12 @@ class Band(ctypes.Structure):
                 ("window_right", ctypes.c_int32)]
 
 
+class KvLanes(ctypes.Structure):
+    _fields_ = [("seqlen_k", ctypes.c_void_p), ("seqstart_k", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
+                ("max_pages", ctypes.c_int32)]
+
+
 class MslkError(RuntimeError):
     """A non-OK mslk_status, with the library's reason string."""
 
@@ -79,6 +85,9 @@ SIGNATURES = {
     "mslk_attn_partial_band": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32,
                                       _i32, ctypes.c_float, _i32, ctypes.POINTER(Seqlens),
                                       ctypes.POINTER(Band), _i64, _P, _i32, _P, _P]),
+    "mslk_attn_fwd_lanes": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32,
+                                   ctypes.c_float, _i32, ctypes.POINTER(Seqlens),
+                                   ctypes.POINTER(KvLanes), ctypes.POINTER(Band), _P, _P, _P]),
     "mslk_merge_attentions": (_i32, [_P, _P, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _S, _S,
                                      _P, _i32, _P, _P]),
     "mslk_last_error": (ctypes.c_char_p, []),

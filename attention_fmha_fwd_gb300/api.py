@@ -152,6 +152,83 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", 
     return out, lse
 
 
+def _i32_dev(t, name):
+    if t is None:
+        return None
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    return t
+
+
+def _pool_rows(t: torch.Tensor, name: str) -> torch.Tensor:
+    """[n_pages, page_size, H, D] -> a [1, n_pages * page_size, H, D] view (pages adjacent)."""
+    if t.dim() == 4 and t.shape[0] > 1:
+        if t.stride(0) != t.shape[1] * t.stride(1):
+            raise ValueError(f"{name}: pages must be adjacent rows (stride(0) == page_size * stride(1))")
+        return t.as_strided((1, t.shape[0] * t.shape[1], t.shape[2], t.shape[3]),
+                            (t.shape[0] * t.stride(0), t.stride(1), t.stride(2), t.stride(3)))
+    return t
+
+
+def attn_fwd_lanes(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, seqlen_k, cu_seqlens_q,
+                   max_seqlen_q, max_seqlen_k, seqstart_k=None, block_table=None, page_size=None,
+                   mask="blockdiag_causal", scale=None, out=None, lse=True, stream=None,
+                   bottom_right=False, window_left=None, window_right=None):
+    """Forward over per-sequence key lanes: padded (``seqstart_k``) or paged (``block_table``).
+
+    The padded-keys and paged block-diagonal masks of "Attention - Biases & masks": queries
+    packed [1, total_q, H, K] with ``cu_seqlens_q``; sequence s sees ``seqlen_k[s]`` keys,
+    logical key p at K/V row ``seqstart_k[s] + p`` or, paged, at row
+    ``block_table[s, p // page_size] * page_size + p % page_size`` of the pool.  k, v are
+    [1, rows, H, K] or a page pool [n_pages, page_size, H, K].  ``mask`` is a block-diagonal
+    kind; ``bottom_right=True`` (or "blockdiag_causal_bottom_right") is the causal-with-offset
+    alignment (query i of a sequence pairs with key i + seqlen_k - seqlen_q).  Returns
+    (out [1, total_q, H, Kv], lse [1, H, total_q] or None).
+    """
+    q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
+    k, v = _pool_rows(k, "k"), _pool_rows(v, "v")
+    _check_inputs(q, k, v)
+    B, M, H, K = q.shape
+    if B != 1:
+        raise ValueError("attn_fwd_lanes takes packed queries [1, total_q, H, K]")
+    Mkv, Kv = k.shape[1], v.shape[3]
+    mk = _mask_kind(mask)
+    if mk not in _BLOCKDIAG:
+        raise ValueError("key lanes need a block-diagonal mask kind")
+    sk_len = _i32_dev(seqlen_k, "seqlen_k")
+    start = _i32_dev(seqstart_k, "seqstart_k")
+    table = _i32_dev(block_table, "block_table")
+    if sk_len is None or (start is None and table is None):
+        raise ValueError("attn_fwd_lanes needs seqlen_k and either seqstart_k or block_table")
+    max_pages = 0
+    if table is not None:
+        if table.dim() != 2 or page_size is None:
+            raise ValueError("block_table must be [n_seqs, max_pages] with page_size given")
+        max_pages = table.shape[1]
+    cq = _i32_dev(cu_seqlens_q, "cu_seqlens_q")
+    if cq is None:
+        raise ValueError("attn_fwd_lanes needs cu_seqlens_q")
+    sl = Seqlens(cq.data_ptr(), sk_len.data_ptr(), cq.numel() - 1, int(max_seqlen_q), int(max_seqlen_k))
+    lanes = _capi.KvLanes(sk_len.data_ptr(), _ptr(start), _ptr(table),
+                          0 if page_size is None else int(page_size), max_pages)
+    if out is None:
+        out = torch.empty((1, M, H, Kv), dtype=torch.bfloat16, device=q.device)
+    if lse is True:
+        lse = torch.empty((1, H, M), dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
+    so = _bmhk_strides(out, "out")
+    band = _band(bottom_right, window_left, window_right)
+    lib = _capi.load()
+    check(lib.mslk_attn_fwd_lanes(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
+                                  ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), M, Mkv, H, K,
+                                  Kv, 0.0 if scale is None else float(scale), mk, ctypes.byref(sl),
+                                  ctypes.byref(lanes), None if band is None else ctypes.byref(band),
+                                  out.data_ptr(), _ptr(lse), _stream_handle(stream, q.device)))
+    return out, lse
+
+
 def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none",
                  scale=None, kv_offset: int = 0, cu_seqlens_q=None, cu_seqlens_k=None,
                  max_seqlen_q=None, max_seqlen_k=None, out_dtype=torch.float32, out=None,

@@ -60,8 +60,20 @@ struct DecArgs {
   int hk_shared;
   int cs;  // CTAs per (batch, head): the cluster size
   // Key j is allowed for query row m iff m + lo <= j <= m + hi (kv_offset folded in;
-  // +-kBandOpen: open).
+  // +-kBandOpen: open), plus each packed sequence's Lk - Lq when band_seq is set.
   long long lo, hi;
+  int band_seq;
+  // Sequence mode (block-diagonal kinds): grid row = packed sequence s, its queries
+  // cu_q[s]..cu_q[s+1], its keys cu_k[s]..cu_k[s+1] or a key lane (lane_len[s] keys at
+  // lane_start[s] + p, or paged at block_table[s * max_pages + p / page_size] *
+  // page_size + p % page_size).
+  int seq_mode, lanes;
+  const int* cu_q;
+  const int* cu_k;
+  const int* lane_len;
+  const int* lane_start;
+  const int* block_table;
+  int page_size, max_pages;
   float scale_log2;
   void* out;
   int out_fp32;
@@ -170,13 +182,16 @@ struct DecodeState {
 // Folds one tile of keys (in shared memory, row-major [T][D]) into the warp's
 // online-softmax state, 32 keys at a time.
 template <int D, int MQ>
-MSLK_DEV void fold_tile(const DecArgs& a, const float (&qf)[MQ][D / 32], const uint8_t* sK,
-                        const uint8_t* sV, int key0, int kb1, int lane, DecodeState<D, MQ>& st) {
+MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ][D / 32],
+                        const uint8_t* sK, const uint8_t* sV, int key0, int kb1, int lane,
+                        DecodeState<D, MQ>& st) {
   constexpr int VE = D / 32;
   constexpr int T = DecLayout<D>::kT;
   using VT = typename Vec<VE>::T;
 #pragma unroll 1
   for (int sb = 0; sb < T; sb += 32) {
+    const int n_valid = kb1 - (key0 + sb);  // keys of this block below kb1 (warp-uniform)
+    if (n_valid <= 0) break;                // the rest of the tile is past the range
     const int my_key = key0 + sb + lane;
     const VT* kp = reinterpret_cast<const VT*>(sK + (sb * D + lane * VE) * 2);
     const VT* vp = reinterpret_cast<const VT*>(sV + (sb * D + lane * VE) * 2);
@@ -184,7 +199,7 @@ MSLK_DEV void fold_tile(const DecArgs& a, const float (&qf)[MQ][D / 32], const u
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
       p[m] = 0.f;
-      if (m >= a.M) continue;
+      if (m >= nq) continue;
       float part[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -196,7 +211,7 @@ MSLK_DEV void fold_tile(const DecArgs& a, const float (&qf)[MQ][D / 32], const u
         part[j] = d;
       }
       float sc = butterfly_reduce32(part, lane);
-      const bool allowed = my_key < kb1 && my_key <= m + a.hi && my_key >= m + a.lo;
+      const bool allowed = my_key < kb1 && my_key <= m + hi && my_key >= m + lo;
       sc = allowed ? sc : -INFINITY;
       const float m_new = fmaxf(st.m_run[m], warp_max(sc));
       const float msub = (m_new == -INFINITY) ? 0.f : m_new;
@@ -207,6 +222,14 @@ MSLK_DEV void fold_tile(const DecArgs& a, const float (&qf)[MQ][D / 32], const u
 #pragma unroll
       for (int e = 0; e < VE; ++e) st.acc[m][e] *= alpha;
     }
+    // V rows at or past kb1 get p = 0, but they may hold anything (a key lane's
+    // unwritten tail) and 0 * NaN is NaN: this warp owns the tile, so it clears them.
+    if (n_valid < 32) {
+      uint8_t* tail = const_cast<uint8_t*>(sV) + (sb + n_valid) * D * 2;
+      for (int off = lane * 16; off < (32 - n_valid) * D * 2; off += 32 * 16)
+        *reinterpret_cast<uint4*>(tail + off) = make_uint4(0, 0, 0, 0);
+      __syncwarp();
+    }
     // One pass over the V rows for every query row.
 #pragma unroll 4
     for (int j = 0; j < 32; ++j) {
@@ -214,7 +237,7 @@ MSLK_DEV void fold_tile(const DecArgs& a, const float (&qf)[MQ][D / 32], const u
       Vec<VE>::to_float(vp[j * (D / VE)], vf);
 #pragma unroll
       for (int m = 0; m < MQ; ++m) {
-        if (m >= a.M) continue;
+        if (m >= nq) continue;
         const float pj = __shfl_sync(0xffffffffu, p[m], j);
 #pragma unroll
         for (int e = 0; e < VE; ++e) st.acc[m][e] = fmaf(pj, vf[e], st.acc[m][e]);
@@ -239,17 +262,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int rank = static_cast<int>(blockIdx.x) % a.cs;  // CTA rank inside the cluster
   const int h = static_cast<int>(blockIdx.x) / a.cs;
-  const int b = blockIdx.y;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int hk = a.hk_shared ? 0 : h;
+  // This CTA's query rows [qrow0, qrow0 + nq) and keys [0, nk) (row krow0 + key, or paged)
+  // of batch coordinate bc: a batch (dense) or a packed sequence s (sequence mode).
+  const int s_idx = blockIdx.y;
+  int bc = s_idx, qrow0 = 0, nq = a.M, nk = a.Mkv, krow0 = 0;
+  long long lo = a.lo, hi = a.hi;
+  if (a.seq_mode) {
+    bc = 0;
+    qrow0 = min(max(a.cu_q[s_idx], 0), a.M);
+    nq = min(min(max(a.cu_q[s_idx + 1], qrow0), a.M) - qrow0, MQ);
+    if (a.lanes) {
+      nk = max(a.lane_len[s_idx], 0);
+      if (a.block_table != nullptr)
+        nk = static_cast<int>(min(static_cast<long long>(nk), static_cast<long long>(a.max_pages) * a.page_size));
+      else
+        krow0 = a.lane_start[s_idx];
+    } else {
+      krow0 = min(max(a.cu_k[s_idx], 0), a.Mkv);
+      nk = min(max(a.cu_k[s_idx + 1], krow0), a.Mkv) - krow0;
+    }
+    if (a.band_seq) {
+      const long long shift = static_cast<long long>(nk) - nq;
+      if (lo > -kBandOpen) lo += shift;
+      if (hi < kBandOpen) hi += shift;
+    }
+  }
 
-  // Keys of this (batch, head) that some row may see: from row 0's lower band edge to
-  // row M-1's upper edge, split over the cluster's CTAs in whole tiles.
-  const long long k_first = max(0LL, a.lo);
-  const long long k_last = min(static_cast<long long>(a.Mkv) - 1, static_cast<long long>(a.M - 1) + a.hi);
-  const int tile_first = k_first <= k_last ? static_cast<int>(k_first / T) : 0;
-  const int tiles_all = k_first <= k_last ? static_cast<int>(k_last / T) + 1 - tile_first : 0;
+  // Keys of this (batch or sequence, head) that some row may see: from row 0's lower band
+  // edge to the last row's upper edge, split over the cluster's CTAs in whole tiles.
+  const long long k_first = max(0LL, lo);
+  const long long k_last = min(static_cast<long long>(nk) - 1, static_cast<long long>(nq - 1) + hi);
+  const bool any = k_first <= k_last && nq > 0;
+  const int tile_first = any ? static_cast<int>(k_first / T) : 0;
+  const int tiles_all = any ? static_cast<int>(k_last / T) + 1 - tile_first : 0;
   const int per_cta = (tiles_all + a.cs - 1) / a.cs;
   const int t0 = min(tiles_all, rank * per_cta);
   const int n_tiles = max(0, min(tiles_all, t0 + per_cta) - t0);
@@ -285,6 +333,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int issued = 0;
+      // Paged lane (T divides page_size): the page table entry of the next page is read
+      // one page ahead, so its latency is off the issue path.
+      const bool paged = a.seq_mode && a.block_table != nullptr;
+      const int* table = paged ? a.block_table + static_cast<long long>(s_idx) * a.max_pages : nullptr;
+      const int n_pages_lane = paged ? (nk + a.page_size - 1) / a.page_size : 0;
+      int page = paged ? key_base / a.page_size : 0;
+      int in_page = paged ? key_base - page * a.page_size : 0;  // key offset inside the page
+      int phys = (paged && page < n_pages_lane) ? table[page] : 0;
+      int phys_next = (paged && page + 1 < n_pages_lane) ? table[page + 1] : 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % kStages;
         if (i >= kStages &&
@@ -292,9 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         const uint32_t full = sbase + L::kFullOff + 8 * s;
         const uint32_t dst = sbase + s * L::kStageBytes;
+        const int row = paged ? phys * a.page_size + in_page : krow0 + key_base + i * T;
+        if (paged && (in_page += T) == a.page_size) {  // the next tile starts the next page
+          in_page = 0;
+          ++page;
+          phys = phys_next;
+          phys_next = page + 1 < n_pages_lane ? table[page + 1] : 0;
+        }
         mbar_arrive_expect_tx(full, L::kStageBytes);
-        tma_load_4d(dst, &tm_k, full, 0, key_base + i * T, hk, b);
-        tma_load_4d(dst + L::kTileBytes, &tm_v, full, 0, key_base + i * T, hk, b);
+        tma_load_4d(dst, &tm_k, full, 0, row, hk, bc);
+        tma_load_4d(dst + L::kTileBytes, &tm_v, full, 0, row, hk, bc);
         ++issued;
         __threadfence_block();
         *issued_ctr = issued;
@@ -318,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float qf[MQ][VE];
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
-      if (m < a.M) {
-        const VT x = *reinterpret_cast<const VT*>(a.q + b * a.sq_b + m * a.sq_m + h * a.sq_h + lane * VE);
+      if (m < nq) {
+        const VT x = *reinterpret_cast<const VT*>(a.q + bc * a.sq_b + (qrow0 + m) * a.sq_m + h * a.sq_h + lane * VE);
         Vec<VE>::to_float(x, qf[m]);
 #pragma unroll
         for (int e = 0; e < VE; ++e) qf[m][e] *= a.scale_log2;
@@ -335,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      wait_bounded(sbase + L::kFullOff + 8 * s, (i / kStages) & 1, abort_flag, a));
       if (!ok) break;
       const uint8_t* sK = smem + s * L::kStageBytes;
-      fold_tile<D, MQ>(a, qf, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
+      fold_tile<D, MQ>(nq, lo, hi, qf, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
       __syncwarp();
       if (lane == 0) mbar_arrive(sbase + L::kEmptyOff + 8 * s);
     }
@@ -364,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   // Warp w merges row w (MQ <= 8: at most one row per warp).
-  for (int m = warp; m < a.M && m < MQ; m += kWarps + 1) {
+  for (int m = warp; m < nq; m += kWarps + 1) {
     float mstar = -INFINITY;
     for (int w = 0; w < kWarps; ++w) mstar = fmaxf(mstar, s_m[w][m]);
     const float msub = (mstar == -INFINITY) ? 0.f : mstar;
@@ -391,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // memory) alive until rank 0 has read them.
   if (a.cs > 1) cluster_sync(); else __syncthreads();
   if (rank == 0) {
-    for (int m = warp; m < a.M && m < MQ; m += kWarps + 1) {
+    for (int m = warp; m < nq; m += kWarps + 1) {
       float mstar = -INFINITY;
       for (int r = 0; r < a.cs; ++r)
         mstar = fmaxf(mstar, a.cs > 1 ? ld_shared_cluster_f32(mapa_shared(smem_u32(&c_m[m]), r)) : c_m[m]);
@@ -414,27 +478,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
       if (a.out_fp32) {
-        float* op = static_cast<float*>(a.out) + b * a.so_b + m * a.so_m + h * a.so_h + lane * VE;
+        float* op = static_cast<float*>(a.out) + bc * a.so_b + (qrow0 + m) * a.so_m + h * a.so_h + lane * VE;
 #pragma unroll
         for (int e = 0; e < VE; ++e) op[e] = o[e] * inv;
       } else {
         __nv_bfloat16* op =
-            static_cast<__nv_bfloat16*>(a.out) + b * a.so_b + m * a.so_m + h * a.so_h + lane * VE;
+            static_cast<__nv_bfloat16*>(a.out) + bc * a.so_b + (qrow0 + m) * a.so_m + h * a.so_h + lane * VE;
 #pragma unroll
         for (int e = 0; e < VE; e += 2)
           *reinterpret_cast<uint32_t*>(op + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
       }
       if (lane == 0 && a.lse != nullptr)
-        a.lse[(static_cast<long long>(b) * a.H + h) * a.M + m] =
+        a.lse[(static_cast<long long>(bc) * a.H + h) * a.M + qrow0 + m] =
             (Ls > 0.f) ? (mstar + lg2_approx(Ls)) * kLn2 : -INFINITY;
     }
   }
   if (a.cs > 1) cluster_sync();
 }
 
+// B: grid rows (batches, or packed sequences in sequence mode); rows_q / rows_k: the
+// longest query and key range of one grid row.
 template <int D, int MQ>
 cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, int B, int H,
-                      cudaStream_t stream) {
+                      int rows_q, int rows_k, cudaStream_t stream) {
   using L = DecLayout<D>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory");
   static_assert(2 * kWarps * MQ * 4 + kWarps * MQ * D * 4 + 2 * MQ * 4 + MQ * D * 4 <= L::kRingBytes,
@@ -482,9 +548,11 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, i
   // with every CTA keeping at least two tiles per consumer warp (ties: the smaller c).
   {
     const long long units = static_cast<long long>(B) * H;
-    // key tiles some row may see (the band's reach, as in the kernel)
-    const long long k_first = std::max(0LL, a.lo);
-    const long long k_last = std::min(static_cast<long long>(a.Mkv) - 1, static_cast<long long>(a.M - 1) + a.hi);
+    // key tiles some row may see (the band's reach, as in the kernel; a per-sequence
+    // shift is unknown here, so such bands count every key)
+    const long long lo = a.band_seq ? -kBandOpen : a.lo, hi = a.band_seq ? kBandOpen : a.hi;
+    const long long k_first = std::max(0LL, lo);
+    const long long k_last = std::min(static_cast<long long>(rows_k) - 1, static_cast<long long>(rows_q - 1) + hi);
     const long long tiles = k_first <= k_last ? k_last / L::kT + 1 - k_first / L::kT : 0;
     int best = 1;
     double best_cost = 1e300;
@@ -517,11 +585,11 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, i
 
 template <int D>
 cudaError_t launch_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecArgs& a, int B, int H,
-                     cudaStream_t stream) {
-  if (a.M <= 1) return launch_dm<D, 1>(tk, tv, a, B, H, stream);
-  if (a.M <= 2) return launch_dm<D, 2>(tk, tv, a, B, H, stream);
-  if (a.M <= 4) return launch_dm<D, 4>(tk, tv, a, B, H, stream);
-  return launch_dm<D, 8>(tk, tv, a, B, H, stream);
+                     int rows_q, int rows_k, cudaStream_t stream) {
+  if (rows_q <= 1) return launch_dm<D, 1>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  if (rows_q <= 2) return launch_dm<D, 2>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  if (rows_q <= 4) return launch_dm<D, 4>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  return launch_dm<D, 8>(tk, tv, a, B, H, rows_q, rows_k, stream);
 }
 
 
@@ -564,9 +632,26 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   a.err = ctl.err;
   a.timeout_ns = ctl.timeout_ns;
   a.cs = 1;  // chosen per kernel instantiation from the device's cluster residency
+  int grid_rows = p.B, rows_q = p.M, rows_k = p.Mkv;
+  if (is_blockdiag(p.mask_kind)) {
+    a.seq_mode = 1;
+    a.cu_q = p.cu_q;
+    a.cu_k = p.cu_k;
+    a.band_seq = p.band_seq_shift ? 1 : 0;
+    a.lanes = p.lanes ? 1 : 0;
+    a.lane_len = p.lane_len;
+    a.lane_start = p.lane_start;
+    a.block_table = p.block_table;
+    a.page_size = p.page_size;
+    a.max_pages = p.max_pages;
+    grid_rows = p.n_seqs;
+    rows_q = p.max_seqlen_q;
+    rows_k = p.max_seqlen_k;
+  }
+  if (grid_rows == 0 || rows_q == 0) return cudaSuccess;
   *why = "decode kernel launch failed";
-  if (D == 128) return launch_d<128>(tk, tv, a, p.B, p.H, stream);
-  return launch_d<64>(tk, tv, a, p.B, p.H, stream);
+  if (D == 128) return launch_d<128>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
+  return launch_d<64>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
 }
 
 }  // namespace mslk

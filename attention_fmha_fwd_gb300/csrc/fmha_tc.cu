@@ -104,6 +104,13 @@ struct TcArgs {
   // when band_seq is set.
   long long lo, hi;
   int band_seq;
+  // Key lanes (varlen only): lane_len[z] keys, at lane_start[z] + p or, paged, at
+  // block_table[z * max_pages + p / page_size] * page_size + p % page_size.
+  int lanes;
+  const int* lane_len;
+  const int* lane_start;
+  const int* block_table;
+  int page_size, max_pages;
   const int* cu_q;
   const int* cu_k;
   void* out;
@@ -183,7 +190,7 @@ MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32
 
 // One work unit: 256 query rows of one (batch or packed sequence, head).
 struct Unit {
-  int b, h, hk;
+  int b, h, hk, z;
   int q_base, Lq, k_base, Lk;
   int r0;
   int lo, hi;  // the band of this unit's sequence (see TcArgs), clamped to +-2^30
@@ -207,16 +214,27 @@ MSLK_DEV bool decode_unit(const TcArgs& a, int i, Unit& u) {
   u.h = rem % a.H;
   const int z = rem / a.H;
   u.hk = a.hk_shared ? 0 : u.h;
+  u.z = z;
   if (a.varlen) {
     u.b = 0;
     const int qs = min(max(a.cu_q[z], 0), a.M);
     const int qe = min(max(a.cu_q[z + 1], qs), a.M);
-    const int ks = min(max(a.cu_k[z], 0), a.Mkv);
-    const int ke = min(max(a.cu_k[z + 1], ks), a.Mkv);
     u.q_base = qs;
     u.Lq = qe - qs;
-    u.k_base = ks;
-    u.Lk = ke - ks;
+    if (a.lanes) {
+      // Rows outside [0, Mkv) are clipped by the tensor map (zero fill); a paged lane is
+      // cut at the end of its page table.
+      u.k_base = a.block_table != nullptr ? 0 : a.lane_start[z];
+      int len = max(a.lane_len[z], 0);
+      if (a.block_table != nullptr) len = static_cast<int>(min(static_cast<long long>(len),
+                                                               static_cast<long long>(a.max_pages) * a.page_size));
+      u.Lk = len;
+    } else {
+      const int ks = min(max(a.cu_k[z], 0), a.Mkv);
+      const int ke = min(max(a.cu_k[z + 1], ks), a.Mkv);
+      u.k_base = ks;
+      u.Lk = ke - ks;
+    }
   } else {
     u.b = z;
     u.q_base = 0;
@@ -359,9 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wait_bar_warp(kv_empty(s), ((it / L::kStages) & 1) ^ 1, wc))) return;
       mbar_arrive_expect_tx_elect(kv_full(s), L::kTileBytes);
       const CUtensorMap* tm = which ? &tm_v : &tm_k;
+      int row = u.k_base + j * kBlockN;
+      if (a.block_table != nullptr) {  // paged lane: the tile lies inside one page
+        const int key = j * kBlockN;
+        row = a.block_table[static_cast<long long>(u.z) * a.max_pages + key / a.page_size] * a.page_size +
+              key % a.page_size;
+      }
       for (int kb = 0; kb < L::kKBlocks; ++kb)
-        tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64,
-                          u.k_base + j * kBlockN, u.hk, u.b);
+        tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64, row, u.hk, u.b);
       ++it;
     };
     for (int k = 0; k < n_rounds && ok; ++k) {
@@ -452,6 +475,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sv = iv % L::kStages;
         const int sk = ik % L::kStages;
         if (!(ok = wait_bar_warp(kv_full(sv), (iv / L::kStages) & 1, wc))) break;
+        if (a.lane_len != nullptr && (j + 1) * kBlockN > u.Lk) {
+          // A key lane's last tile: the rows past its last key may hold anything (an
+          // unwritten cache).  Their P is 0, but 0 * NaN is NaN in the PV MMA, so they are
+          // cleared first (row r of each 64-column block: bytes [128 r, 128 r + 128)).
+          const int r0 = max(0, u.Lk - j * kBlockN);
+          uint8_t* vt = smem + L::kKVOff + sv * L::kTileBytes;
+          for (int kb = 0; kb < L::kKBlocks; ++kb)
+            for (int off = r0 * 128 + lane * 16; off < kBlockN * 128; off += 32 * 16)
+              *reinterpret_cast<uint4*>(vt + kb * kSwizzleAtom + off) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor core
+          __syncwarp();
+        }
         // Q tile 0 (while key tile j is in its range): PV0_j, then S0_{j+1}
         if ((lo0 <= j && j < hi0)) {
           if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
@@ -863,6 +898,12 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.lo = p.band_lo <= -kBandOpen ? -kBandOpen : p.band_lo - p.kv_offset;
   a.hi = p.band_hi >= kBandOpen ? kBandOpen : p.band_hi - p.kv_offset;
   a.band_seq = p.band_seq_shift ? 1 : 0;
+  a.lanes = p.lanes ? 1 : 0;
+  a.lane_len = p.lane_len;
+  a.lane_start = p.lane_start;
+  a.block_table = p.block_table;
+  a.page_size = p.page_size;
+  a.max_pages = p.max_pages;
   a.varlen = is_blockdiag(p.mask_kind) ? 1 : 0;
   const int rows = a.varlen ? p.max_seqlen_q : p.M;
   a.units_m = (rows + kUnitRows - 1) / kUnitRows;

@@ -27,6 +27,13 @@ struct AttnProblem {
   // kinds with band_seq_shift, each sequence's Lk - Lq added to both bounds.
   int64_t band_lo, band_hi;
   bool band_seq_shift;
+  // Key lanes (block-diagonal kinds only): per-sequence key count, first row (padded
+  // lanes) or page table (paged lanes); lanes == false: keys come from cu_k.
+  bool lanes;
+  const int32_t* lane_len;
+  const int32_t* lane_start;
+  const int32_t* block_table;
+  int page_size, max_pages;
   void* out;
   bool out_fp32;
   float* lse;           // may be null (forward without lse)

@@ -229,7 +229,8 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   const DeviceCtl ctl = device_ctl();
   if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "%s: no CUDA device / module", who);
   const int policy = g_path_policy.load();
-  const bool decode_ok = p.M <= kDecodeMaxRows && !is_blockdiag(p.mask_kind);
+  const bool decode_ok = is_blockdiag(p.mask_kind) ? p.max_seqlen_q <= kDecodeMaxRows
+                                                   : p.M <= kDecodeMaxRows;
   cudaError_t e;
   const char* why = "launch failed";
   if (decode_ok && policy != 1) {
@@ -301,6 +302,53 @@ mslk_status mslk_attn_partial_band(const void* q, const void* k, const void* v,
                                       true, true, "mslk_attn_partial_band");
   if (s != MSLK_OK) return s;
   return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_partial_band");
+}
+
+mslk_status mslk_attn_fwd_lanes(const void* q, const void* k, const void* v, const mslk_strides* sq,
+                                const mslk_strides* sk, const mslk_strides* sv, const mslk_strides* so,
+                                int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv, float scale,
+                                int32_t mask_kind, const mslk_seqlens* seqlens,
+                                const mslk_kv_lanes* lanes, const mslk_band* band, void* out,
+                                float* lse, void* stream) {
+  const char* who = "mslk_attn_fwd_lanes";
+  if (!is_blockdiag(mask_kind))
+    return fail(MSLK_ERR_INVALID_ARG, "%s: key lanes need a block-diagonal mask kind (got %d)", who, mask_kind);
+  if (lanes == nullptr || lanes->seqlen_k == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: lanes->seqlen_k is required", who);
+  if (lanes->block_table != nullptr) {
+    if (lanes->page_size <= 0 || lanes->max_pages <= 0)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: paged lanes need page_size > 0 and max_pages > 0", who);
+  } else if (lanes->seqstart_k == nullptr) {
+    return fail(MSLK_ERR_INVALID_ARG, "%s: lanes need seqstart_k or block_table", who);
+  }
+  // cu_seqlens_k is not read for lanes: validation only needs a non-null pointer there.
+  mslk_seqlens sl{};
+  if (seqlens != nullptr) {
+    sl = *seqlens;
+    if (sl.cu_seqlens_k == nullptr) sl.cu_seqlens_k = lanes->seqlen_k;
+  }
+  AttnProblem p;
+  const mslk_status s = validate_attn(p, q, k, v, sq, sk, sv, so, 1, M, Mkv, H, K, Kv, scale,
+                                      mask_kind, seqlens ? &sl : nullptr, band, 0, out,
+                                      MSLK_DTYPE_BF16, lse, false, false, who);
+  if (s != MSLK_OK) return s;
+  if (lanes->block_table != nullptr) {
+    // A key tile never straddles a page: 64-key tiles (decode kernel, D = 64; 32 for D =
+    // 128), 128-key tiles (tensor-core kernel).
+    const bool decode = p.max_seqlen_q <= kDecodeMaxRows && g_path_policy.load() != 1;
+    const int multiple = decode ? 64 : 128;
+    if (lanes->page_size % multiple)
+      return fail(MSLK_ERR_UNSUPPORTED, "%s: page_size %d must be a multiple of %d", who,
+                  lanes->page_size, multiple);
+  }
+  p.lanes = true;
+  p.lane_len = lanes->seqlen_k;
+  p.lane_start = lanes->seqstart_k;
+  p.block_table = lanes->block_table;
+  p.page_size = lanes->page_size;
+  p.max_pages = lanes->max_pages;
+  p.cu_k = nullptr;
+  return run_attn(p, static_cast<cudaStream_t>(stream), who);
 }
 
 mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split, int32_t n_chunks,

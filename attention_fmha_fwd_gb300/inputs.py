@@ -54,6 +54,30 @@ def cu_seqlens(lengths) -> list[int]:
     return out
 
 
+def page_table(lengths, page_size: int, spare_pages: int = 1, seed: int = 0):
+    """A seeded paged layout for key lanes of the given lengths.
+
+    Lane s gets ceil(L_s / page_size) pages; all pages (those plus ``spare_pages`` unused
+    ones) are shuffled by a seeded permutation.  Table entries past a lane's pages point at
+    the last spare page.  Returns (table [n_seqs, max_pages] int32, n_pages, spare) with
+    ``spare`` the list of unused page indices (CPU tensors / ints).
+    """
+    if spare_pages < 1:
+        raise ValueError("page_table needs at least one spare page")
+    need = [(int(n) + page_size - 1) // page_size for n in lengths]
+    n_pages = sum(need) + spare_pages
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(n_pages, generator=g).tolist()
+    spare = perm[sum(need):]
+    max_pages = max(1, max(need))
+    table = torch.full((len(need), max_pages), spare[-1], dtype=torch.int32)
+    at = 0
+    for s, n in enumerate(need):
+        table[s, :n] = torch.tensor(perm[at:at + n], dtype=torch.int32)
+        at += n
+    return table, n_pages, spare
+
+
 def equal_chunks(Mkv: int, n: int) -> list[tuple[int, int]]:
     """``n`` contiguous key ranges [start, end) covering [0, Mkv), as equal as possible."""
     return [(c * Mkv // n, (c + 1) * Mkv // n) for c in range(n)]

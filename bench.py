@@ -536,6 +536,30 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
                                               "frac_hbm": b_few / t_few / 1e9 / peaks["hbm_gbs"],
                                               "launches": 1}
     del q1, k1, v1
+    # the same decode step over a paged cache: 16 lanes of 32768 keys in shuffled 256-key
+    # pages (one launch; rows come from the page table)
+    ps = 256
+    lk = [w.Mkv] * w.B
+    table, n_pages, _ = inputs.page_table(lk, ps, seed=0)
+    pad = n_pages * ps - w.B * w.Mkv  # the spare page
+    kp = torch.cat([kd.reshape(-1, w.H, w.K), kd.new_zeros((pad, w.H, w.K))]).view(n_pages, ps, w.H, w.K)
+    vp = torch.cat([vd.reshape(-1, w.H, w.Kv), vd.new_zeros((pad, w.H, w.Kv))]).view(n_pages, ps, w.H, w.Kv)
+    qp = qd.reshape(1, w.B, w.H, w.K)
+    tbl, sk = table.to(dev), torch.tensor(lk, dtype=torch.int32, device=dev)
+    cq = torch.arange(w.B + 1, dtype=torch.int32, device=dev)
+    op = torch.empty((1, w.B, w.H, w.Kv), dtype=torch.bfloat16, device=dev)
+    lp = torch.empty((1, w.H, w.B), dtype=torch.float32, device=dev)
+    paged = lambda: fa.attn_fwd_lanes(qp, kp, vp, seqlen_k=sk, cu_seqlens_q=cq, max_seqlen_q=1,  # noqa: E731
+                                      max_seqlen_k=w.Mkv, block_table=tbl, page_size=ps,
+                                      scale=w.scale, bottom_right=True, out=op, lse=lp)
+    for _ in range(3):
+        paged()
+    t_pg = _time_it(paged, 10, stream, flush)
+    b_pg = sum(lk) * w.H * (w.K + w.Kv) * 2
+    res["decode_paged_16x32768_page256"] = {"us": t_pg * 1e6, "GB/s": b_pg / t_pg / 1e9,
+                                            "frac_hbm": b_pg / t_pg / 1e9 / peaks["hbm_gbs"],
+                                            "launches": 1}
+    del kp, vp
     del kd, vd, k, v
     # varlen packed block-diagonal causal
     w = inputs.WORKLOADS["varlen_packed"]
@@ -585,6 +609,29 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
         bflops = band_pairs(M, Mkv, Mkv - M if br else 0, wl) * 2 * 256 * 32
         res[name] = {"us": t_b * 1e6, "TFLOP/s": bflops / t_b / 1e12,
                      "frac_bf16": bflops / t_b / 1e12 / peaks["bf16_tflops"]}
+        if br:
+            # the same chunked prefill over a paged cache: 8192 keys in shuffled 256-key pages
+            ps = 256
+            table, n_pages, _ = inputs.page_table([Mkv], ps, seed=6)
+            pad = n_pages * ps - Mkv
+            kp = torch.cat([kd[0], kd.new_zeros((pad, 32, 128))]).view(n_pages, ps, 32, 128)
+            vp = torch.cat([vd[0], vd.new_zeros((pad, 32, 128))]).view(n_pages, ps, 32, 128)
+            tbl = table.to(dev)
+            sk = torch.tensor([Mkv], dtype=torch.int32, device=dev)
+            cq = torch.tensor([0, M], dtype=torch.int32, device=dev)
+
+            def pstep():
+                fa.attn_fwd_lanes(qd, kp, vp, seqlen_k=sk, cu_seqlens_q=cq, max_seqlen_q=M,
+                                  max_seqlen_k=Mkv, block_table=tbl, page_size=ps, scale=w.scale,
+                                  bottom_right=True, out=bo, lse=bl)
+
+            for _ in range(3):
+                pstep()
+            t_p = _time_it(pstep, 10, stream, flush)
+            res["prefill_paged_1x2048x8192x32x128_page256"] = {
+                "us": t_p * 1e6, "TFLOP/s": bflops / t_p / 1e12,
+                "frac_bf16": bflops / t_p / 1e12 / peaks["bf16_tflops"]}
+            del kp, vp
         del qd, kd, vd
     return res
 

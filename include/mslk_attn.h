@@ -182,6 +182,41 @@ mslk_status mslk_attn_partial_band(const void* q, const void* k, const void* v,
                                    void* stream);
 
 /*
+ * Key lanes (same page: BlockDiagonalPaddedKeysMask, BlockDiagonalCausalWithOffsetPadded-
+ * KeysMask, PagedBlockDiagonalPaddedKeysMask and their local variants; named without
+ * formulas, this is the reading the library implements).  Queries are packed as for the
+ * block-diagonal kinds (cu_seqlens_q); sequence s owns a key lane of seqlen_k[s] valid
+ * keys.  Logical key p of lane s is K/V row seqstart_k[s] + p (padded lanes), or, when
+ * block_table is given, row block_table[s * max_pages + p / page_size] * page_size +
+ * p % page_size of a pool of pages.  All arrays are DEVICE int32.  Rows past a lane's
+ * valid keys are never read; keys past max_pages * page_size are ignored; rows outside
+ * [0, Mkv) read as zeros.  page_size: a multiple of 128, or of 64 when every sequence has
+ * at most 8 queries (the decode kernel streams 32/64-key tiles).
+ */
+typedef struct {
+  const int32_t* seqlen_k;     /* [n_seqs] valid keys of each lane */
+  const int32_t* seqstart_k;   /* [n_seqs] first row of each lane (unused with block_table) */
+  const int32_t* block_table;  /* [n_seqs * max_pages] physical page per logical page, or NULL */
+  int32_t page_size;           /* rows per page (block_table only) */
+  int32_t max_pages;           /* columns of block_table */
+} mslk_kv_lanes;
+
+/*
+ * mslk_attn_fwd_lanes — forward over key lanes.  q [1, total_q, H, K] packed with
+ * seqlens->cu_seqlens_q (n_seqs, max_seqlen_q; max_seqlen_k = the longest lane;
+ * cu_seqlens_k is not read); k, v [1, Mkv, H, D] hold the lanes or the page pool.
+ * mask_kind: MSLK_MASK_BLOCKDIAG, _BLOCKDIAG_CAUSAL or _BLOCKDIAG_CAUSAL_BOTTOM_RIGHT
+ * (the pages' "causal with offset"); band: optional window (NULL: none).
+ */
+mslk_status mslk_attn_fwd_lanes(const void* q, const void* k, const void* v,
+                                const mslk_strides* sq, const mslk_strides* sk,
+                                const mslk_strides* sv, const mslk_strides* so, int32_t M,
+                                int32_t Mkv, int32_t H, int32_t K, int32_t Kv, float scale,
+                                int32_t mask_kind, const mslk_seqlens* seqlens,
+                                const mslk_kv_lanes* lanes, const mslk_band* band, void* out,
+                                float* lse, void* stream);
+
+/*
  * mslk_merge_attentions — exact log-sum-exp merge of n chunk results into preallocated
  * outputs.  MSLK kernel reference, "Attention - Core fMHA" > merge_attentions (exact
  * normalised output over the union of chunks, not an average; write_lse; output_dtype)

@@ -184,3 +184,48 @@ def test_valid_call_without_device_reports_cuda_error(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="no fallback"):
         _capi.load(str(tmp_path / "libmslk_attn.so"))
+
+
+def _lanes_call(lib, lanes, mask=3, band=None, sl=None):
+    s = S(8 * 128 * 64, 8 * 128, 128)
+    r = ctypes.byref
+    sl = _capi.Seqlens(FAKE, None, 4, 8, 64) if sl is None else sl
+    st = lib.mslk_attn_fwd_lanes(FAKE, FAKE, FAKE, r(s), r(s), r(s), r(s), 64, 64, 8, 128, 128, 0.0,
+                                 mask, r(sl), None if lanes is None else r(lanes),
+                                 None if band is None else r(band), FAKE, FAKE, None)
+    return st, lib.mslk_last_error().decode()
+
+
+L = _capi.KvLanes
+
+
+@pytest.mark.parametrize("lanes,mask,status,needle", [
+    (L(FAKE, FAKE, None, 0, 0), 1, _capi.MSLK_ERR_INVALID_ARG, "block-diagonal"),
+    (None, 3, _capi.MSLK_ERR_INVALID_ARG, "seqlen_k"),
+    (L(None, FAKE, None, 0, 0), 3, _capi.MSLK_ERR_INVALID_ARG, "seqlen_k"),
+    (L(FAKE, None, None, 0, 0), 3, _capi.MSLK_ERR_INVALID_ARG, "seqstart_k or block_table"),
+    (L(FAKE, None, FAKE, 0, 4), 3, _capi.MSLK_ERR_INVALID_ARG, "page_size"),
+    (L(FAKE, None, FAKE, 64, 0), 3, _capi.MSLK_ERR_INVALID_ARG, "max_pages"),
+    (L(FAKE, None, FAKE, 96, 4), 3, _capi.MSLK_ERR_UNSUPPORTED, "multiple of 64"),
+])
+def test_lanes_rejects(lib, lanes, mask, status, needle):
+    st, why = _lanes_call(lib, lanes, mask)
+    assert st == status, why
+    assert needle in why
+
+
+def test_lanes_page_multiple_follows_query_rows(lib):
+    """Sequences of more than 8 queries take the 128-key tensor-core tiles."""
+    st, why = _lanes_call(lib, L(FAKE, None, FAKE, 64, 4), sl=_capi.Seqlens(FAKE, None, 4, 9, 64))
+    assert st == _capi.MSLK_ERR_UNSUPPORTED and "multiple of 128" in why
+
+
+def test_lanes_pass_validation(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for lanes, mask, band in ((L(FAKE, FAKE, None, 0, 0), 2, None),
+                              (L(FAKE, None, FAKE, 64, 4), 3, None),
+                              (L(FAKE, None, FAKE, 256, 2), 5, _capi.Band(0, 100, -1))):
+        st, why = _lanes_call(lib, lanes, mask, band)
+        assert st == _capi.MSLK_ERR_CUDA, why
