@@ -9,10 +9,14 @@ from .attention import (  # noqa: F401
     MASK_CAUSAL,
     MASK_NONE,
     attention,
+    attention_fp8,
     attention_head,
     attention_lanes,
+    attention_lanes_fp8,
     attention_partial,
+    decode_e4m3,
     default_scale,
+    dequantize_e4m3,
     lane_rows,
     merge_attentions,
     widen_bf16_bits,

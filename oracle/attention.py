@@ -326,3 +326,60 @@ def merge_attentions(out_split, lse_split):
         out += np.transpose(coef[c], (0, 2, 1))[..., None] * o   # [B,H,M] -> [B,M,H,1]
     return out, lse
 
+
+
+# --------------------------------------------------------------------------------------
+# FP8 E4M3 inputs
+# --------------------------------------------------------------------------------------
+#
+# The pages' Blackwell and FlashAttention-3 forward paths take FP8 E4M3 query, key and
+# value tensors with tensorwise or per-head scales ("Attention - Core fMHA" backends'
+# FP8 E4M3 topics; ``pack_fp8_tensorwise_per_head`` and the ``descale_q/k/v`` arguments of
+# the raw flash3 op).  Plainest reading: element x of head h stands for the real number
+# decode(x) * descale[h] (one shared value when tensorwise), and the attention is the
+# definition above applied to those real numbers.
+#
+# E4M3 (PyTorch's float8_e4m3fn): bit 7 sign; bits 6..3 exponent, bias 7; bits 2..0
+# mantissa.  Exponent field 0: subnormal, mantissa/8 * 2^-6.  Otherwise
+# (1 + mantissa/8) * 2^(exponent - 7).  Exponent 15 with mantissa 7 (0x7F, 0xFF) is NaN;
+# there are no infinities, so the largest finite magnitude is 1.75 * 2^8 = 448.
+
+def decode_e4m3(codes) -> np.ndarray:
+    """float64 values of E4M3 byte codes (any integer array of 0..255)."""
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def dequantize_e4m3(codes, descale) -> np.ndarray:
+    """[B, M, Hx, D] E4M3 codes times a per-head descale (scalar or [Hx], float32)."""
+    x = decode_e4m3(codes)
+    d = np.asarray(descale, dtype=np.float32).astype(np.float64).reshape(-1)
+    if d.size == 1:
+        return x * d[0]
+    if d.size != x.shape[2]:
+        raise ValueError(f"descale has {d.size} entries for {x.shape[2]} heads")
+    return x * d[None, None, :, None]
+
+
+def attention_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale, mask_kind=MASK_NONE,
+                  cu_seqlens_q=None, cu_seqlens_k=None, bottom_right=False, window_left=None,
+                  window_right=None):
+    """Attention forward on E4M3 inputs: the definition on the dequantized values."""
+    return attention(dequantize_e4m3(q8, descale_q), dequantize_e4m3(k8, descale_k),
+                     dequantize_e4m3(v8, descale_v), scale, mask_kind, cu_seqlens_q,
+                     cu_seqlens_k, 0, bottom_right, window_left, window_right)
+
+
+def attention_lanes_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale, mask_kind,
+                        cu_seqlens_q, seqlen_k, seqstart_k=None, block_table=None,
+                        page_size=None, bottom_right=False, window_left=None, window_right=None):
+    """Key-lane attention on E4M3 inputs (padded or paged), on the dequantized values."""
+    return attention_lanes(dequantize_e4m3(q8, descale_q), dequantize_e4m3(k8, descale_k),
+                           dequantize_e4m3(v8, descale_v), scale, mask_kind, cu_seqlens_q,
+                           seqlen_k, seqstart_k, block_table, page_size, bottom_right,
+                           window_left, window_right)

@@ -693,7 +693,108 @@ def pin_paged_equals_padded(orc):
         _close(a[1], b[1], 0.0, f"paged = padded lse kind{kind}")
 
 
+# --------------------------------------------------------------------------------------
+# FP8 E4M3 inputs
+# --------------------------------------------------------------------------------------
+
+def _torch_e4m3_table():
+    """PyTorch's own float8_e4m3fn widening of every byte code (a library routine)."""
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def pin_e4m3_table(orc):
+    """Every one of the 256 codes decodes as PyTorch's float8_e4m3fn does (NaN where it has NaN)."""
+    ref = _torch_e4m3_table()
+    got = np.asarray(orc.decode_e4m3(np.arange(256)), dtype=np.float64)
+    assert np.array_equal(np.isnan(ref), np.isnan(got)), "NaN codes differ"
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ref[fin], got[fin]), "decoded values differ"
+    assert np.array_equal(np.signbit(ref[fin]), np.signbit(got[fin])), "signs of zero differ"
+
+
+def pin_e4m3_known_values(orc):
+    """Values fixed by the format's definition (sign, exponent bias 7, 3-bit mantissa,
+    subnormals m/8 * 2^-6, 0x7F/0xFF NaN, largest finite 448), and ordering."""
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x0F: 1.875 * 2.0 ** -6,
+             0x38: 1.0, 0x39: 1.125, 0x3C: 1.5, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0,
+             0x81: -(2.0 ** -9), 0xB8: -1.0, 0xFE: -448.0}
+    got = orc.decode_e4m3(np.array(list(cases)))
+    for (code, want), g in zip(cases.items(), got):
+        assert g == want, f"code {code:#04x}: {g} != {want}"
+    assert np.isnan(orc.decode_e4m3(np.array([0x7F, 0xFF]))).all(), "0x7F/0xFF must be NaN"
+    pos = orc.decode_e4m3(np.arange(0x7F))
+    assert np.all(np.diff(pos) > 0), "positive codes must increase"
+
+
+def _fp8_case(rng, B, M, Mkv, H, Hk, D):
+    # finite codes only (NaN codes excluded), the whole range otherwise
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    q8 = rng.choice(codes, size=(B, M, H, D))
+    k8 = rng.choice(codes, size=(B, Mkv, Hk, D))
+    v8 = rng.choice(codes, size=(B, Mkv, Hk, D))
+    dq = np.float32(rng.uniform(0.001, 0.01, H))
+    dk = np.float32(rng.uniform(0.001, 0.01, Hk))
+    dv = np.float32(rng.uniform(0.001, 0.01, Hk))
+    return q8, k8, v8, dq, dk, dv
+
+
+def pin_fp8_bruteforce(orc):
+    """Per-head descales, element by element through PyTorch's E4M3 table, then the brute force."""
+    table = _torch_e4m3_table()
+    rng = np.random.default_rng(61)
+    for (B, M, Mkv, H, Hk, D, kind) in ((1, 3, 4, 2, 2, 4, 0), (2, 4, 5, 3, 1, 4, 1), (1, 3, 3, 2, 2, 8, 1)):
+        q8, k8, v8, dq, dk, dv = _fp8_case(rng, B, M, Mkv, H, Hk, D)
+
+        def deq(codes, d):
+            out = np.zeros(codes.shape)
+            for idx in np.ndindex(codes.shape):
+                out[idx] = table[codes[idx]] * float(d[idx[2]])
+            return out
+
+        ro, rl = brute_attention(deq(q8, dq), deq(k8, dk), deq(v8, dv), 0.3, kind)
+        o, l_ = orc.attention_fp8(q8, k8, v8, dq, dk, dv, 0.3, kind)
+        _close(o, ro, 1e-12, f"fp8 brute out {B, M, Mkv, H, Hk, D, kind}")
+        _close(l_, rl, 1e-12, f"fp8 brute lse {B, M, Mkv, H, Hk, D, kind}")
+
+
+def pin_fp8_descale_folding(orc):
+    """The value descale scales the output; the query and key descales multiply the scale."""
+    rng = np.random.default_rng(62)
+    q8, k8, v8, _, _, _ = _fp8_case(rng, 1, 5, 7, 2, 2, 8)
+    one = np.ones(2, dtype=np.float32)
+    a, b, c = np.float32(0.003), np.float32(0.004), np.float32(0.37)
+    base_o, base_l = orc.attention_fp8(q8, k8, v8, one, one, one, 0.5 * float(a) * float(b))
+    o, l_ = orc.attention_fp8(q8, k8, v8, np.full(2, a), np.full(2, b), np.full(2, c), 0.5)
+    # (the folded scale is rounded to float32 once more: relative differences ~1e-7)
+    _close(o, float(c) * base_o, 1e-5 * np.abs(base_o).max(), "descale_v scales out")
+    _close(l_, base_l, 1e-5 * max(1.0, np.abs(base_l).max()), "descale_q * descale_k fold into the scale")
+    # tensorwise (one value) equals the same value per head
+    o2, l2 = orc.attention_fp8(q8, k8, v8, a, b, c, 0.5)
+    _close(o2, o, 0.0, "tensorwise out")
+    _close(l2, l_, 0.0, "tensorwise lse")
+
+
+def pin_fp8_lanes(orc):
+    """FP8 key lanes laid out contiguously equal the FP8 block-diagonal forward."""
+    rng = np.random.default_rng(63)
+    lq, lk = [2, 3], [3, 4]
+    q8, k8, v8, dq, dk, dv = _fp8_case(rng, 1, 5, 7, 2, 2, 8)
+    cu_q, cu_k = [0, 2, 5], [0, 3, 7]
+    a = orc.attention_fp8(q8, k8, v8, dq, dk, dv, 0.4, orc.MASK_BLOCKDIAG_CAUSAL, cu_q, cu_k,
+                          bottom_right=True)
+    b = orc.attention_lanes_fp8(q8, k8, v8, dq, dk, dv, 0.4, orc.MASK_BLOCKDIAG_CAUSAL, cu_q, lk,
+                                seqstart_k=cu_k[:-1], bottom_right=True)
+    _close(a[0], b[0], 0.0, "fp8 lanes out")
+    _close(a[1], b[1], 0.0, "fp8 lanes lse")
+    assert lq == [2, 3]
+
+
 PINS = [
+    pin_e4m3_table,
+    pin_e4m3_known_values,
+    pin_fp8_bruteforce,
+    pin_fp8_descale_folding,
+    pin_fp8_lanes,
     pin_lanes_contiguous_equal_blockdiag,
     pin_lanes_padding_unread,
     pin_paged_equals_padded,

@@ -49,6 +49,16 @@ MUTANTS = {
     "lane_bottom_right_uses_padding": (
         "_band(mask_kind, bottom_right, window_left, window_right, qe - qs, len(rows))",
         "_band(mask_kind, bottom_right, window_left, window_right, qe - qs, len(rows) + 1)"),
+    "e4m3_bias_8": ("2.0 ** (e - 7)", "2.0 ** (e - 8)"),
+    "e4m3_subnormal_implicit_one": ("m / 8.0 * 2.0 ** -6", "(1.0 + m / 8.0) * 2.0 ** -6"),
+    "e4m3_no_nan": ("mag = np.where((e == 15) & (m == 7), np.nan, mag)", "mag = mag"),
+    "e4m3_sign_ignored": ("sign = np.where(c & 0x80, -1.0, 1.0)", "sign = 1.0"),
+    "fp8_descale_wrong_axis": ("d[None, None, :, None]", "d[None, :, None, None]"),
+    "fp8_descale_first_head_only": ("return x * d[0]\n", "return x * d[0]\n    d = d[:1]\n"),
+    "fp8_v_descale_ignored": ("dequantize_e4m3(v8, descale_v), scale, mask_kind, cu_seqlens_q,\n                     cu_seqlens_k",
+                              "dequantize_e4m3(v8, 1.0), scale, mask_kind, cu_seqlens_q,\n                     cu_seqlens_k"),
+    "fp8_k_uses_q_descale": ("attention(dequantize_e4m3(q8, descale_q), dequantize_e4m3(k8, descale_k),",
+                             "attention(dequantize_e4m3(q8, descale_q), dequantize_e4m3(k8, descale_q),"),
     "merge_averages": ("coef = w / sum_w[None]", "coef = np.ones_like(w) / w.shape[0]"),
     "merge_lse_drops_shift": ("lse = m_star + np.log(sum_w)", "lse = np.log(sum_w)"),
     "merge_unnormalised": ("coef = w / sum_w[None]", "coef = w"),
