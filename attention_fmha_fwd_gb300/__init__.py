@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     MASKS,
     MslkError,
     attn_fwd,
+    attn_fwd_fp8,
     attn_fwd_lanes,
     attn_partial,
     device_status,

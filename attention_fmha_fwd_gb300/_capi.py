@@ -58,6 +58,11 @@ class KvLanes(ctypes.Structure):
                 ("max_pages", ctypes.c_int32)]
 
 
+class Fp8Scales(ctypes.Structure):
+    _fields_ = [("descale_q", ctypes.c_void_p), ("descale_k", ctypes.c_void_p),
+                ("descale_v", ctypes.c_void_p), ("per_tensor", ctypes.c_int32)]
+
+
 class MslkError(RuntimeError):
     """A non-OK mslk_status, with the library's reason string."""
 
@@ -88,6 +93,9 @@ SIGNATURES = {
     "mslk_attn_fwd_lanes": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32,
                                    ctypes.c_float, _i32, ctypes.POINTER(Seqlens),
                                    ctypes.POINTER(KvLanes), ctypes.POINTER(Band), _P, _P, _P]),
+    "mslk_attn_fwd_fp8": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32, _i32,
+                                 ctypes.c_float, _i32, ctypes.POINTER(Seqlens), ctypes.POINTER(Band),
+                                 ctypes.POINTER(KvLanes), ctypes.POINTER(Fp8Scales), _P, _P, _P]),
     "mslk_merge_attentions": (_i32, [_P, _P, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _S, _S,
                                      _P, _i32, _P, _P]),
     "mslk_last_error": (ctypes.c_char_p, []),

@@ -229,6 +229,97 @@ def attn_fwd_lanes(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, seqlen_
     return out, lse
 
 
+_FP8_DTYPES = tuple(d for d in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if d is not None)
+
+
+def _descale(x, name, device):
+    """A descale argument as a contiguous fp32 device tensor (a Python float -> one value)."""
+    if isinstance(x, torch.Tensor):
+        if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor (or a float)")
+        return x.reshape(-1)
+    return torch.full((1,), float(x), dtype=torch.float32, device=device)
+
+
+def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descale_q, descale_k, descale_v,
+                 *, mask="none", scale=None, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
+                 max_seqlen_k=None, seqlen_k=None, seqstart_k=None, block_table=None, page_size=None,
+                 out=None, lse=True, stream=None, bottom_right=False, window_left=None,
+                 window_right=None):
+    """Forward on FP8 E4M3 q, k, v (uint8 codes or float8_e4m3fn tensors, [B, M, H, K]).
+
+    Element x of head h stands for x * descale[h]: each descale is a float (tensorwise) or
+    a float32 CUDA tensor of one value or one per head ([H] for q; [H], or [1] for a shared
+    k/v head, for k and v) — the FP8 E4M3 inputs of the pages' Blackwell / FlashAttention-3
+    forward backends.  Masks, windows and packed sequences as ``attn_fwd``; key lanes
+    (``seqlen_k`` with ``seqstart_k`` or ``block_table`` + ``page_size``) as
+    ``attn_fwd_lanes``.  Returns (out bf16 [B, M, H, Kv], lse fp32 [B, H, M] or None).
+    """
+    q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
+    lanes_mode = seqlen_k is not None
+    if lanes_mode:
+        k, v = _pool_rows(k, "k"), _pool_rows(v, "v")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (the library reads device memory)")
+        if t.dtype not in _FP8_DTYPES:
+            raise ValueError(f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    B, M, H, K = q.shape
+    Mkv, Kv = k.shape[1], v.shape[3]
+    mk = _mask_kind(mask)
+    dq, dk, dv = (_descale(x, n, q.device) for x, n in ((descale_q, "descale_q"),
+                                                       (descale_k, "descale_k"),
+                                                       (descale_v, "descale_v")))
+    sizes = {dq.numel(), dk.numel(), dv.numel()}
+    per_tensor = 1 if sizes == {1} else 0
+    if not per_tensor:
+        hk = 1 if (k.stride(2) == 0 and H > 1) else H
+        if dq.numel() != H or dk.numel() != hk or dv.numel() != hk:
+            raise ValueError(f"per-head descales need {H} (q) and {hk} (k, v) entries, or one each")
+    scales = _capi.Fp8Scales(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), per_tensor)
+    lanes = None
+    keep = []
+    if lanes_mode:
+        sk_len = _i32_dev(seqlen_k, "seqlen_k")
+        start = _i32_dev(seqstart_k, "seqstart_k")
+        table = _i32_dev(block_table, "block_table")
+        if start is None and table is None:
+            raise ValueError("key lanes need seqstart_k or block_table")
+        max_pages = 0
+        if table is not None:
+            if table.dim() != 2 or page_size is None:
+                raise ValueError("block_table must be [n_seqs, max_pages] with page_size given")
+            max_pages = table.shape[1]
+        cq = _i32_dev(cu_seqlens_q, "cu_seqlens_q")
+        if cq is None or max_seqlen_q is None or max_seqlen_k is None:
+            raise ValueError("key lanes need cu_seqlens_q, max_seqlen_q and max_seqlen_k")
+        sl_struct = Seqlens(cq.data_ptr(), sk_len.data_ptr(), cq.numel() - 1, int(max_seqlen_q),
+                            int(max_seqlen_k))
+        keep.append(sl_struct)
+        sl = ctypes.byref(sl_struct)
+        lanes = _capi.KvLanes(sk_len.data_ptr(), _ptr(start), _ptr(table),
+                              0 if page_size is None else int(page_size), max_pages)
+    else:
+        sl, keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    if out is None:
+        out = torch.empty((B, M, H, Kv), dtype=torch.bfloat16, device=q.device)
+    if lse is True:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
+    so = _bmhk_strides(out, "out")
+    band = _band(bottom_right, window_left, window_right)
+    lib = _capi.load()
+    check(lib.mslk_attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
+                                ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H, K,
+                                Kv, 0.0 if scale is None else float(scale), mk, sl,
+                                None if band is None else ctypes.byref(band),
+                                None if lanes is None else ctypes.byref(lanes), ctypes.byref(scales),
+                                out.data_ptr(), _ptr(lse), _stream_handle(stream, q.device)))
+    return out, lse
+
+
 def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none",
                  scale=None, kv_offset: int = 0, cu_seqlens_q=None, cu_seqlens_k=None,
                  max_seqlen_q=None, max_seqlen_k=None, out_dtype=torch.float32, out=None,

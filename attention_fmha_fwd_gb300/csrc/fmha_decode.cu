@@ -39,10 +39,12 @@ constexpr int kStages = 12;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+// F8: K/V (and Q) are E4M3 bytes, so a tile holds twice the keys in the same 8 KiB.
+template <int D, bool F8>
 struct DecLayout {
-  static constexpr int kT = 4096 / D;              // keys per tile: 32 (D=128), 64 (D=64)
-  static constexpr int kTileBytes = kT * D * 2;    // one tensor's tile: 8 KiB
+  static constexpr int kEsz = F8 ? 1 : 2;          // bytes per element
+  static constexpr int kT = 8192 / (D * kEsz);     // keys per tile: 32/64 (bf16), 64/128 (E4M3)
+  static constexpr int kTileBytes = kT * D * kEsz; // one tensor's tile: 8 KiB
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kFullOff = kRingBytes;      // full[kStages] mbarriers
@@ -54,7 +56,7 @@ struct DecLayout {
 };
 
 struct DecArgs {
-  const __nv_bfloat16* q;
+  const uint8_t* q;  // bf16 or E4M3 elements
   long long sq_b, sq_m, sq_h;
   int M, Mkv, H;
   int hk_shared;
@@ -75,6 +77,12 @@ struct DecArgs {
   const int* block_table;
   int page_size, max_pages;
   float scale_log2;
+  // E4M3 inputs: element x of head h stands for x * descale[h] (descale[0] when
+  // desc_per_tensor); q and k descales fold into the score scale, v's into the output.
+  const float* dq;
+  const float* dk;
+  const float* dv;
+  int desc_per_tensor;
   void* out;
   int out_fp32;
   long long so_b, so_m, so_h;
@@ -83,10 +91,11 @@ struct DecArgs {
   unsigned long long timeout_ns;
 };
 
-template <int V>
+// V consecutive head-dim elements of one row -> fp32 (bf16: widen; E4M3: exact convert).
+template <int V, bool F8>
 struct Vec;
 template <>
-struct Vec<4> {
+struct Vec<4, false> {
   using T = uint2;
   MSLK_DEV static void to_float(T x, float* f) {
     f[0] = __uint_as_float(x.x << 16);
@@ -96,11 +105,32 @@ struct Vec<4> {
   }
 };
 template <>
-struct Vec<2> {
+struct Vec<2, false> {
   using T = uint32_t;
   MSLK_DEV static void to_float(T x, float* f) {
     f[0] = __uint_as_float(x << 16);
     f[1] = __uint_as_float(x & 0xFFFF0000u);
+  }
+};
+template <>
+struct Vec<4, true> {
+  using T = uint32_t;
+  MSLK_DEV static void to_float(T x, float* f) {
+    const float2 a = e4m3x2_to_f2(static_cast<uint16_t>(x & 0xFFFFu));
+    const float2 b = e4m3x2_to_f2(static_cast<uint16_t>(x >> 16));
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+  }
+};
+template <>
+struct Vec<2, true> {
+  using T = uint16_t;
+  MSLK_DEV static void to_float(T x, float* f) {
+    const float2 a = e4m3x2_to_f2(x);
+    f[0] = a.x;
+    f[1] = a.y;
   }
 };
 
@@ -181,20 +211,21 @@ struct DecodeState {
 
 // Folds one tile of keys (in shared memory, row-major [T][D]) into the warp's
 // online-softmax state, 32 keys at a time.
-template <int D, int MQ>
+template <int D, int MQ, bool F8>
 MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ][D / 32],
                         const uint8_t* sK, const uint8_t* sV, int key0, int kb1, int lane,
                         DecodeState<D, MQ>& st) {
   constexpr int VE = D / 32;
-  constexpr int T = DecLayout<D>::kT;
-  using VT = typename Vec<VE>::T;
+  constexpr int T = DecLayout<D, F8>::kT;
+  constexpr int ES = DecLayout<D, F8>::kEsz;
+  using VT = typename Vec<VE, F8>::T;
 #pragma unroll 1
   for (int sb = 0; sb < T; sb += 32) {
     const int n_valid = kb1 - (key0 + sb);  // keys of this block below kb1 (warp-uniform)
     if (n_valid <= 0) break;                // the rest of the tile is past the range
     const int my_key = key0 + sb + lane;
-    const VT* kp = reinterpret_cast<const VT*>(sK + (sb * D + lane * VE) * 2);
-    const VT* vp = reinterpret_cast<const VT*>(sV + (sb * D + lane * VE) * 2);
+    const VT* kp = reinterpret_cast<const VT*>(sK + (sb * D + lane * VE) * ES);
+    const VT* vp = reinterpret_cast<const VT*>(sV + (sb * D + lane * VE) * ES);
     float p[MQ];
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
@@ -204,7 +235,7 @@ MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float kf[VE];
-        Vec<VE>::to_float(kp[j * (D / VE)], kf);
+        Vec<VE, F8>::to_float(kp[j * (D / VE)], kf);
         float d = 0.f;
 #pragma unroll
         for (int e = 0; e < VE; ++e) d = fmaf(qf[m][e], kf[e], d);
@@ -225,8 +256,8 @@ MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ
     // V rows at or past kb1 get p = 0, but they may hold anything (a key lane's
     // unwritten tail) and 0 * NaN is NaN: this warp owns the tile, so it clears them.
     if (n_valid < 32) {
-      uint8_t* tail = const_cast<uint8_t*>(sV) + (sb + n_valid) * D * 2;
-      for (int off = lane * 16; off < (32 - n_valid) * D * 2; off += 32 * 16)
+      uint8_t* tail = const_cast<uint8_t*>(sV) + (sb + n_valid) * D * ES;
+      for (int off = lane * 16; off < (32 - n_valid) * D * ES; off += 32 * 16)
         *reinterpret_cast<uint4*>(tail + off) = make_uint4(0, 0, 0, 0);
       __syncwarp();
     }
@@ -234,7 +265,7 @@ MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ
 #pragma unroll 4
     for (int j = 0; j < 32; ++j) {
       float vf[VE];
-      Vec<VE>::to_float(vp[j * (D / VE)], vf);
+      Vec<VE, F8>::to_float(vp[j * (D / VE)], vf);
 #pragma unroll
       for (int m = 0; m < MQ; ++m) {
         if (m >= nq) continue;
@@ -246,11 +277,9 @@ MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ
   }
 }
 
-template <int D, int MQ>
-__global__ void __launch_bounds__(kThreads, 1)
-    fmha_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                       const DecArgs a) {
-  using L = DecLayout<D>;
+template <int D, int MQ, bool F8>
+MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecArgs& a) {
+  using L = DecLayout<D, F8>;
   constexpr int VE = D / 32;  // head-dim elements per lane
   constexpr int T = L::kT;
   extern __shared__ uint8_t smem_raw[];
@@ -378,15 +407,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // Query rows, pre-multiplied by scale * log2(e): scores come out in base 2.
-    using VT = typename Vec<VE>::T;
+    using VT = typename Vec<VE, F8>::T;
+    float qscale = a.scale_log2;
+    if constexpr (F8) qscale *= a.dq[a.desc_per_tensor ? 0 : h] * a.dk[a.desc_per_tensor ? 0 : hk];
     float qf[MQ][VE];
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
       if (m < nq) {
-        const VT x = *reinterpret_cast<const VT*>(a.q + bc * a.sq_b + (qrow0 + m) * a.sq_m + h * a.sq_h + lane * VE);
-        Vec<VE>::to_float(x, qf[m]);
+        const long long el = bc * a.sq_b + (qrow0 + m) * a.sq_m + h * a.sq_h + lane * VE;
+        const VT x = *reinterpret_cast<const VT*>(a.q + el * L::kEsz);
+        Vec<VE, F8>::to_float(x, qf[m]);
 #pragma unroll
-        for (int e = 0; e < VE; ++e) qf[m][e] *= a.scale_log2;
+        for (int e = 0; e < VE; ++e) qf[m][e] *= qscale;
       } else {
 #pragma unroll
         for (int e = 0; e < VE; ++e) qf[m][e] = 0.f;
@@ -399,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      wait_bounded(sbase + L::kFullOff + 8 * s, (i / kStages) & 1, abort_flag, a));
       if (!ok) break;
       const uint8_t* sK = smem + s * L::kStageBytes;
-      fold_tile<D, MQ>(nq, lo, hi, qf, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
+      fold_tile<D, MQ, F8>(nq, lo, hi, qf, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
       __syncwarp();
       if (lane == 0) mbar_arrive(sbase + L::kEmptyOff + 8 * s);
     }
@@ -476,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           o[e] = fmaf(c, x, o[e]);
         }
       }
-      const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
+      float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
+      if constexpr (F8) inv *= a.dv[a.desc_per_tensor ? 0 : hk];
       if (a.out_fp32) {
         float* op = static_cast<float*>(a.out) + bc * a.so_b + (qrow0 + m) * a.so_m + h * a.so_h + lane * VE;
 #pragma unroll
@@ -496,12 +529,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.cs > 1) cluster_sync();
 }
 
+template <int D, int MQ>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const DecArgs a) {
+  decode_body<D, MQ, false>(tm_k, tm_v, a);
+}
+
+// E4M3 q, k, v with per-head or tensorwise descales.
+template <int D, int MQ>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                           const DecArgs a) {
+  decode_body<D, MQ, true>(tm_k, tm_v, a);
+}
+
 // B: grid rows (batches, or packed sequences in sequence mode); rows_q / rows_k: the
 // longest query and key range of one grid row.
-template <int D, int MQ>
+template <int D, int MQ, bool F8>
 cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, int B, int H,
                       int rows_q, int rows_k, cudaStream_t stream) {
-  using L = DecLayout<D>;
+  using L = DecLayout<D, F8>;
+  constexpr auto kernel = F8 ? fmha_decode_fp8_kernel<D, MQ> : fmha_decode_kernel<D, MQ>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory");
   static_assert(2 * kWarps * MQ * 4 + kWarps * MQ * D * 4 + 2 * MQ * 4 + MQ * D * 4 <= L::kRingBytes,
                 "merge arrays must fit in the ring");
@@ -517,10 +566,10 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, i
   static std::atomic<int> resident[kMaxDevices][kSizes];
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!opted_in[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fmha_decode_kernel<D, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kAlloc);
     if (e != cudaSuccess) return e;
-    const bool big_ok = cudaFuncSetAttribute(fmha_decode_kernel<D, MQ>,
+    const bool big_ok = cudaFuncSetAttribute(kernel,
                                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
     for (int si = 0; si < kSizes; ++si) {
       const int c = si + 1;
@@ -537,7 +586,7 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, i
         qa[0].val.clusterDim.z = 1;
         q.attrs = qa;
         q.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, fmha_decode_kernel<D, MQ>, &q) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess) n = 0;
       }
       resident[dev][si].store(n, std::memory_order_relaxed);
     }
@@ -580,16 +629,16 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, i
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fmha_decode_kernel<D, MQ>, tk, tv, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tk, tv, a);
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecArgs& a, int B, int H,
                      int rows_q, int rows_k, cudaStream_t stream) {
-  if (rows_q <= 1) return launch_dm<D, 1>(tk, tv, a, B, H, rows_q, rows_k, stream);
-  if (rows_q <= 2) return launch_dm<D, 2>(tk, tv, a, B, H, rows_q, rows_k, stream);
-  if (rows_q <= 4) return launch_dm<D, 4>(tk, tv, a, B, H, rows_q, rows_k, stream);
-  return launch_dm<D, 8>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  if (rows_q <= 1) return launch_dm<D, 1, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  if (rows_q <= 2) return launch_dm<D, 2, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  if (rows_q <= 4) return launch_dm<D, 4, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  return launch_dm<D, 8, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
 }
 
 
@@ -603,16 +652,21 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
     return cudaErrorNotSupported;
   }
   const int D = p.K;
-  const int T = 4096 / D;
+  const int esz = p.fp8 ? 1 : 2;
+  const int T = 8192 / (D * esz);
   const long long hk = p.kv_head_shared ? 1 : p.H;
   CUtensorMap tk, tv;
-  if (!encode_rows_plain(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, D, T) ||
-      !encode_rows_plain(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, D, T)) {
+  if (!encode_rows_plain(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, D, T, p.fp8) ||
+      !encode_rows_plain(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, D, T, p.fp8)) {
     *why = "cuTensorMapEncodeTiled rejected a k/v layout";
     return cudaErrorInvalidValue;
   }
   DecArgs a{};
-  a.q = static_cast<const __nv_bfloat16*>(p.q);
+  a.q = static_cast<const uint8_t*>(p.q);
+  a.dq = p.descale_q;
+  a.dk = p.descale_k;
+  a.dv = p.descale_v;
+  a.desc_per_tensor = p.descale_per_tensor ? 1 : 0;
   a.sq_b = p.sq.b;
   a.sq_m = p.sq.m;
   a.sq_h = p.sq.h;
@@ -650,8 +704,12 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   }
   if (grid_rows == 0 || rows_q == 0) return cudaSuccess;
   *why = "decode kernel launch failed";
-  if (D == 128) return launch_d<128>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
-  return launch_d<64>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
+  if (p.fp8) {
+    if (D == 128) return launch_d<128, true>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
+    return launch_d<64, true>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
+  }
+  if (D == 128) return launch_d<128, false>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
+  return launch_d<64, false>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
 }
 
 }  // namespace mslk

@@ -71,11 +71,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest un-rescaled p (256)
 
-template <int D>
+// F8: q, k, v are E4M3 bytes; a 128-wide row is then one 128-byte swizzle atom.
+template <int D, bool F8>
 struct Layout {
-  static constexpr int kKBlocks = D / 64;
-  static constexpr int kTileBytes = kBlockM * D * 2;  // Q, K or V tile (128 rows)
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kEsz = F8 ? 1 : 2;             // bytes per input element
+  static constexpr int kKBlocks = D * kEsz / 128;     // 128-byte swizzle atoms per row
+  static constexpr int kTileBytes = kBlockM * D * kEsz;  // Q, K or V tile (128 rows)
+  static constexpr int kStages = kTileBytes == 32768 ? 4 : 8;  // a 128 KiB K/V ring
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
   // Output staging: one 16 KiB buffer per softmax warpgroup (128 rows x 128 bytes, the
@@ -118,6 +120,12 @@ struct TcArgs {
   long long so_b, so_m, so_h;
   float* lse;
   int tma_store;    // 1: write output tiles through shared memory with TMA stores
+  // E4M3 inputs: element x of head h stands for x * descale[h] (descale[0] when
+  // desc_per_tensor); q and k descales fold into the score scale, v's into the output.
+  const float* dq;
+  const float* dk;
+  const float* dv;
+  int desc_per_tensor;
   unsigned int* err;
   unsigned long long timeout_ns;
 };
@@ -167,25 +175,41 @@ __host__ __device__ constexpr uint32_t kmajor_step(int kk) {
   return static_cast<uint32_t>(((kk / 4) * kSwizzleAtom + (kk % 4) * 32) >> 4);
 }
 
-// S_t = Q_t K^T over the head dim, 16 columns per MMA.
-template <int D>
+// S_t = Q_t K^T over the head dim, 32 bytes of it per MMA (16 bf16 or 32 E4M3 columns).
+template <int D, bool F8>
 MSLK_DEV void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, false);
+  if constexpr (F8) {
+    constexpr uint32_t idesc = idesc_e4m3_f32(kBlockM, kBlockN, false);
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
-    mma_f16_ss_elect(d_tmem, q_desc + kmajor_step(kk), k_desc + kmajor_step(kk), idesc, kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < D / 32; ++kk)
+      mma_f8_ss_elect(d_tmem, q_desc + kmajor_step(kk), k_desc + kmajor_step(kk), idesc, kk > 0 ? 1u : 0u);
+  } else {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, false);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_f16_ss_elect(d_tmem, q_desc + kmajor_step(kk), k_desc + kmajor_step(kk), idesc, kk > 0 ? 1u : 0u);
+  }
 }
 
-// O_t (+)= P_t V over the 128 keys of the tile, 16 keys per MMA.  P_t is read from tensor
-// memory (16 bf16 keys = 8 columns per MMA); V is read MN-major: 8-key groups 1024 bytes
-// apart (SBO), 64-column halves of the head dim 16 KiB apart (LBO); 16 keys are 2048 bytes.
-template <int D>
+// O_t (+)= P_t V over the 128 keys of the tile.  P_t is read from tensor memory, 8 columns
+// per MMA (16 bf16 keys, or 32 E4M3 keys); V is read MN-major: 8-key groups 1024 bytes
+// apart (SBO), 128-byte column blocks of the head dim 16 KiB apart (LBO; bf16 has two);
+// one MMA's keys span 2048 (bf16) or 4096 (E4M3) bytes.
+template <int D, bool F8>
 MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, D, true);
+  if constexpr (F8) {
+    constexpr uint32_t idesc = idesc_e4m3_f32(kBlockM, D, true);
 #pragma unroll
-  for (int kk = 0; kk < kBlockN / 16; ++kk)
-    mma_f16_ts_elect(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint32_t>(kk * 2048 / 16),
-                     idesc, kk > 0 ? 1u : accumulate);
+    for (int kk = 0; kk < kBlockN / 32; ++kk)
+      mma_f8_ts_elect(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint32_t>(kk * 4096 / 16),
+                      idesc, kk > 0 ? 1u : accumulate);
+  } else {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, D, true);
+#pragma unroll
+    for (int kk = 0; kk < kBlockN / 16; ++kk)
+      mma_f16_ts_elect(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint32_t>(kk * 2048 / 16),
+                       idesc, kk > 0 ? 1u : accumulate);
+  }
 }
 
 // One work unit: 256 query rows of one (batch or packed sequence, head).
@@ -200,7 +224,6 @@ struct Unit {
   int tlo[2], thi[2];
   int jlo, jhi;
   MSLK_DEV bool has(int t) const { return tlo[t] < thi[t]; }
-  MSLK_DEV bool act(int t, int j) const { return tlo[t] <= j && j < thi[t]; }
 };
 
 // Unit i of the heavy-first order: unit rows descend level by level (causal units late in
@@ -286,12 +309,11 @@ MSLK_DEV int unit_at(int round, int c, int G) {
 
 // kLowerEdge: the band has a lower edge (a local window), so masked tiles test both
 // edges; without it the per-row lower limit is compiled out of the softmax.
-template <int D, bool kLowerEdge>
-__global__ void __launch_bounds__(kThreads, 1)
-    fmha_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                   const TcArgs a) {
-  using L = Layout<D>;
+// F8: E4M3 q, k, v (kind::f8f6f4 MMAs; P is rounded to E4M3 for the PV MMA).
+template <int D, bool kLowerEdge, bool F8>
+MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                      const CUtensorMap& tm_o, const TcArgs& a) {
+  using L = Layout<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -368,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wait_bar_warp(q_empty(t), (uc & 1) ^ 1, wc))) return;
       mbar_arrive_expect_tx_elect(q_full(t), L::kTileBytes);
       for (int kb = 0; kb < L::kKBlocks; ++kb)
-        tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, q_full(t), kb * 64,
+        tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, q_full(t), kb * (128 / L::kEsz),
                           u.q_base + u.r0 + t * kBlockM, u.h, u.b);
       ++q_issued[t];
     };
@@ -384,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               key % a.page_size;
       }
       for (int kb = 0; kb < L::kKBlocks; ++kb)
-        tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * 64, row, u.hk, u.b);
+        tma_load_4d_elect(kv_addr(s) + kb * kSwizzleAtom, tm, kv_full(s), kb * (128 / L::kEsz), row, u.hk, u.b);
       ++it;
     };
     for (int k = 0; k < n_rounds && ok; ++k) {
@@ -452,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_bar_warp(kv_full(sk0), (ik0 / L::kStages) & 1, wc))) break;
         tc_fence_after();
         if ((lo0 <= jlo && jlo < hi0)) {
-          issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk0));
+          issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(sk0));
           mma_commit_elect(s_full(0));
         }
         if (lo0 >= hi0 || hi0 == jlo + 1) mma_commit_elect(q_empty(0));  // Q0's last S issued
@@ -462,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wait_bar_warp(kv_full(sk0), (ik0 / L::kStages) & 1, wc))) break;
       tc_fence_after();
       if ((lo1 <= jlo && jlo < hi1)) {
-        issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk0));
+        issue_qk<D, F8>(tm_s[1], q_desc[1], kv_kdesc(sk0));
         mma_commit_elect(s_full(1));
       }
       mma_commit_elect(kv_empty(sk0));
@@ -492,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
           if (j == lo0 && !(ok = wait_bar_warp(o_free(0), (uc0 & 1) ^ 1, wc))) break;
           tc_fence_after();
-          issue_pv<D>(tm_o[0], tm_s[0], kv_vdesc(sv), j > lo0 ? 1u : 0u);
+          issue_pv<D, F8>(tm_o[0], tm_s[0], kv_vdesc(sv), j > lo0 ? 1u : 0u);
           if (j == hi0 - 1) mma_commit_elect(o_done(0));
           ++jg0;
         }
@@ -500,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar_warp(kv_full(sk), (ik / L::kStages) & 1, wc))) break;
           tc_fence_after();
           if ((lo0 <= j + 1 && j + 1 < hi0)) {
-            issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(sk));
+            issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(sk));
             mma_commit_elect(s_full(0));
             if (j + 2 == hi0) mma_commit_elect(q_empty(0));
           }
@@ -510,14 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar_warp(p_full(1), jg1 & 1, wc))) break;
           if (j == lo1 && !(ok = wait_bar_warp(o_free(1), (uc1 & 1) ^ 1, wc))) break;
           tc_fence_after();
-          issue_pv<D>(tm_o[1], tm_s[1], kv_vdesc(sv), j > lo1 ? 1u : 0u);
+          issue_pv<D, F8>(tm_o[1], tm_s[1], kv_vdesc(sv), j > lo1 ? 1u : 0u);
           if (j == hi1 - 1) mma_commit_elect(o_done(1));
           ++jg1;
         }
         mma_commit_elect(kv_empty(sv));
         if (more) {
           if ((lo1 <= j + 1 && j + 1 < hi1)) {
-            issue_qk<D>(tm_s[1], q_desc[1], kv_kdesc(sk));
+            issue_qk<D, F8>(tm_s[1], q_desc[1], kv_kdesc(sk));
             mma_commit_elect(s_full(1));
             if (j + 2 == hi1) mma_commit_elect(q_empty(1));  // the unit's last S1 MMA was issued
           }
@@ -530,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar_warp(q_full(0), (uc + 1) & 1, wc))) break;
           if (!(ok = wait_bar_warp(kv_full(ikn % L::kStages), (ikn / L::kStages) & 1, wc))) break;
           tc_fence_after();
-          issue_qk<D>(tm_s[0], q_desc[0], kv_kdesc(ikn % L::kStages));
+          issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(ikn % L::kStages));
           mma_commit_elect(s_full(0));
           if (un.thi[0] == un.jlo + 1) mma_commit_elect(q_empty(0));
           s0_issued = true;
@@ -555,7 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_bits = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t ts = tmem + static_cast<uint32_t>(t * 128) + lane_bits;
     const uint32_t to = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_bits;
-    const float sl2 = a.scale_log2;
     int uc = 0, jg = 0;
     bool ok = true;
     for (int k = 0; k < n_rounds && ok; ++k) {
@@ -569,6 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this Q tile's key tiles (selects, not a runtime index, keep u in registers)
       const int tlo_t = t == 0 ? u.tlo[0] : u.tlo[1];
       const int n_t = (t == 0 ? u.thi[0] : u.thi[1]) - tlo_t;
+      float sl2 = a.scale_log2;
+      if constexpr (F8) sl2 *= a.dq[a.desc_per_tensor ? 0 : u.h] * a.dk[a.desc_per_tensor ? 0 : u.hk];
       if (n_t <= 0) {  // no allowed key for any row of this Q tile
         if (valid) {
           for (int c = 0; c < D; c += 4) {
@@ -647,17 +670,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // 8 independent partial sums, in pairs
 #pragma unroll
         for (int qtr = 0; qtr < 4; ++qtr) {
-          uint32_t pk[16];
+          if constexpr (F8) {
+            // P as E4M3, four per column, over S's first 32 columns.  p <= 2^8 (the lazy
+            // rescale bound) stays inside E4M3's range (448).
+            uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = qtr * 32 + 2 * e;
-            const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
-            const float p0 = ex2_approx(x.x);
-            const float p1 = ex2_approx(x.y);
-            rs2[e % 4] = fadd2(rs2[e % 4], pack_f2(p0, p1));
-            pk[e] = pack_bf16x2(p0, p1);
+            for (int e = 0; e < 8; ++e) {
+              const int c = qtr * 32 + 4 * e;
+              const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
+              const float2 y = unpack_f2(ffma2(pack_f2(u2f(sr[c + 2]), u2f(sr[c + 3])), sl2x2, nmx2));
+              const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+              const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
+              rs2[(2 * e) % 4] = fadd2(rs2[(2 * e) % 4], pack_f2(p0, p1));
+              rs2[(2 * e + 1) % 4] = fadd2(rs2[(2 * e + 1) % 4], pack_f2(p2, p3));
+              pk[e] = pack_e4m3x4(p0, p1, p2, p3);
+            }
+            tmem_st_32x32b_x8(ts + qtr * 8, pk);
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c = qtr * 32 + 2 * e;
+              const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
+              const float p0 = ex2_approx(x.x);
+              const float p1 = ex2_approx(x.y);
+              rs2[e % 4] = fadd2(rs2[e % 4], pack_f2(p0, p1));
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st_32x32b_x16(ts + qtr * 16, pk);
           }
-          tmem_st_32x32b_x16(ts + qtr * 16, pk);
         }
         {
           const float2 r0 = unpack_f2(fadd2(rs2[0], rs2[1]));
@@ -688,7 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
-      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      if constexpr (F8) inv_l *= a.dv[a.desc_per_tensor ? 0 : u.hk];
       // Output tiles go through this warpgroup's staging buffer and one TMA store per
       // 128-byte column band, except the tail tile of a packed sequence (a whole 128-row
       // box would spill into the next sequence), which is stored row by row.
@@ -791,6 +833,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int D, bool kLowerEdge>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const TcArgs a) {
+  tc_body<D, kLowerEdge, false>(tm_q, tm_k, tm_v, tm_o, a);
+}
+
+// E4M3 q, k, v (head dim 128), bf16 or fp32 output.
+template <bool kLowerEdge>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_tc_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       const TcArgs a) {
+  tc_body<128, kLowerEdge, true>(tm_q, tm_k, tm_v, tm_o, a);
+}
 
 // ------------------------------------------------------------------ host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -812,12 +870,13 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [batch, rows, heads, D] bf16 tensor with free strides (elements) -> 4-D tiled map with a
-// 64 x 128 box (one 128-byte swizzle atom per row).  Dimensions of extent 1 get a dummy
-// stride (never stepped over).
+// [batch, rows, heads, D] bf16 (or, with u8, E4M3 bytes) tensor with free strides
+// (elements) -> 4-D tiled map with a 128-byte x 128-row box (one 128-byte swizzle atom per
+// row).  Dimensions of extent 1 get a dummy stride (never stepped over).
 bool encode_bhmd(EncodeTiledFn enc, CUtensorMap* map, const void* base, int D, long long rows,
-                 long long heads, long long batch, long long s_m, long long s_h, long long s_b) {
-  const long long elt = 2;
+                 long long heads, long long batch, long long s_m, long long s_h, long long s_b,
+                 bool u8) {
+  const long long elt = u8 ? 1 : 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
   long long st_m = s_m * elt;
@@ -828,9 +887,10 @@ bool encode_bhmd(EncodeTiledFn enc, CUtensorMap* map, const void* base, int D, l
   if (st_b <= 0 || st_b % 16) st_b = 16;
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(st_m), static_cast<cuuint64_t>(st_h),
                            static_cast<cuuint64_t>(st_b)};
-  cuuint32_t box[4] = {64, kBlockM, 1, 1};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), kBlockM, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+  return enc(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+             const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -870,10 +930,10 @@ bool encode_out(EncodeTiledFn enc, CUtensorMap* map, void* base, bool fp32, int 
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
                      const char** why) {
-  using Lt = Layout<D>;
+  using Lt = Layout<D, F8>;
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) {
     *why = "cuTensorMapEncodeTiled is not available from the driver";
@@ -881,9 +941,9 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   }
   const long long hk = p.kv_head_shared ? 1 : p.H;
   CUtensorMap tq, tk, tv;
-  if (!encode_bhmd(enc, &tq, p.q, D, p.M, p.H, p.B, p.sq.m, p.sq.h, p.sq.b) ||
-      !encode_bhmd(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b) ||
-      !encode_bhmd(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b)) {
+  if (!encode_bhmd(enc, &tq, p.q, D, p.M, p.H, p.B, p.sq.m, p.sq.h, p.sq.b, F8) ||
+      !encode_bhmd(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, F8) ||
+      !encode_bhmd(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, F8)) {
     *why = "cuTensorMapEncodeTiled rejected a q/k/v layout";
     return cudaErrorInvalidValue;
   }
@@ -917,6 +977,10 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.so_h = p.so.h;
   a.lse = p.lse;
   a.tma_store = tma_store ? 1 : 0;
+  a.dq = p.descale_q;
+  a.dk = p.descale_k;
+  a.dv = p.descale_v;
+  a.desc_per_tensor = p.descale_per_tensor ? 1 : 0;
   a.err = ctl.err;
   a.timeout_ns = ctl.timeout_ns;
   a.Z = a.varlen ? p.n_seqs : p.B;
@@ -930,6 +994,7 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   // Persistent: one CTA per SM (or fewer when there are fewer units).
   const dim3 grid(static_cast<unsigned>(std::min<long long>(total, num_sms())));
   auto kernel = a.lo > -kBandOpen ? fmha_tc_kernel<D, true> : fmha_tc_kernel<D, false>;
+  if constexpr (F8) kernel = a.lo > -kBandOpen ? fmha_tc_fp8_kernel<true> : fmha_tc_fp8_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lt::kAlloc);
   if (e != cudaSuccess) {
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -953,8 +1018,13 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
 
 cudaError_t launch_fmha_tc(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
                            const char** why) {
-  if (p.K == 128) return launch_d<128>(p, ctl, stream, why);
-  if (p.K == 64) return launch_d<64>(p, ctl, stream, why);
+  if (p.fp8) {
+    if (p.K == 128) return launch_d<128, true>(p, ctl, stream, why);
+    *why = "E4M3 inputs on the tensor-core path need head dim 128";
+    return cudaErrorInvalidValue;
+  }
+  if (p.K == 128) return launch_d<128, false>(p, ctl, stream, why);
+  if (p.K == 64) return launch_d<64, false>(p, ctl, stream, why);
   *why = "head dim must be 64 or 128";
   return cudaErrorInvalidValue;
 }

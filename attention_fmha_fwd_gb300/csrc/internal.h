@@ -34,6 +34,13 @@ struct AttnProblem {
   const int32_t* lane_start;
   const int32_t* block_table;
   int page_size, max_pages;
+  // E4M3 q/k/v: element x of head h stands for x * descale[h] (descale[0] when
+  // descale_per_tensor); device fp32 arrays.
+  bool fp8;
+  const float* descale_q;
+  const float* descale_k;
+  const float* descale_v;
+  bool descale_per_tensor;
   void* out;
   bool out_fp32;
   float* lse;           // may be null (forward without lse)

@@ -81,7 +81,7 @@ mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const vo
                           int32_t K, int32_t Kv, float scale, int32_t mask_kind,
                           const mslk_seqlens* seqlens, const mslk_band* band, int64_t kv_offset,
                           void* out, int32_t out_dtype, float* lse, bool lse_required,
-                          bool partial, const char* who) {
+                          bool partial, const char* who, int in_bytes = 2) {
   if (B < 0 || M < 0 || Mkv < 0 || H < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative size", who);
   if (mask_kind < MSLK_MASK_NONE || mask_kind > MSLK_MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT)
     return fail(MSLK_ERR_INVALID_ARG, "%s: unknown mask_kind %d", who, mask_kind);
@@ -163,12 +163,13 @@ mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const vo
   p.kv_head_shared = H > 1 && sk->h == 0;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v))
     return fail(MSLK_ERR_MISALIGNED, "%s: q/k/v base must be 16-byte aligned", who);
-  if (const char* w = check_strides(*sq, B, M, H, 8, false))
-    return fail(MSLK_ERR_MISALIGNED, "%s: q %s must be a positive multiple of 8 elements (16 bytes)", who, w);
-  if (const char* w = check_strides(*sk, B, Mkv, H, 8, true))
-    return fail(MSLK_ERR_MISALIGNED, "%s: k %s must be a positive multiple of 8 elements (16 bytes)", who, w);
-  if (const char* w = check_strides(*sv, B, Mkv, H, 8, true))
-    return fail(MSLK_ERR_MISALIGNED, "%s: v %s must be a positive multiple of 8 elements (16 bytes)", who, w);
+  const int in_mult = 16 / in_bytes;  // elements per 16 bytes
+  if (const char* w = check_strides(*sq, B, M, H, in_mult, false))
+    return fail(MSLK_ERR_MISALIGNED, "%s: q %s must be a positive multiple of %d elements (16 bytes)", who, w, in_mult);
+  if (const char* w = check_strides(*sk, B, Mkv, H, in_mult, true))
+    return fail(MSLK_ERR_MISALIGNED, "%s: k %s must be a positive multiple of %d elements (16 bytes)", who, w, in_mult);
+  if (const char* w = check_strides(*sv, B, Mkv, H, in_mult, true))
+    return fail(MSLK_ERR_MISALIGNED, "%s: v %s must be a positive multiple of %d elements (16 bytes)", who, w, in_mult);
   if (!aligned16(out)) return fail(MSLK_ERR_MISALIGNED, "%s: out base must be 16-byte aligned", who);
   if (const char* w = check_strides(*so, B, M, H, p.out_fp32 ? 4 : 8, false))
     return fail(MSLK_ERR_MISALIGNED, "%s: out %s must be a positive multiple of 16 bytes", who, w);
@@ -247,6 +248,55 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
 
 using namespace mslk;
 
+namespace {
+
+// The key-lane descriptor on its own (before the problem is validated).
+mslk_status check_lanes(const mslk_kv_lanes* lanes, int32_t mask_kind, const char* who) {
+  if (!is_blockdiag(mask_kind))
+    return fail(MSLK_ERR_INVALID_ARG, "%s: key lanes need a block-diagonal mask kind (got %d)", who, mask_kind);
+  if (lanes == nullptr || lanes->seqlen_k == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: lanes->seqlen_k is required", who);
+  if (lanes->block_table != nullptr) {
+    if (lanes->page_size <= 0 || lanes->max_pages <= 0)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: paged lanes need page_size > 0 and max_pages > 0", who);
+  } else if (lanes->seqstart_k == nullptr) {
+    return fail(MSLK_ERR_INVALID_ARG, "%s: lanes need seqstart_k or block_table", who);
+  }
+  return ok();
+}
+
+// cu_seqlens_k is not read for lanes: validation only needs a non-null pointer there.
+mslk_seqlens lanes_seqlens(const mslk_seqlens* seqlens, const mslk_kv_lanes* lanes) {
+  mslk_seqlens sl{};
+  if (seqlens != nullptr) {
+    sl = *seqlens;
+    if (sl.cu_seqlens_k == nullptr) sl.cu_seqlens_k = lanes->seqlen_k;
+  }
+  return sl;
+}
+
+// Lanes on a validated problem: a key tile never straddles a page (the decode kernel's
+// tiles hold 8192 / (K * element bytes) keys, the tensor-core kernel's 128).
+mslk_status apply_lanes(AttnProblem& p, const mslk_kv_lanes* lanes, const char* who) {
+  if (lanes->block_table != nullptr) {
+    const bool decode = p.max_seqlen_q <= kDecodeMaxRows && g_path_policy.load() != 1;
+    const int multiple = decode ? (p.fp8 ? 8192 / p.K : 64) : 128;
+    if (lanes->page_size % multiple)
+      return fail(MSLK_ERR_UNSUPPORTED, "%s: page_size %d must be a multiple of %d", who,
+                  lanes->page_size, multiple);
+  }
+  p.lanes = true;
+  p.lane_len = lanes->seqlen_k;
+  p.lane_start = lanes->seqstart_k;
+  p.block_table = lanes->block_table;
+  p.page_size = lanes->page_size;
+  p.max_pages = lanes->max_pages;
+  p.cu_k = nullptr;
+  return ok();
+}
+
+}  // namespace
+
 extern "C" {
 
 mslk_status mslk_attn_fwd(const void* q, const void* k, const void* v, const mslk_strides* sq,
@@ -311,43 +361,62 @@ mslk_status mslk_attn_fwd_lanes(const void* q, const void* k, const void* v, con
                                 const mslk_kv_lanes* lanes, const mslk_band* band, void* out,
                                 float* lse, void* stream) {
   const char* who = "mslk_attn_fwd_lanes";
-  if (!is_blockdiag(mask_kind))
-    return fail(MSLK_ERR_INVALID_ARG, "%s: key lanes need a block-diagonal mask kind (got %d)", who, mask_kind);
-  if (lanes == nullptr || lanes->seqlen_k == nullptr)
-    return fail(MSLK_ERR_INVALID_ARG, "%s: lanes->seqlen_k is required", who);
-  if (lanes->block_table != nullptr) {
-    if (lanes->page_size <= 0 || lanes->max_pages <= 0)
-      return fail(MSLK_ERR_INVALID_ARG, "%s: paged lanes need page_size > 0 and max_pages > 0", who);
-  } else if (lanes->seqstart_k == nullptr) {
-    return fail(MSLK_ERR_INVALID_ARG, "%s: lanes need seqstart_k or block_table", who);
-  }
-  // cu_seqlens_k is not read for lanes: validation only needs a non-null pointer there.
+  mslk_status s = check_lanes(lanes, mask_kind, who);
+  if (s != MSLK_OK) return s;
+  const mslk_seqlens sl = lanes_seqlens(seqlens, lanes);
+  AttnProblem p;
+  s = validate_attn(p, q, k, v, sq, sk, sv, so, 1, M, Mkv, H, K, Kv, scale, mask_kind,
+                    seqlens ? &sl : nullptr, band, 0, out, MSLK_DTYPE_BF16, lse, false, false, who);
+  if (s != MSLK_OK) return s;
+  s = apply_lanes(p, lanes, who);
+  if (s != MSLK_OK) return s;
+  return run_attn(p, static_cast<cudaStream_t>(stream), who);
+}
+
+mslk_status mslk_attn_fwd_fp8(const void* q, const void* k, const void* v, const mslk_strides* sq,
+                              const mslk_strides* sk, const mslk_strides* sv, const mslk_strides* so,
+                              int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv,
+                              float scale, int32_t mask_kind, const mslk_seqlens* seqlens,
+                              const mslk_band* band, const mslk_kv_lanes* lanes,
+                              const mslk_fp8_scales* scales, void* out, float* lse, void* stream) {
+  const char* who = "mslk_attn_fwd_fp8";
+  if (scales == nullptr || scales->descale_q == nullptr || scales->descale_k == nullptr ||
+      scales->descale_v == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: descale_q, descale_k and descale_v are required", who);
+  if (scales->per_tensor != 0 && scales->per_tensor != 1)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: scales.per_tensor must be 0 or 1", who);
+  if ((reinterpret_cast<uintptr_t>(scales->descale_q) | reinterpret_cast<uintptr_t>(scales->descale_k) |
+       reinterpret_cast<uintptr_t>(scales->descale_v)) & 3u)
+    return fail(MSLK_ERR_MISALIGNED, "%s: descales must be 4-byte aligned", who);
+  mslk_status s = ok();
   mslk_seqlens sl{};
-  if (seqlens != nullptr) {
+  if (lanes != nullptr) {
+    s = check_lanes(lanes, mask_kind, who);
+    if (s != MSLK_OK) return s;
+    if (B != 1) return fail(MSLK_ERR_INVALID_ARG, "%s: key lanes take packed queries (B = 1), got B = %d", who, B);
+    sl = lanes_seqlens(seqlens, lanes);
+  } else if (seqlens != nullptr) {
     sl = *seqlens;
-    if (sl.cu_seqlens_k == nullptr) sl.cu_seqlens_k = lanes->seqlen_k;
   }
   AttnProblem p;
-  const mslk_status s = validate_attn(p, q, k, v, sq, sk, sv, so, 1, M, Mkv, H, K, Kv, scale,
-                                      mask_kind, seqlens ? &sl : nullptr, band, 0, out,
-                                      MSLK_DTYPE_BF16, lse, false, false, who);
+  s = validate_attn(p, q, k, v, sq, sk, sv, so, B, M, Mkv, H, K, Kv, scale, mask_kind,
+                    seqlens ? &sl : nullptr, band, 0, out, MSLK_DTYPE_BF16, lse, false, false, who, 1);
   if (s != MSLK_OK) return s;
-  if (lanes->block_table != nullptr) {
-    // A key tile never straddles a page: 64-key tiles (decode kernel, D = 64; 32 for D =
-    // 128), 128-key tiles (tensor-core kernel).
-    const bool decode = p.max_seqlen_q <= kDecodeMaxRows && g_path_policy.load() != 1;
-    const int multiple = decode ? 64 : 128;
-    if (lanes->page_size % multiple)
-      return fail(MSLK_ERR_UNSUPPORTED, "%s: page_size %d must be a multiple of %d", who,
-                  lanes->page_size, multiple);
+  p.fp8 = true;
+  p.descale_q = scales->descale_q;
+  p.descale_k = scales->descale_k;
+  p.descale_v = scales->descale_v;
+  p.descale_per_tensor = scales->per_tensor == 1;
+  if (lanes != nullptr) {
+    s = apply_lanes(p, lanes, who);
+    if (s != MSLK_OK) return s;
   }
-  p.lanes = true;
-  p.lane_len = lanes->seqlen_k;
-  p.lane_start = lanes->seqstart_k;
-  p.block_table = lanes->block_table;
-  p.page_size = lanes->page_size;
-  p.max_pages = lanes->max_pages;
-  p.cu_k = nullptr;
+  const int rows = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
+  const bool decode = rows <= kDecodeMaxRows && g_path_policy.load() != 1;
+  if (!decode && K != 128 && p.B > 0 && p.H > 0 && p.M > 0)
+    return fail(MSLK_ERR_UNSUPPORTED,
+                "%s: E4M3 inputs with more than %d query rows need head dim 128 (got %d)", who,
+                kDecodeMaxRows, K);
   return run_attn(p, static_cast<cudaStream_t>(stream), who);
 }
 

@@ -29,13 +29,13 @@ inline EncodeTiledFn tensor_map_encoder() {
   return fn;
 }
 
-// bf16 [batch, rows, heads, D] with free strides (elements) -> 4-D tiled map with a
-// box_d x box_rows box and no swizzle (rows land densely in shared memory, D elements
-// each).  Dimensions of extent 1 get a dummy stride (never stepped over).
+// bf16 (or, with u8, one-byte E4M3) [batch, rows, heads, D] with free strides (elements)
+// -> 4-D tiled map with a box_d x box_rows box and no swizzle (rows land densely in shared
+// memory, D elements each).  Dimensions of extent 1 get a dummy stride (never stepped over).
 inline bool encode_rows_plain(EncodeTiledFn enc, CUtensorMap* map, const void* base, int D,
                               long long rows, long long heads, long long batch, long long s_m,
-                              long long s_h, long long s_b, int box_d, int box_rows) {
-  const long long elt = 2;
+                              long long s_h, long long s_b, int box_d, int box_rows, bool u8 = false) {
+  const long long elt = u8 ? 1 : 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
   long long st_m = s_m * elt;
@@ -49,7 +49,8 @@ inline bool encode_rows_plain(EncodeTiledFn enc, CUtensorMap* map, const void* b
                            static_cast<cuuint64_t>(st_b)};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(box_d), static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+  return enc(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+             const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -31,6 +31,34 @@ def qkv(B: int, M: int, Mkv: int, H: int, K: int, Kv: int | None = None,
     return q, k, v
 
 
+def quantize_e4m3(x: torch.Tensor, head_axis: int = 2, per_head: bool = True):
+    """E4M3 codes (uint8) and fp32 descales for a float tensor: descale = amax / 448 per
+    head (or over the whole tensor), codes = x / descale rounded by PyTorch's own
+    float8_e4m3fn conversion (round to nearest even).  Input generation only."""
+    xf = x.float()
+    if per_head:
+        dims = [d for d in range(xf.dim()) if d != head_axis]
+        amax = xf.abs().amax(dim=dims)
+    else:
+        amax = xf.abs().amax().reshape(1)
+    descale = (amax.clamp_min(1e-12) / 448.0).float()
+    shape = [1] * xf.dim()
+    if per_head:
+        shape[head_axis] = -1
+    codes = (xf / descale.reshape(shape)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, descale
+
+
+def qkv_fp8(B: int, M: int, Mkv: int, H: int, K: int, Hkv: int | None = None, seed: int = 0,
+            per_head: bool = True):
+    """E4M3 q, k, v (uint8 codes, CPU) and their descales: ``qkv``'s bf16 draws quantized."""
+    q, k, v = qkv(B, M, Mkv, H, K, Hkv=Hkv, seed=seed)
+    out = []
+    for t in (q, k, v):
+        out.extend(quantize_e4m3(t, per_head=per_head))
+    return tuple(out)  # q8, dq, k8, dk, v8, dv
+
+
 def varlen_seqlens(n_seqs: int = 12, total: int = 16384, lo: int = 128, hi: int = 4096,
                    seed: int = 0) -> list[int]:
     """Sequence lengths for a packed batch: ``n_seqs`` integers uniform in [lo, hi],

@@ -560,6 +560,21 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
                                             "frac_hbm": b_pg / t_pg / 1e9 / peaks["hbm_gbs"],
                                             "launches": 1}
     del kp, vp
+    # the same decode step with an E4M3 cache (per-head descales): half the bytes
+    k8, dk8 = inputs.quantize_e4m3(kd)
+    v8, dv8 = inputs.quantize_e4m3(vd)
+    q8, dq8 = inputs.quantize_e4m3(qd)
+    dk8, dv8, dq8 = dk8.to(dev), dv8.to(dev), dq8.to(dev)
+    o8 = torch.empty((w.B, w.M, w.H, w.Kv), dtype=torch.bfloat16, device=dev)
+    fp8_dec = lambda: fa.attn_fwd_fp8(q8, k8, v8, dq8, dk8, dv8, scale=w.scale, out=o8, lse=fl)  # noqa: E731
+    for _ in range(3):
+        fp8_dec()
+    t_f8 = _time_it(fp8_dec, 10, stream, flush)
+    b_f8 = k8.numel() + v8.numel()
+    res["fp8_decode_single_launch_16x32768"] = {"us": t_f8 * 1e6, "GB/s": b_f8 / t_f8 / 1e9,
+                                                "frac_hbm": b_f8 / t_f8 / 1e9 / peaks["hbm_gbs"],
+                                                "speedup_vs_bf16": t_one / t_f8, "launches": 1}
+    del k8, v8
     del kd, vd, k, v
     # varlen packed block-diagonal causal
     w = inputs.WORKLOADS["varlen_packed"]
@@ -633,6 +648,26 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
                 "frac_bf16": bflops / t_p / 1e12 / peaks["bf16_tflops"]}
             del kp, vp
         del qd, kd, vd
+    # E4M3 q/k/v on the tensor cores: the causal 2 x 2048 x 32 x 128 workload, per-head
+    # descales; peak = measured bf16 x 2 (the nominal E4M3 : bf16 dense ratio, 4.5 : 2.25)
+    w = inputs.WORKLOADS["causal_fwd"]
+    q, k, v = inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0)
+    q8, dq8 = inputs.quantize_e4m3(q.to(dev))
+    k8, dk8 = inputs.quantize_e4m3(k.to(dev))
+    v8, dv8 = inputs.quantize_e4m3(v.to(dev))
+    fo = torch.empty((w.B, w.M, w.H, w.Kv), dtype=torch.bfloat16, device=dev)
+    fl = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=dev)
+
+    def f8step():
+        fa.attn_fwd_fp8(q8, k8, v8, dq8, dk8, dv8, mask="causal", scale=w.scale, out=fo, lse=fl)
+
+    for _ in range(3):
+        f8step()
+    t_c8 = _time_it(f8step, 20, stream, flush)
+    fl8 = fwd_flops(w)
+    res["fp8_causal_fwd_2x2048x32x128"] = {"us": t_c8 * 1e6, "TFLOP/s": fl8 / t_c8 / 1e12,
+                                           "frac_fp8": fl8 / t_c8 / 1e12 / (2 * peaks["bf16_tflops"]),
+                                           "peak": "2 x measured bf16"}
     return res
 
 

@@ -217,6 +217,42 @@ mslk_status mslk_attn_fwd_lanes(const void* q, const void* k, const void* v,
                                 float* lse, void* stream);
 
 /*
+ * FP8 E4M3 inputs ("Attention - Core fMHA": the Blackwell and FlashAttention-3 forward
+ * backends list FP8 E4M3; pack_fp8_tensorwise_per_head carries tensorwise or per-head
+ * scales; the raw flash3 op takes descale_q / descale_k / descale_v).  Element x of head
+ * h stands for the real value e4m3(x) * descale[h]; with per_tensor = 1 every head uses
+ * descale[0].  The descales are DEVICE fp32 arrays read by the kernels: descale_q [H],
+ * descale_k and descale_v [H] (or [1] when k/v use a shared head, head stride 0).
+ */
+typedef struct {
+  const float* descale_q;
+  const float* descale_k;
+  const float* descale_v;
+  int32_t per_tensor;
+} mslk_fp8_scales;
+
+/*
+ * mslk_attn_fwd_fp8 — forward on E4M3 q, k, v (one byte per element; strides in
+ * elements, multiples of 16; bases 16-byte aligned), bf16 out, fp32 lse (or NULL).
+ * Masks, windows and bottom-right alignment as mslk_attn_fwd_band (band may be NULL);
+ * key lanes as mslk_attn_fwd_lanes when `lanes` is non-NULL (then B must be 1).
+ * The result is attention on the dequantized values.  Query blocks of at most 8 rows (per
+ * packed sequence) run on the CUDA-core kernel with fp32 probabilities; larger ones on the
+ * tensor cores (kind::f8f6f4, K = Kv = 128 only, else MSLK_ERR_UNSUPPORTED), where the
+ * probabilities are rounded to E4M3 before P.V (relative error <= 2^-4 per probability;
+ * the row sum uses the unrounded values).  Paged lanes need page_size a multiple of 128
+ * (of 8192 / K when every sequence has at most 8 queries).
+ */
+mslk_status mslk_attn_fwd_fp8(const void* q, const void* k, const void* v,
+                              const mslk_strides* sq, const mslk_strides* sk,
+                              const mslk_strides* sv, const mslk_strides* so, int32_t B,
+                              int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv,
+                              float scale, int32_t mask_kind, const mslk_seqlens* seqlens,
+                              const mslk_band* band, const mslk_kv_lanes* lanes,
+                              const mslk_fp8_scales* scales, void* out, float* lse,
+                              void* stream);
+
+/*
  * mslk_merge_attentions — exact log-sum-exp merge of n chunk results into preallocated
  * outputs.  MSLK kernel reference, "Attention - Core fMHA" > merge_attentions (exact
  * normalised output over the union of chunks, not an average; write_lse; output_dtype)

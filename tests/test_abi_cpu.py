@@ -229,3 +229,50 @@ def test_lanes_pass_validation(lib):
                               (L(FAKE, None, FAKE, 256, 2), 5, _capi.Band(0, 100, -1))):
         st, why = _lanes_call(lib, lanes, mask, band)
         assert st == _capi.MSLK_ERR_CUDA, why
+
+
+def _fp8_call(lib, scales="ok", B=2, M=64, K=128, sq=None, lanes=None, mask=0, sl=None):
+    s = S(8 * 128 * 64, 8 * 128, 128) if sq is None else sq
+    so = S(8 * 128 * 64, 8 * 128, 128)
+    r = ctypes.byref
+    if scales == "ok":
+        scales = _capi.Fp8Scales(FAKE, FAKE, FAKE, 0)
+    st = lib.mslk_attn_fwd_fp8(FAKE, FAKE, FAKE, r(s), r(s), r(s), r(so), B, M, 64, 8, K, K, 0.0,
+                               mask, None if sl is None else r(sl), None,
+                               None if lanes is None else r(lanes),
+                               None if scales is None else r(scales), FAKE, FAKE, None)
+    return st, lib.mslk_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(scales=None), _capi.MSLK_ERR_INVALID_ARG, "descale"),
+    (dict(scales=_capi.Fp8Scales(FAKE, None, FAKE, 0)), _capi.MSLK_ERR_INVALID_ARG, "descale"),
+    (dict(scales=_capi.Fp8Scales(FAKE, FAKE, FAKE, 2)), _capi.MSLK_ERR_INVALID_ARG, "per_tensor"),
+    (dict(scales=_capi.Fp8Scales(FAKE, FAKE + 2, FAKE, 0)), _capi.MSLK_ERR_MISALIGNED, "4-byte"),
+    (dict(sq=S(8 * 136 * 64, 8 * 136, 136)), _capi.MSLK_ERR_MISALIGNED, "16 elements"),  # 136 % 16
+    (dict(K=64), _capi.MSLK_ERR_UNSUPPORTED, "head dim 128"),       # > 8 rows on the tensor cores
+    (dict(lanes=L(FAKE, FAKE, None, 0, 0), mask=2), _capi.MSLK_ERR_INVALID_ARG, "B = 1"),
+])
+def test_fp8_rejects(lib, kw, status, needle):
+    st, why = _fp8_call(lib, **kw)
+    assert st == status, why
+    assert needle in why
+
+
+def test_fp8_bf16_strides_pass(lib):
+    """A stride that is a multiple of 8 bf16 elements but not of 16 bytes of E4M3 is refused
+    only for the E4M3 call."""
+    sq = S(8 * 136 * 64, 8 * 136, 136)
+    st, why = _fwd(lib, sq=sq)
+    assert st != _capi.MSLK_ERR_MISALIGNED, why
+
+
+def test_fp8_pass_validation(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for kw in (dict(), dict(K=64, M=4), dict(scales=_capi.Fp8Scales(FAKE, FAKE, FAKE, 1)),
+               dict(B=1, mask=3, lanes=L(FAKE, None, FAKE, 128, 4),
+                    sl=_capi.Seqlens(FAKE, None, 4, 16, 64))):
+        st, why = _fp8_call(lib, **kw)
+        assert st == _capi.MSLK_ERR_CUDA, why

@@ -28,3 +28,15 @@ def test_page_table_is_a_partition():
 def test_varlen_seqlens_sum():
     lens = inputs.varlen_seqlens(12, 16384, seed=0)
     assert sum(lens) == 16384 and min(lens) >= 1
+
+
+def test_quantize_e4m3_round_trip():
+    """Codes times descale reproduce the input to E4M3 precision (relative 2^-4 for normal
+    values, 2^-10 descales below); the largest magnitude per head lands on 448."""
+    x = inputs.qkv(1, 64, 8, 4, 32, seed=9)[0]
+    codes, d = inputs.quantize_e4m3(x)
+    back = codes.view(torch.float8_e4m3fn).float() * d.reshape(1, 1, -1, 1)
+    err = (back - x.float()).abs()
+    assert torch.all(err <= x.float().abs() * 2.0 ** -4 + d.reshape(1, 1, -1, 1) * 2.0 ** -10)
+    top = codes.view(torch.float8_e4m3fn).float().abs().amax(dim=(0, 1, 3))
+    assert torch.all(top == 448.0)
