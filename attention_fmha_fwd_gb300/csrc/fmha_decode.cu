@@ -210,70 +210,151 @@ struct DecodeState {
 };
 
 // Folds one tile of keys (in shared memory, row-major [T][D]) into the warp's
-// online-softmax state, 32 keys at a time.
+// online-softmax state, 32 keys at a time.  bf16: qf holds the query rows pre-multiplied by
+// the base-2 score scale.  E4M3: qh holds them as exact f16 pairs, the products are formed
+// with mixed-precision FMAs (exact, added in fp32), the score is scaled by qscale after the
+// reduction, and p is rounded to f16 (relative 2^-11) for P.V.
 template <int D, int MQ, bool F8>
 MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ][D / 32],
-                        const uint8_t* sK, const uint8_t* sV, int key0, int kb1, int lane,
-                        DecodeState<D, MQ>& st) {
+                        const uint32_t (&qh)[MQ][D / 64], float qscale, const uint8_t* sK,
+                        const uint8_t* sV, int key0, int kb1, int lane, DecodeState<D, MQ>& st) {
   constexpr int VE = D / 32;
   constexpr int T = DecLayout<D, F8>::kT;
   constexpr int ES = DecLayout<D, F8>::kEsz;
+  // Blocks of 32 keys folded per step: two when the tile holds 64 or more keys, so the
+  // two score reductions interleave and one max / sum / rescale covers both.
+  constexpr int NB = T >= 64 ? 2 : 1;
+  // With few query rows each lane has only MQ * VE accumulator chains; the blocks of a
+  // step then accumulate separately (twice the independent FMA chains) and are summed once.
+  constexpr int NA = (NB == 2 && MQ <= 2) ? 2 : 1;
   using VT = typename Vec<VE, F8>::T;
 #pragma unroll 1
-  for (int sb = 0; sb < T; sb += 32) {
-    const int n_valid = kb1 - (key0 + sb);  // keys of this block below kb1 (warp-uniform)
+  for (int sb = 0; sb < T; sb += 32 * NB) {
+    const int n_valid = kb1 - (key0 + sb);  // keys of this step below kb1 (warp-uniform)
     if (n_valid <= 0) break;                // the rest of the tile is past the range
-    const int my_key = key0 + sb + lane;
     const VT* kp = reinterpret_cast<const VT*>(sK + (sb * D + lane * VE) * ES);
     const VT* vp = reinterpret_cast<const VT*>(sV + (sb * D + lane * VE) * ES);
-    float p[MQ];
+    float p[NB][MQ];
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
-      p[m] = 0.f;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) p[b][m] = 0.f;
       if (m >= nq) continue;
-      float part[32];
+      float part[NB][32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float kf[VE];
-        Vec<VE, F8>::to_float(kp[j * (D / VE)], kf);
-        float d = 0.f;
 #pragma unroll
-        for (int e = 0; e < VE; ++e) d = fmaf(qf[m][e], kf[e], d);
-        part[j] = d;
+        for (int b = 0; b < NB; ++b) {
+          const VT kx = kp[(b * 32 + j) * (D / VE)];
+          float d = 0.f;
+          if constexpr (F8) {
+            if constexpr (VE == 4) {
+              d = dot2_f16_f32(d, qh[m][0], e4m3x2_to_f16x2(static_cast<uint16_t>(kx & 0xFFFFu)));
+              d = dot2_f16_f32(d, qh[m][1], e4m3x2_to_f16x2(static_cast<uint16_t>(kx >> 16)));
+            } else {
+              d = dot2_f16_f32(d, qh[m][0], e4m3x2_to_f16x2(kx));
+            }
+          } else {
+            float kf[VE];
+            Vec<VE, F8>::to_float(kx, kf);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) d = fmaf(qf[m][e], kf[e], d);
+          }
+          part[b][j] = d;
+        }
       }
-      float sc = butterfly_reduce32(part, lane);
-      const bool allowed = my_key < kb1 && my_key <= m + hi && my_key >= m + lo;
-      sc = allowed ? sc : -INFINITY;
-      const float m_new = fmaxf(st.m_run[m], warp_max(sc));
+      float sc[NB];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        sc[b] = butterfly_reduce32(part[b], lane);
+        if constexpr (F8) sc[b] *= qscale;
+        const int my_key = key0 + sb + b * 32 + lane;
+        const bool allowed = my_key < kb1 && my_key <= m + hi && my_key >= m + lo;
+        sc[b] = allowed ? sc[b] : -INFINITY;
+        mx = fmaxf(mx, sc[b]);
+      }
+      const float m_new = fmaxf(st.m_run[m], warp_max(mx));
       const float msub = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(st.m_run[m] - msub);  // m_run = -inf -> 0
-      p[m] = ex2_approx(sc - msub);
-      st.l_run[m] = st.l_run[m] * alpha + warp_sum(p[m]);
+      float psum = 0.f;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        p[b][m] = ex2_approx(sc[b] - msub);
+        psum += p[b][m];
+      }
+      st.l_run[m] = st.l_run[m] * alpha + warp_sum(psum);
       st.m_run[m] = m_new;
 #pragma unroll
       for (int e = 0; e < VE; ++e) st.acc[m][e] *= alpha;
     }
     // V rows at or past kb1 get p = 0, but they may hold anything (a key lane's
     // unwritten tail) and 0 * NaN is NaN: this warp owns the tile, so it clears them.
-    if (n_valid < 32) {
+    if (n_valid < 32 * NB) {
       uint8_t* tail = const_cast<uint8_t*>(sV) + (sb + n_valid) * D * ES;
-      for (int off = lane * 16; off < (32 - n_valid) * D * ES; off += 32 * 16)
+      for (int off = lane * 16; off < (32 * NB - n_valid) * D * ES; off += 32 * 16)
         *reinterpret_cast<uint4*>(tail + off) = make_uint4(0, 0, 0, 0);
       __syncwarp();
     }
     // One pass over the V rows for every query row.
+    float acc2[NA][MQ][VE];
+#pragma unroll
+    for (int m = 0; m < MQ; ++m)
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        acc2[0][m][e] = st.acc[m][e];
+        if constexpr (NA == 2) acc2[NA - 1][m][e] = 0.f;
+      }
+    if constexpr (F8) {
+      uint32_t ph[NB][MQ];
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int m = 0; m < MQ; ++m) ph[b][m] = f32_to_f16_bits(p[b][m]);
+#pragma unroll 2
+      for (int j = 0; j < 32; ++j) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const VT vx = vp[(b * 32 + j) * (D / VE)];
+          uint32_t vh[VE / 2];
+          if constexpr (VE == 4) {
+            vh[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(vx & 0xFFFFu));
+            vh[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(vx >> 16));
+          } else {
+            vh[0] = e4m3x2_to_f16x2(vx);
+          }
+#pragma unroll
+          for (int m = 0; m < MQ; ++m) {
+            if (m >= nq) continue;
+            const uint32_t pj = __shfl_sync(0xffffffffu, ph[b][m], j);
+            float(&ac)[VE] = acc2[b % NA][m];
+#pragma unroll
+            for (int e = 0; e < VE / 2; ++e) axpy2_f16_f32(ac[2 * e], ac[2 * e + 1], pj, vh[e]);
+          }
+        }
+      }
+    } else {
 #pragma unroll 4
-    for (int j = 0; j < 32; ++j) {
-      float vf[VE];
-      Vec<VE, F8>::to_float(vp[j * (D / VE)], vf);
+      for (int j = 0; j < 32; ++j) {
 #pragma unroll
-      for (int m = 0; m < MQ; ++m) {
-        if (m >= nq) continue;
-        const float pj = __shfl_sync(0xffffffffu, p[m], j);
+        for (int b = 0; b < NB; ++b) {
+          float vf[VE];
+          Vec<VE, F8>::to_float(vp[(b * 32 + j) * (D / VE)], vf);
 #pragma unroll
-        for (int e = 0; e < VE; ++e) st.acc[m][e] = fmaf(pj, vf[e], st.acc[m][e]);
+          for (int m = 0; m < MQ; ++m) {
+            if (m >= nq) continue;
+            const float pj = __shfl_sync(0xffffffffu, p[b][m], j);
+            float(&ac)[VE] = acc2[b % NA][m];
+#pragma unroll
+            for (int e = 0; e < VE; ++e) ac[e] = fmaf(pj, vf[e], ac[e]);
+          }
+        }
       }
     }
+#pragma unroll
+    for (int m = 0; m < MQ; ++m)
+#pragma unroll
+      for (int e = 0; e < VE; ++e) st.acc[m][e] = NA == 2 ? acc2[0][m][e] + acc2[NA - 1][m][e] : acc2[0][m][e];
   }
 }
 
@@ -283,8 +364,8 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
   constexpr int VE = D / 32;  // head-dim elements per lane
   constexpr int T = L::kT;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned, derived from the shared array itself so accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbortOff);
   volatile int* issued_ctr = reinterpret_cast<volatile int*>(smem + L::kIssuedOff);
@@ -411,11 +492,22 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
     float qscale = a.scale_log2;
     if constexpr (F8) qscale *= a.dq[a.desc_per_tensor ? 0 : h] * a.dk[a.desc_per_tensor ? 0 : hk];
     float qf[MQ][VE];
+    uint32_t qh[MQ][VE / 2];  // E4M3 rows as exact f16 pairs
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
+#pragma unroll
+      for (int e = 0; e < VE / 2; ++e) qh[m][e] = 0u;
       if (m < nq) {
         const long long el = bc * a.sq_b + (qrow0 + m) * a.sq_m + h * a.sq_h + lane * VE;
         const VT x = *reinterpret_cast<const VT*>(a.q + el * L::kEsz);
+        if constexpr (F8) {
+          if constexpr (VE == 4) {
+            qh[m][0] = e4m3x2_to_f16x2(static_cast<uint16_t>(x & 0xFFFFu));
+            qh[m][1] = e4m3x2_to_f16x2(static_cast<uint16_t>(x >> 16));
+          } else {
+            qh[m][0] = e4m3x2_to_f16x2(x);
+          }
+        }
         Vec<VE, F8>::to_float(x, qf[m]);
 #pragma unroll
         for (int e = 0; e < VE; ++e) qf[m][e] *= qscale;
@@ -431,7 +523,7 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
                                      wait_bounded(sbase + L::kFullOff + 8 * s, (i / kStages) & 1, abort_flag, a));
       if (!ok) break;
       const uint8_t* sK = smem + s * L::kStageBytes;
-      fold_tile<D, MQ, F8>(nq, lo, hi, qf, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
+      fold_tile<D, MQ, F8>(nq, lo, hi, qf, qh, qscale, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
       __syncwarp();
       if (lane == 0) mbar_arrive(sbase + L::kEmptyOff + 8 * s);
     }

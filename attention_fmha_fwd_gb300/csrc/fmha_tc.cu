@@ -315,8 +315,8 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
                       const CUtensorMap& tm_o, const TcArgs& a) {
   using L = Layout<D, F8>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned, derived from the shared array itself so accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int G = gridDim.x;

@@ -395,4 +395,39 @@ MSLK_DEV float2 e4m3x2_to_f2(uint16_t v) {
   return r;
 }
 
+// Two E4M3 bytes (the low byte first) -> f16x2 (exact).
+MSLK_DEV uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  return h2;
+}
+// d + a . b over the two f16 halves of a and b, each product exact, added in fp32
+// (mixed-precision FMA).
+MSLK_DEV float dot2_f16_f32(float d, uint32_t a, uint32_t b) {
+  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+      "mov.b32 {a0, a1}, %1;\n\t"
+      "mov.b32 {b0, b1}, %2;\n\t"
+      "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+      "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+      : "+f"(d)
+      : "r"(a), "r"(b));
+  return d;
+}
+// acc0 += p * v.lo, acc1 += p * v.hi; p is the f16 in the low half of p_h.
+MSLK_DEV void axpy2_f16_f32(float& acc0, float& acc1, uint32_t p_h, uint32_t v) {
+  asm("{\n\t.reg .f16 p0, p1, v0, v1;\n\t"
+      "mov.b32 {p0, p1}, %2;\n\t"
+      "mov.b32 {v0, v1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, p0, v0, %0;\n\t"
+      "fma.rn.f32.f16 %1, p0, v1, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(p_h), "r"(v));
+}
+// fp32 -> f16 (round to nearest even) in the low half of a 32-bit word.
+MSLK_DEV uint32_t f32_to_f16_bits(float x) {
+  uint16_t h;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return h;
+}
+
 }  // namespace mslk
