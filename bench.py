@@ -59,6 +59,15 @@ def fwd_flops(w):
     return causal_pairs(w.M, w.Mkv) * 2 * (w.K + w.Kv) * w.B * w.H
 
 
+def check_device(fa, what):
+    """A kernel that gave up on a bounded wait leaves its output incomplete: no number
+    measured over it is reported."""
+    st = fa.device_status()
+    if st != 0:
+        raise RuntimeError(f"device error word set during the {what} (status {st}): "
+                           "a kernel timed out on a bounded wait; the measurement is void")
+
+
 def kernel_sha():
     with open(KERNEL_SRC, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -320,6 +329,7 @@ def run_gpu(args):
     t1 = time.time()
     per = [s.elapsed_time(e) * 1e-3 for s, e in zip(starts, ends)]
     t_step = sum(per) / len(per)
+    check_device(fa, "timed steps")
     value, t_max = aggregate(t_step, flops, world, reduce_max)
     value /= 1e12
     clocks = sampler.summary(t0, t1) if sampler else None
@@ -393,7 +403,10 @@ def run_gpu(args):
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
 
+    check_device(fa, "end-to-end steps")
     secondary = measure_secondary(fa, inputs, dev, flush, peaks) if (rank == 0 and not args.no_secondary) else None
+    if secondary is not None:
+        check_device(fa, "secondary measurements")
 
     if rank == 0:
         achieved = flops / t_step / 1e12
@@ -703,6 +716,28 @@ def run_profile_other(args):
             for c, (a, b) in enumerate(bounds):
                 fa.attn_partial(qd, kd[:, a:b], vd[:, a:b], scale=w.scale, out=po[c], lse=pl[c])
             fa.merge_attentions(po, pl)
+    elif args.workload == "fp8_causal_fwd":
+        w = inputs.WORKLOADS["causal_fwd"]
+        q, k, v = inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0)
+        q8, dq = inputs.quantize_e4m3(q.to(dev))
+        k8, dk = inputs.quantize_e4m3(k.to(dev))
+        v8, dv = inputs.quantize_e4m3(v.to(dev))
+
+        def step():
+            fa.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, mask="causal", scale=w.scale)
+    elif args.workload == "fp8_decode":
+        # E4M3 decode, 16 x 8192 keys x 8 heads x 128 (268 MB of K/V: larger than L2)
+        g = torch.Generator(device=dev).manual_seed(0)
+        k = torch.randn((16, 8192, 8, 128), generator=g, device=dev)
+        v = torch.randn((16, 8192, 8, 128), generator=g, device=dev)
+        q = torch.randn((16, 1, 8, 128), generator=g, device=dev)
+        k8, dk = inputs.quantize_e4m3(k)
+        v8, dv = inputs.quantize_e4m3(v)
+        q8, dq = inputs.quantize_e4m3(q)
+        del k, v
+
+        def step():
+            fa.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, scale=128 ** -0.5)
     else:
         w = inputs.WORKLOADS["varlen_packed"]
         lens = inputs.varlen_seqlens(w.n_seqs, w.M, seed=0)
@@ -723,6 +758,7 @@ def run_profile_other(args):
         step()
     b.record()
     torch.cuda.synchronize()
+    check_device(fa, "profiled steps")
     print(json.dumps({"profile_mode": True, "workload": args.workload,
                       "ms_per_step": a.elapsed_time(b) / args.steps}))
     return 0
@@ -740,7 +776,8 @@ def main():
     ap.add_argument("--profile-mode", action="store_true",
                     help="only the warm-up and timed steps (for ncu); prints a short line")
     ap.add_argument("--workload", default="causal_fwd",
-                    choices=["causal_fwd", "merge", "decode_split_kv", "varlen_packed"],
+                    choices=["causal_fwd", "merge", "decode_split_kv", "varlen_packed", "fp8_causal_fwd",
+                             "fp8_decode"],
                     help="with --profile-mode: which kernel's workload to run")
     args = ap.parse_args()
     if args.warmup < 3:
