@@ -261,6 +261,26 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------- GPU arm
 
+def make_collectives(world, device):
+    """(reduce_max, barrier) over the ranks of the initialised process group (identity and
+    no-op for one rank): the slowest rank's time and the step fences around the timed
+    region.  ``device`` is where the reduced scalar lives ("cuda" for NCCL, "cpu" for gloo)."""
+    if world <= 1:
+        return (lambda x: x), (lambda: None)
+    import torch
+    import torch.distributed as dist
+
+    def reduce_max(x):
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def barrier():
+        dist.barrier()
+
+    return reduce_max, barrier
+
+
 def run_gpu(args):
     import torch
 
@@ -269,22 +289,10 @@ def run_gpu(args):
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-
-        def reduce_max(x):
-            t = torch.tensor([x], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-
-        def barrier():
-            dist.barrier()
+        reduce_max, barrier = make_collectives(world, "cuda")
     else:
         torch.cuda.set_device(0)
-
-        def reduce_max(x):
-            return x
-
-        def barrier():
-            pass
+        reduce_max, barrier = make_collectives(1, "cuda")
 
     import attention_fmha_fwd_gb300 as fa
     from attention_fmha_fwd_gb300 import build, inputs
@@ -423,6 +431,7 @@ def run_gpu(args):
             "roofline": {"bound": "tensor", "achieved": achieved,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                         "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
                          "kernel": "fmha_tc_kernel<128, false>", "peak_source": peak_src + " bf16 burst"},
             "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
@@ -466,6 +475,35 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
     import torch
     stream = torch.cuda.current_stream()
     res = {}
+    # tiny forward [1, 128, 2, 64], scale 1/8 (launch-latency bound: microseconds only)
+    w = inputs.WORKLOADS["tiny_fwd"]
+    qt, kt, vt = (t.to(dev) for t in inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0))
+    tiny = lambda: fa.attn_fwd(qt, kt, vt, scale=w.scale)  # noqa: E731
+    for _ in range(10):
+        tiny()
+    res["tiny_fwd_1x128x2x64"] = {"us": _time_it(tiny, 50, stream, flush) * 1e6, "launches": 1}
+    # split-KV: q [1, 128, 16, 128] against k/v [1, 1024, 16, 128] in n equal chunks
+    # (strided views, no copies): n partial launches (fp32 out) + one merge, timed apart
+    w = inputs.WORKLOADS["split_kv"]
+    qs, ks, vs = (t.to(dev) for t in inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0))
+    for n in (2, 8):
+        bounds = inputs.equal_chunks(w.Mkv, n)
+        po = torch.empty((n, w.B, w.M, w.H, w.Kv), dtype=torch.float32, device=dev)
+        pl = torch.empty((n, w.B, w.H, w.M), dtype=torch.float32, device=dev)
+        mo = torch.empty((w.B, w.M, w.H, w.Kv), dtype=torch.bfloat16, device=dev)
+        ml = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=dev)
+
+        def parts(bounds=bounds, po=po, pl=pl):
+            for c, (a0, b0) in enumerate(bounds):
+                fa.attn_partial(qs, ks[:, a0:b0], vs[:, a0:b0], scale=w.scale, out=po[c], lse=pl[c])
+
+        merge = lambda po=po, pl=pl, mo=mo, ml=ml: fa.merge_attentions(po, pl, out=mo, lse=ml)  # noqa: E731
+        for _ in range(10):
+            parts()
+            merge()
+        res[f"split_kv_{n}_chunks_1x128x1024x16x128"] = {
+            "partials_us": _time_it(parts, 50, stream, flush) * 1e6,
+            "merge_us": _time_it(merge, 50, stream, flush) * 1e6, "launches": n + 1}
     # merge: 8 chunks of [2, 2048, 32, 128] fp32 -> bf16 out + fp32 lse
     n, B, M, H, Kv = 8, 2, 2048, 32, 128
     g = torch.Generator(device=dev).manual_seed(0)
