@@ -67,8 +67,11 @@ an average):
 
 Inputs are arrays of any float dtype holding the exact bf16 values; they are widened to
 float64 here.  ``scale`` is the float32 value the library receives, widened to float64.
-Heads of K/V: either H (one per query head) or 1 (a single head shared by every query
-head, which is what a stride-0 head expansion denotes).
+Heads of K/V: Hk dividing H.  Query head h reads K/V head h // (H / Hk): grouped-query
+attention in the pages' BMGHK layout flattened group-major (query head g * (H / Hk) + i
+belongs to group g, whose keys and values are shared; ``bmghk2bmhk``).  Hk = H is plain
+multi-head attention; Hk = 1 is one head shared by every query head (what a stride-0
+head expansion denotes).
 
 Parity pins for every function here live in ``tests/oracle_pins.py``.
 """
@@ -162,8 +165,8 @@ def _check_shapes(q, k, v):
         raise ValueError("batch / key length mismatch")
     if k.shape[3] != K:
         raise ValueError("q and k head dims differ")
-    if k.shape[2] not in (H, 1) or v.shape[2] != k.shape[2]:
-        raise ValueError("k/v must have H heads or a single shared head")
+    if k.shape[2] < 1 or H % k.shape[2] or v.shape[2] != k.shape[2]:
+        raise ValueError("k/v must have a number of heads dividing H (grouped-query attention)")
     return B, M, H, K, k.shape[1], v.shape[3]
 
 
@@ -178,7 +181,7 @@ def attention_head(q, k, v, b, h, scale, mask_kind=MASK_NONE, cu_seqlens_q=None,
     select the alignment and local window described in the module docstring.
     """
     B, M, H, K, Mkv, Kv = _check_shapes(q, k, v)
-    hk = h if k.shape[2] == H else 0
+    hk = h // (H // k.shape[2])  # the query head's group
     s64 = _scale64(scale)
     kb_all = np.asarray(k[b, :, hk, :], dtype=np.float64)
     vb_all = np.asarray(v[b, :, hk, :], dtype=np.float64)
@@ -276,7 +279,7 @@ def attention_lanes(q, k, v, scale, mask_kind, cu_seqlens_q, seqlen_k, seqstart_
         rows = lane_rows(s, seqlen_k, seqstart_k, block_table, page_size)
         lo, hi = _band(mask_kind, bottom_right, window_left, window_right, qe - qs, len(rows))
         for h in range(H):
-            hk = 0 if k.shape[2] == 1 else h
+            hk = h // (H // k.shape[2])
             qb = np.asarray(q[0, qs:qe, h, :], dtype=np.float64)
             kb = np.asarray(k[0, rows, hk, :], dtype=np.float64)
             vb = np.asarray(v[0, rows, hk, :], dtype=np.float64)

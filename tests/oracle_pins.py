@@ -86,7 +86,7 @@ def brute_attention(q, k, v, scale, kind=0, cu_q=None, cu_k=None, kv_offset=0,
     lse = [[[NEG_INF] * M for _ in range(H)] for _ in range(B)]
     for b in range(B):
         for h in range(H):
-            hk = h if Hk == H else 0
+            hk = (h * Hk) // H  # query heads in Hk equal consecutive groups
             for i in range(M):
                 x = []
                 for j in range(Mkv):
@@ -330,6 +330,25 @@ def pin_scale_folds_into_q(orc):
     o2, l2 = orc.attention(2 * q, k, v, 0.25)
     _close(o2, o1, 1e-13, "scale out")
     _close(l2, l1, 1e-13, "scale lse")
+
+
+def pin_grouped_query_heads(orc):
+    """Grouped-query attention: query heads g*r .. g*r + r - 1 share K/V head g.  Checked
+    against the brute force and against explicitly repeating each K/V head r times."""
+    rng = np.random.default_rng(71)
+    for (B, M, Mkv, H, Hk, kind) in ((1, 4, 5, 4, 2, 0), (2, 3, 6, 6, 3, 1), (1, 5, 5, 6, 2, 1)):
+        q = _rand(rng, (B, M, H, 8))
+        k = _rand(rng, (B, Mkv, Hk, 8))
+        v = _rand(rng, (B, Mkv, Hk, 8))
+        ro, rl = brute_attention(q, k, v, 0.4, kind)
+        o, l_ = orc.attention(q, k, v, 0.4, kind)
+        _close(o, ro, 1e-12, f"gqa out {H}/{Hk}")
+        _close(l_, rl, 1e-12, f"gqa lse {H}/{Hk}")
+        r = H // Hk
+        ke, ve = np.repeat(k, r, axis=2), np.repeat(v, r, axis=2)  # head g*r + i <- group g
+        oe, le = orc.attention(q, ke, ve, 0.4, kind)
+        _close(o, oe, 1e-12, "gqa = repeated heads (out)")
+        _close(l_, le, 1e-12, "gqa = repeated heads (lse)")
 
 
 def pin_shared_kv_head(orc):
@@ -812,6 +831,7 @@ PINS = [
     pin_permute_keys,
     pin_scale_folds_into_q,
     pin_shared_kv_head,
+    pin_grouped_query_heads,
     pin_merge_any_chunking,
     pin_merge_against_brute,
     pin_merge_identities,

@@ -36,14 +36,16 @@ MUTANTS = {
     "out_not_normalised": ("out = (p @ vb) / l[:, None]", "out = (p @ vb)"),
     "exp_not_shifted": ("p = np.exp(x - np.where(empty, 0.0, m)[:, None])", "p = np.exp(x)"),
     "empty_rows_not_zeroed": ("    out[empty] = 0.0\n", ""),
-    "shared_head_always_zero": ("hk = h if k.shape[2] == H else 0", "hk = 0"),
+    "shared_head_always_zero": ("hk = h // (H // k.shape[2])  # the query head's group", "hk = 0"),
+    "gqa_heads_interleaved": ("hk = h // (H // k.shape[2])  # the query head's group",
+                              "hk = h % k.shape[2]"),
     "blockdiag_sees_all_keys": ("_block(qb_all[qs:qe], kb_all[ks:ke], vb_all[ks:ke], s64,",
                                 "_block(qb_all[qs:qe], kb_all, vb_all, s64,"),
     "blockdiag_absolute_positions": ("s64, lo, hi, 0,\n                              kv_offset)",
                                      "s64, lo, hi, qs,\n                              ks + kv_offset)"),
     "paged_index_swapped": ("return pages[p // page_size] * page_size + p % page_size",
                             "return pages[p % page_size] * page_size + p // page_size"),
-    "lane_shared_head_always_zero": ("hk = 0 if k.shape[2] == 1 else h", "hk = 0"),
+    "lane_shared_head_always_zero": ("            hk = h // (H // k.shape[2])\n", "            hk = 0\n"),
     "lane_start_ignored": ("return int(seqstart_k[s]) + p", "return p"),
     "lane_reads_padding": ("n = int(seqlen_k[s])", "n = int(seqlen_k[s]) + 1"),
     "lane_bottom_right_uses_padding": (
