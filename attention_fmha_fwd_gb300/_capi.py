@@ -63,6 +63,17 @@ class Fp8Scales(ctypes.Structure):
                 ("descale_v", ctypes.c_void_p), ("per_tensor", ctypes.c_int32)]
 
 
+class AttnArgs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("sq", Strides), ("sk", Strides), ("sv", Strides), ("so", Strides),
+                ("B", ctypes.c_int32), ("M", ctypes.c_int32), ("Mkv", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("Kv", ctypes.c_int32), ("scale", ctypes.c_float), ("mask_kind", ctypes.c_int32),
+                ("seqlens", ctypes.c_void_p), ("band", ctypes.c_void_p), ("lanes", ctypes.c_void_p),
+                ("fp8", ctypes.c_void_p), ("partial", ctypes.c_int32), ("kv_offset", ctypes.c_int64),
+                ("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int32), ("lse", ctypes.c_void_p)]
+
+
 class MslkError(RuntimeError):
     """A non-OK mslk_status, with the library's reason string."""
 
@@ -96,6 +107,7 @@ SIGNATURES = {
     "mslk_attn_fwd_fp8": (_i32, [_P, _P, _P, _S, _S, _S, _S, _i32, _i32, _i32, _i32, _i32, _i32,
                                  ctypes.c_float, _i32, ctypes.POINTER(Seqlens), ctypes.POINTER(Band),
                                  ctypes.POINTER(KvLanes), ctypes.POINTER(Fp8Scales), _P, _P, _P]),
+    "mslk_attn": (_i32, [ctypes.POINTER(AttnArgs), _P]),
     "mslk_merge_attentions": (_i32, [_P, _P, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _S, _S,
                                      _P, _i32, _P, _P]),
     "mslk_last_error": (ctypes.c_char_p, []),

@@ -83,6 +83,46 @@ def _check_inputs(q, k, v):
             raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
 
 
+def _kv_heads(q, k, v) -> int:
+    """K/V head count, checked against q: equal batch, key count and head dims, and a number
+    of K/V heads dividing the query heads (query head h reads K/V head h // (H // Hkv))."""
+    H = q.shape[2]
+    if k.shape[0] != q.shape[0] or v.shape[0] != q.shape[0]:
+        raise ValueError("q, k and v must have the same batch size")
+    if k.shape[1] != v.shape[1] or k.shape[2] != v.shape[2]:
+        raise ValueError("k and v must have the same number of keys and heads")
+    if k.shape[3] != q.shape[3]:
+        raise ValueError("q and k head dims differ")
+    Hkv = k.shape[2]
+    if Hkv < 1 or H % Hkv:
+        raise ValueError(f"k/v heads ({Hkv}) must divide the query heads ({H})")
+    return Hkv
+
+
+def _addr(x):
+    """Address of a ctypes struct, or of the struct behind ctypes.byref(...); None stays None."""
+    if x is None:
+        return None
+    return ctypes.addressof(x if isinstance(x, ctypes.Structure) else x._obj)
+
+
+def _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, *, lanes=None,
+             fp8=None, partial=0, kv_offset=0):
+    """mslk_attn with every option in one argument struct (grouped K/V heads)."""
+    B, M, H, K = q.shape
+    a = _capi.AttnArgs()
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.sq, a.sk, a.sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
+    a.so = _bmhk_strides(out, "out")
+    a.B, a.M, a.Mkv, a.H, a.Hkv, a.K, a.Kv = B, M, k.shape[1], H, Hkv, K, v.shape[3]
+    a.scale = 0.0 if scale is None else float(scale)
+    a.mask_kind = mk
+    a.seqlens, a.band, a.lanes, a.fp8 = _addr(sl), _addr(band), _addr(lanes), _addr(fp8)
+    a.partial, a.kv_offset = int(partial), int(kv_offset)
+    a.out, a.out_dtype, a.lse = out.data_ptr(), _DTYPES[out_dtype], _ptr(lse)
+    check(_capi.load().mslk_attn(ctypes.byref(a), _stream_handle(stream, q.device)))
+
+
 def _band(bottom_right, window_left, window_right):
     """mslk_band for the *_band entry points, or None when the plain call suffices."""
     if not bottom_right and window_left is None and window_right is None:
@@ -124,6 +164,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", 
     """
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
     _check_inputs(q, k, v)
+    Hkv = _kv_heads(q, k, v)
     B, M, H, K = q.shape
     Mkv, Kv = k.shape[1], v.shape[3]
     mk = _mask_kind(mask)
@@ -134,10 +175,13 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", 
     elif lse is False:
         lse = None
     sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    band = _band(bottom_right, window_left, window_right)
+    if Hkv != H:  # grouped K/V heads
+        _general(q, k, v, Hkv, mk, scale, sl, band, out, torch.bfloat16, lse, stream)
+        return out, lse
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")
     lib = _capi.load()
-    band = _band(bottom_right, window_left, window_right)
     sc = 0.0 if scale is None else float(scale)
     if band is None:
         check(lib.mslk_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
@@ -188,6 +232,7 @@ def attn_fwd_lanes(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, seqlen_
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
     k, v = _pool_rows(k, "k"), _pool_rows(v, "v")
     _check_inputs(q, k, v)
+    Hkv = _kv_heads(q, k, v)
     B, M, H, K = q.shape
     if B != 1:
         raise ValueError("attn_fwd_lanes takes packed queries [1, total_q, H, K]")
@@ -220,6 +265,9 @@ def attn_fwd_lanes(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, seqlen_
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")
     band = _band(bottom_right, window_left, window_right)
+    if Hkv != H:  # grouped K/V heads
+        _general(q, k, v, Hkv, mk, scale, sl, band, out, torch.bfloat16, lse, stream, lanes=lanes)
+        return out, lse
     lib = _capi.load()
     check(lib.mslk_attn_fwd_lanes(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
                                   ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), M, Mkv, H, K,
@@ -264,6 +312,7 @@ def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descale_q, d
             raise ValueError(f"{name} must be a CUDA tensor (the library reads device memory)")
         if t.dtype not in _FP8_DTYPES:
             raise ValueError(f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    Hkv = _kv_heads(q, k, v)
     B, M, H, K = q.shape
     Mkv, Kv = k.shape[1], v.shape[3]
     mk = _mask_kind(mask)
@@ -273,7 +322,7 @@ def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descale_q, d
     sizes = {dq.numel(), dk.numel(), dv.numel()}
     per_tensor = 1 if sizes == {1} else 0
     if not per_tensor:
-        hk = 1 if (k.stride(2) == 0 and H > 1) else H
+        hk = 1 if (k.stride(2) == 0 and H > 1) else Hkv
         if dq.numel() != H or dk.numel() != hk or dv.numel() != hk:
             raise ValueError(f"per-head descales need {H} (q) and {hk} (k, v) entries, or one each")
     scales = _capi.Fp8Scales(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), per_tensor)
@@ -310,6 +359,10 @@ def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descale_q, d
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")
     band = _band(bottom_right, window_left, window_right)
+    if Hkv != H:  # grouped K/V heads
+        _general(q, k, v, Hkv, mk, scale, sl, band, out, torch.bfloat16, lse, stream, lanes=lanes,
+                 fp8=scales)
+        return out, lse
     lib = _capi.load()
     check(lib.mslk_attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),
                                 ctypes.byref(sk), ctypes.byref(sv), ctypes.byref(so), B, M, Mkv, H, K,
@@ -331,6 +384,7 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
     """
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
     _check_inputs(q, k, v)
+    Hkv = _kv_heads(q, k, v)
     B, M, H, K = q.shape
     Mkv, Kv = k.shape[1], v.shape[3]
     mk = _mask_kind(mask)
@@ -343,10 +397,14 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
     if lse is None:
         lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
     sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    band = _band(False, window_left, window_right)
+    if Hkv != H:  # grouped K/V heads
+        _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, partial=1,
+                 kv_offset=kv_offset)
+        return out, lse
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")
     lib = _capi.load()
-    band = _band(False, window_left, window_right)
     sc = 0.0 if scale is None else float(scale)
     if band is None:
         check(lib.mslk_attn_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(sq),

@@ -51,7 +51,8 @@ struct DecLayout {
   static constexpr int kEmptyOff = kFullOff + 8 * kStages;
   static constexpr int kAbortOff = kEmptyOff + 8 * kStages;
   static constexpr int kIssuedOff = kAbortOff + 4;  // tiles issued so far (producer-written)
-  static constexpr int kBytes = kAbortOff + 16;
+  static constexpr int kPosOff = kAbortOff + 16;    // query position of each row [8]
+  static constexpr int kBytes = kPosOff + 32;
   static constexpr int kAlloc = kBytes + 1024;     // slack for 1024-byte alignment
 };
 
@@ -59,7 +60,9 @@ struct DecArgs {
   const uint8_t* q;  // bf16 or E4M3 elements
   long long sq_b, sq_m, sq_h;
   int M, Mkv, H;
-  int hk_shared;
+  // Query head h reads K/V head h / kv_group; each CTA takes `fold` query heads of one K/V
+  // head (a divisor of kv_group) as extra rows, so that K/V head is streamed once for them.
+  int kv_group, fold;
   int cs;  // CTAs per (batch, head): the cluster size
   // Key j is allowed for query row m iff m + lo <= j <= m + hi (kv_offset folded in;
   // +-kBandOpen: open), plus each packed sequence's Lk - Lq when band_seq is set.
@@ -214,10 +217,12 @@ struct DecodeState {
 // the base-2 score scale.  E4M3: qh holds them as exact f16 pairs, the products are formed
 // with mixed-precision FMAs (exact, added in fp32), the score is scaled by qscale after the
 // reduction, and p is rounded to f16 (relative 2^-11) for P.V.
+// Row m (m < nrows) holds the query at position pos[m] (folded query heads share positions).
 template <int D, int MQ, bool F8>
-MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ][D / 32],
-                        const uint32_t (&qh)[MQ][D / 64], float qscale, const uint8_t* sK,
-                        const uint8_t* sV, int key0, int kb1, int lane, DecodeState<D, MQ>& st) {
+MSLK_DEV void fold_tile(int nrows, const int* pos, long long lo, long long hi,
+                        const float (&qf)[MQ][D / 32], const uint32_t (&qh)[MQ][D / 64],
+                        const float (&qscale)[MQ], const uint8_t* sK, const uint8_t* sV, int key0,
+                        int kb1, int lane, DecodeState<D, MQ>& st) {
   constexpr int VE = D / 32;
   constexpr int T = DecLayout<D, F8>::kT;
   constexpr int ES = DecLayout<D, F8>::kEsz;
@@ -239,7 +244,7 @@ MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ
     for (int m = 0; m < MQ; ++m) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) p[b][m] = 0.f;
-      if (m >= nq) continue;
+      if (m >= nrows) continue;
       float part[NB][32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -268,9 +273,9 @@ MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         sc[b] = butterfly_reduce32(part[b], lane);
-        if constexpr (F8) sc[b] *= qscale;
+        if constexpr (F8) sc[b] *= qscale[m];
         const int my_key = key0 + sb + b * 32 + lane;
-        const bool allowed = my_key < kb1 && my_key <= m + hi && my_key >= m + lo;
+        const bool allowed = my_key < kb1 && my_key <= pos[m] + hi && my_key >= pos[m] + lo;
         sc[b] = allowed ? sc[b] : -INFINITY;
         mx = fmaxf(mx, sc[b]);
       }
@@ -325,7 +330,7 @@ MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ
           }
 #pragma unroll
           for (int m = 0; m < MQ; ++m) {
-            if (m >= nq) continue;
+            if (m >= nrows) continue;
             const uint32_t pj = __shfl_sync(0xffffffffu, ph[b][m], j);
             float(&ac)[VE] = acc2[b % NA][m];
 #pragma unroll
@@ -342,7 +347,7 @@ MSLK_DEV void fold_tile(int nq, long long lo, long long hi, const float (&qf)[MQ
           Vec<VE, F8>::to_float(vp[(b * 32 + j) * (D / VE)], vf);
 #pragma unroll
           for (int m = 0; m < MQ; ++m) {
-            if (m >= nq) continue;
+            if (m >= nrows) continue;
             const float pj = __shfl_sync(0xffffffffu, p[b][m], j);
             float(&ac)[VE] = acc2[b % NA][m];
 #pragma unroll
@@ -371,10 +376,10 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
   volatile int* issued_ctr = reinterpret_cast<volatile int*>(smem + L::kIssuedOff);
 
   const int rank = static_cast<int>(blockIdx.x) % a.cs;  // CTA rank inside the cluster
-  const int h = static_cast<int>(blockIdx.x) / a.cs;
+  const int hq0 = static_cast<int>(blockIdx.x) / a.cs * a.fold;  // first query head of the CTA
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int hk = a.hk_shared ? 0 : h;
+  const int hk = hq0 / a.kv_group;
   // This CTA's query rows [qrow0, qrow0 + nq) and keys [0, nk) (row krow0 + key, or paged)
   // of batch coordinate bc: a batch (dense) or a packed sequence s (sequence mode).
   const int s_idx = blockIdx.y;
@@ -383,7 +388,7 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
   if (a.seq_mode) {
     bc = 0;
     qrow0 = min(max(a.cu_q[s_idx], 0), a.M);
-    nq = min(min(max(a.cu_q[s_idx + 1], qrow0), a.M) - qrow0, MQ);
+    nq = min(min(max(a.cu_q[s_idx + 1], qrow0), a.M) - qrow0, MQ / a.fold);
     if (a.lanes) {
       nk = max(a.lane_len[s_idx], 0);
       if (a.block_table != nullptr)
@@ -400,6 +405,11 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
       if (hi < kBandOpen) hi += shift;
     }
   }
+
+  // Rows: query head hq0 + r / nq at position r % nq, for r < nrows = nq * fold (the
+  // positions live in shared memory: warp-uniform, read by broadcast).
+  const int nrows = nq * a.fold;
+  int* pos = reinterpret_cast<int*>(smem + L::kPosOff);
 
   // Keys of this (batch or sequence, head) that some row may see: from row 0's lower band
   // edge to the last row's upper edge, split over the cluster's CTAs in whole tiles.
@@ -421,6 +431,7 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
     }
     *abort_flag = 0;
     *issued_ctr = 0;
+    for (int r = 0; r < MQ; ++r) pos[r] = nq > 0 ? r % nq : 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -489,16 +500,18 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
   } else {
     // Query rows, pre-multiplied by scale * log2(e): scores come out in base 2.
     using VT = typename Vec<VE, F8>::T;
-    float qscale = a.scale_log2;
-    if constexpr (F8) qscale *= a.dq[a.desc_per_tensor ? 0 : h] * a.dk[a.desc_per_tensor ? 0 : hk];
+    float qscale[MQ];
     float qf[MQ][VE];
     uint32_t qh[MQ][VE / 2];  // E4M3 rows as exact f16 pairs
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
 #pragma unroll
       for (int e = 0; e < VE / 2; ++e) qh[m][e] = 0u;
-      if (m < nq) {
-        const long long el = bc * a.sq_b + (qrow0 + m) * a.sq_m + h * a.sq_h + lane * VE;
+      qscale[m] = a.scale_log2;
+      if (m < nrows) {
+        const int hq = hq0 + m / nq;  // row m: query head hq, position pos[m]
+        if constexpr (F8) qscale[m] *= a.dq[a.desc_per_tensor ? 0 : hq] * a.dk[a.desc_per_tensor ? 0 : hk];
+        const long long el = bc * a.sq_b + (qrow0 + m % nq) * a.sq_m + hq * a.sq_h + lane * VE;
         const VT x = *reinterpret_cast<const VT*>(a.q + el * L::kEsz);
         if constexpr (F8) {
           if constexpr (VE == 4) {
@@ -510,7 +523,7 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
         }
         Vec<VE, F8>::to_float(x, qf[m]);
 #pragma unroll
-        for (int e = 0; e < VE; ++e) qf[m][e] *= qscale;
+        for (int e = 0; e < VE; ++e) qf[m][e] *= qscale[m];
       } else {
 #pragma unroll
         for (int e = 0; e < VE; ++e) qf[m][e] = 0.f;
@@ -523,7 +536,7 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
                                      wait_bounded(sbase + L::kFullOff + 8 * s, (i / kStages) & 1, abort_flag, a));
       if (!ok) break;
       const uint8_t* sK = smem + s * L::kStageBytes;
-      fold_tile<D, MQ, F8>(nq, lo, hi, qf, qh, qscale, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
+      fold_tile<D, MQ, F8>(nrows, pos, lo, hi, qf, qh, qscale, sK, sK + L::kTileBytes, key_base + i * T, kb1, lane, st);
       __syncwarp();
       if (lane == 0) mbar_arrive(sbase + L::kEmptyOff + 8 * s);
     }
@@ -552,7 +565,7 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
   }
   __syncthreads();
   // Warp w merges row w (MQ <= 8: at most one row per warp).
-  for (int m = warp; m < nq; m += kWarps + 1) {
+  for (int m = warp; m < nrows; m += kWarps + 1) {
     float mstar = -INFINITY;
     for (int w = 0; w < kWarps; ++w) mstar = fmaxf(mstar, s_m[w][m]);
     const float msub = (mstar == -INFINITY) ? 0.f : mstar;
@@ -579,7 +592,8 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
   // memory) alive until rank 0 has read them.
   if (a.cs > 1) cluster_sync(); else __syncthreads();
   if (rank == 0) {
-    for (int m = warp; m < nq; m += kWarps + 1) {
+    for (int m = warp; m < nrows; m += kWarps + 1) {
+      const int hq = hq0 + m / nq, qrow = qrow0 + m % nq;
       float mstar = -INFINITY;
       for (int r = 0; r < a.cs; ++r)
         mstar = fmaxf(mstar, a.cs > 1 ? ld_shared_cluster_f32(mapa_shared(smem_u32(&c_m[m]), r)) : c_m[m]);
@@ -603,18 +617,18 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
       float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
       if constexpr (F8) inv *= a.dv[a.desc_per_tensor ? 0 : hk];
       if (a.out_fp32) {
-        float* op = static_cast<float*>(a.out) + bc * a.so_b + (qrow0 + m) * a.so_m + h * a.so_h + lane * VE;
+        float* op = static_cast<float*>(a.out) + bc * a.so_b + qrow * a.so_m + hq * a.so_h + lane * VE;
 #pragma unroll
         for (int e = 0; e < VE; ++e) op[e] = o[e] * inv;
       } else {
         __nv_bfloat16* op =
-            static_cast<__nv_bfloat16*>(a.out) + bc * a.so_b + (qrow0 + m) * a.so_m + h * a.so_h + lane * VE;
+            static_cast<__nv_bfloat16*>(a.out) + bc * a.so_b + qrow * a.so_m + hq * a.so_h + lane * VE;
 #pragma unroll
         for (int e = 0; e < VE; e += 2)
           *reinterpret_cast<uint32_t*>(op + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
       }
       if (lane == 0 && a.lse != nullptr)
-        a.lse[(static_cast<long long>(bc) * a.H + h) * a.M + qrow0 + m] =
+        a.lse[(static_cast<long long>(bc) * a.H + hq) * a.M + qrow] =
             (Ls > 0.f) ? (mstar + lg2_approx(Ls)) * kLn2 : -INFINITY;
     }
   }
@@ -724,12 +738,13 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, i
   return cudaLaunchKernelEx(&cfg, kernel, tk, tv, a);
 }
 
+// H: CTAs per grid row (query heads / fold); rows: query rows per CTA (positions x fold).
 template <int D, bool F8>
 cudaError_t launch_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecArgs& a, int B, int H,
-                     int rows_q, int rows_k, cudaStream_t stream) {
-  if (rows_q <= 1) return launch_dm<D, 1, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
-  if (rows_q <= 2) return launch_dm<D, 2, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
-  if (rows_q <= 4) return launch_dm<D, 4, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
+                     int rows_q, int rows, int rows_k, cudaStream_t stream) {
+  if (rows <= 1) return launch_dm<D, 1, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  if (rows <= 2) return launch_dm<D, 2, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
+  if (rows <= 4) return launch_dm<D, 4, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
   return launch_dm<D, 8, F8>(tk, tv, a, B, H, rows_q, rows_k, stream);
 }
 
@@ -746,7 +761,7 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   const int D = p.K;
   const int esz = p.fp8 ? 1 : 2;
   const int T = 8192 / (D * esz);
-  const long long hk = p.kv_head_shared ? 1 : p.H;
+  const long long hk = p.Hkv;
   CUtensorMap tk, tv;
   if (!encode_rows_plain(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, D, T, p.fp8) ||
       !encode_rows_plain(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, D, T, p.fp8)) {
@@ -765,7 +780,7 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   a.M = p.M;
   a.Mkv = p.Mkv;
   a.H = p.H;
-  a.hk_shared = p.kv_head_shared ? 1 : 0;
+  a.kv_group = p.kv_group;
   a.lo = p.band_lo <= -kBandOpen ? -kBandOpen : p.band_lo - p.kv_offset;
   a.hi = p.band_hi >= kBandOpen ? kBandOpen : p.band_hi - p.kv_offset;
   a.scale_log2 = p.scale * kLog2e;
@@ -795,13 +810,22 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
     rows_k = p.max_seqlen_k;
   }
   if (grid_rows == 0 || rows_q == 0) return cudaSuccess;
+  // Fold the most query heads of a K/V head into one CTA's rows that stay within the
+  // kernel's row limit (a divisor of the group, so a CTA never spans two K/V heads).
+  a.fold = 1;
+  for (int d = p.kv_group; d >= 1; --d)
+    if (p.kv_group % d == 0 && static_cast<long long>(rows_q) * d <= kDecodeMaxRows) {
+      a.fold = d;
+      break;
+    }
+  const int heads = p.H / a.fold, rows = rows_q * a.fold;
   *why = "decode kernel launch failed";
   if (p.fp8) {
-    if (D == 128) return launch_d<128, true>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
-    return launch_d<64, true>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
+    if (D == 128) return launch_d<128, true>(tk, tv, a, grid_rows, heads, rows_q, rows, rows_k, stream);
+    return launch_d<64, true>(tk, tv, a, grid_rows, heads, rows_q, rows, rows_k, stream);
   }
-  if (D == 128) return launch_d<128, false>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
-  return launch_d<64, false>(tk, tv, a, grid_rows, p.H, rows_q, rows_k, stream);
+  if (D == 128) return launch_d<128, false>(tk, tv, a, grid_rows, heads, rows_q, rows, rows_k, stream);
+  return launch_d<64, false>(tk, tv, a, grid_rows, heads, rows_q, rows, rows_k, stream);
 }
 
 }  // namespace mslk

@@ -97,7 +97,7 @@ struct TcArgs {
   int M, Mkv, H;
   int Z;            // batches, or packed sequences
   int total_units;  // units_m * H * Z
-  int hk_shared;
+  int kv_group;     // query heads per K/V head
   int varlen;
   int units_m;
   float scale_log2;
@@ -236,7 +236,7 @@ MSLK_DEV bool decode_unit(const TcArgs& a, int i, Unit& u) {
   const int unit_m = a.units_m - 1 - level;
   u.h = rem % a.H;
   const int z = rem / a.H;
-  u.hk = a.hk_shared ? 0 : u.h;
+  u.hk = u.h / a.kv_group;
   u.z = z;
   if (a.varlen) {
     u.b = 0;
@@ -939,7 +939,7 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
     *why = "cuTensorMapEncodeTiled is not available from the driver";
     return cudaErrorNotSupported;
   }
-  const long long hk = p.kv_head_shared ? 1 : p.H;
+  const long long hk = p.Hkv;
   CUtensorMap tq, tk, tv;
   if (!encode_bhmd(enc, &tq, p.q, D, p.M, p.H, p.B, p.sq.m, p.sq.h, p.sq.b, F8) ||
       !encode_bhmd(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, F8) ||
@@ -954,7 +954,7 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.M = p.M;
   a.Mkv = p.Mkv;
   a.H = p.H;
-  a.hk_shared = p.kv_head_shared ? 1 : 0;
+  a.kv_group = p.kv_group;
   a.lo = p.band_lo <= -kBandOpen ? -kBandOpen : p.band_lo - p.kv_offset;
   a.hi = p.band_hi >= kBandOpen ? kBandOpen : p.band_hi - p.kv_offset;
   a.band_seq = p.band_seq_shift ? 1 : 0;

@@ -44,7 +44,9 @@ struct AttnProblem {
   void* out;
   bool out_fp32;
   float* lse;           // may be null (forward without lse)
-  bool kv_head_shared;  // k/v head stride 0: every query head reads K/V head 0
+  // K/V heads: query head h reads K/V head h / kv_group (kv_group = H / Hkv).  A k/v head
+  // stride of 0 is one shared head (Hkv = 1).
+  int Hkv, kv_group;
 };
 
 struct MergeProblem {

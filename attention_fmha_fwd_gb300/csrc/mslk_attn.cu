@@ -81,7 +81,7 @@ mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const vo
                           int32_t K, int32_t Kv, float scale, int32_t mask_kind,
                           const mslk_seqlens* seqlens, const mslk_band* band, int64_t kv_offset,
                           void* out, int32_t out_dtype, float* lse, bool lse_required,
-                          bool partial, const char* who, int in_bytes = 2) {
+                          bool partial, const char* who, int in_bytes = 2, int32_t Hkv = 0) {
   if (B < 0 || M < 0 || Mkv < 0 || H < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative size", who);
   if (mask_kind < MSLK_MASK_NONE || mask_kind > MSLK_MASK_BLOCKDIAG_CAUSAL_BOTTOM_RIGHT)
     return fail(MSLK_ERR_INVALID_ARG, "%s: unknown mask_kind %d", who, mask_kind);
@@ -122,6 +122,8 @@ mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const vo
   p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : 1.0f / std::sqrt(static_cast<float>(K));
   p.mask_kind = mask_kind;
   p.kv_offset = kv_offset;
+  p.Hkv = H;
+  p.kv_group = 1;
   // Band on (key position - query row): causal kinds close it at 0, windows at -wl / +wr;
   // a dense bottom-right alignment shifts both bounds by Mkv - M, a block-diagonal one by
   // each sequence's Lk - Lq (added in the kernels).
@@ -160,15 +162,21 @@ mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const vo
     return fail(MSLK_ERR_INVALID_ARG, "%s: q/k/v is null", who);
   if ((sk->h == 0) != (sv->h == 0) && H > 1)
     return fail(MSLK_ERR_INVALID_ARG, "%s: k and v must both or neither use a shared (stride 0) head", who);
-  p.kv_head_shared = H > 1 && sk->h == 0;
+  // K/V heads: Hkv (0: as many as H), or one shared head when the k/v head stride is 0.
+  if (Hkv == 0) Hkv = H;
+  if (H > 1 && sk->h == 0) Hkv = 1;
+  if (Hkv < 1 || H % Hkv)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: K/V heads (%d) must divide the query heads (%d)", who, Hkv, H);
+  p.Hkv = Hkv;
+  p.kv_group = H / Hkv;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v))
     return fail(MSLK_ERR_MISALIGNED, "%s: q/k/v base must be 16-byte aligned", who);
   const int in_mult = 16 / in_bytes;  // elements per 16 bytes
   if (const char* w = check_strides(*sq, B, M, H, in_mult, false))
     return fail(MSLK_ERR_MISALIGNED, "%s: q %s must be a positive multiple of %d elements (16 bytes)", who, w, in_mult);
-  if (const char* w = check_strides(*sk, B, Mkv, H, in_mult, true))
+  if (const char* w = check_strides(*sk, B, Mkv, Hkv, in_mult, true))
     return fail(MSLK_ERR_MISALIGNED, "%s: k %s must be a positive multiple of %d elements (16 bytes)", who, w, in_mult);
-  if (const char* w = check_strides(*sv, B, Mkv, H, in_mult, true))
+  if (const char* w = check_strides(*sv, B, Mkv, Hkv, in_mult, true))
     return fail(MSLK_ERR_MISALIGNED, "%s: v %s must be a positive multiple of %d elements (16 bytes)", who, w, in_mult);
   if (!aligned16(out)) return fail(MSLK_ERR_MISALIGNED, "%s: out base must be 16-byte aligned", who);
   if (const char* w = check_strides(*so, B, M, H, p.out_fp32 ? 4 : 8, false))
@@ -295,6 +303,90 @@ mslk_status apply_lanes(AttnProblem& p, const mslk_kv_lanes* lanes, const char* 
   return ok();
 }
 
+mslk_attn_args make_args(const void* q, const void* k, const void* v, const mslk_strides& sq,
+                         const mslk_strides& sk, const mslk_strides& sv, const mslk_strides& so,
+                         int32_t B, int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv,
+                         float scale, int32_t mask_kind, const mslk_seqlens* seqlens,
+                         const mslk_band* band, void* out, float* lse) {
+  mslk_attn_args a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  a.so = so;
+  a.B = B;
+  a.M = M;
+  a.Mkv = Mkv;
+  a.H = H;
+  a.Hkv = 0;
+  a.K = K;
+  a.Kv = Kv;
+  a.scale = scale;
+  a.mask_kind = mask_kind;
+  a.seqlens = seqlens;
+  a.band = band;
+  a.out = out;
+  a.out_dtype = MSLK_DTYPE_BF16;
+  a.lse = lse;
+  return a;
+}
+
+// Every option of the forward / partial call: validation, then the kernels.
+mslk_status attn_general(const mslk_attn_args& a, cudaStream_t stream, const char* who) {
+  const mslk_fp8_scales* f8 = a.fp8;
+  if (f8 != nullptr) {
+    if (f8->descale_q == nullptr || f8->descale_k == nullptr || f8->descale_v == nullptr)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: descale_q, descale_k and descale_v are required", who);
+    if (f8->per_tensor != 0 && f8->per_tensor != 1)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: scales.per_tensor must be 0 or 1", who);
+    if ((reinterpret_cast<uintptr_t>(f8->descale_q) | reinterpret_cast<uintptr_t>(f8->descale_k) |
+         reinterpret_cast<uintptr_t>(f8->descale_v)) & 3u)
+      return fail(MSLK_ERR_MISALIGNED, "%s: descales must be 4-byte aligned", who);
+  }
+  if (a.partial != 0 && a.partial != 1)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: partial must be 0 or 1", who);
+  if (a.Hkv < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative Hkv", who);
+  mslk_status s = ok();
+  mslk_seqlens sl{};
+  const mslk_seqlens* slp = a.seqlens;
+  if (a.lanes != nullptr) {
+    if (a.partial) return fail(MSLK_ERR_UNSUPPORTED, "%s: key lanes are forward only", who);
+    s = check_lanes(a.lanes, a.mask_kind, who);
+    if (s != MSLK_OK) return s;
+    if (a.B != 1)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: key lanes take packed queries (B = 1), got B = %d", who, a.B);
+    sl = lanes_seqlens(a.seqlens, a.lanes);
+    slp = a.seqlens ? &sl : nullptr;
+  }
+  AttnProblem p;
+  s = validate_attn(p, a.q, a.k, a.v, &a.sq, &a.sk, &a.sv, &a.so, a.B, a.M, a.Mkv, a.H, a.K, a.Kv,
+                    a.scale, a.mask_kind, slp, a.band, a.partial ? a.kv_offset : 0, a.out,
+                    a.out_dtype, a.lse, a.partial == 1, a.partial == 1, who, f8 ? 1 : 2, a.Hkv);
+  if (s != MSLK_OK) return s;
+  if (f8 != nullptr) {
+    p.fp8 = true;
+    p.descale_q = f8->descale_q;
+    p.descale_k = f8->descale_k;
+    p.descale_v = f8->descale_v;
+    p.descale_per_tensor = f8->per_tensor == 1;
+  }
+  if (a.lanes != nullptr) {
+    s = apply_lanes(p, a.lanes, who);
+    if (s != MSLK_OK) return s;
+  }
+  if (p.fp8 && p.B > 0 && p.H > 0 && p.M > 0) {
+    const int rows = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
+    const bool decode = rows <= kDecodeMaxRows && g_path_policy.load() != 1;
+    if (!decode && p.K != 128)
+      return fail(MSLK_ERR_UNSUPPORTED,
+                  "%s: E4M3 inputs with more than %d query rows need head dim 128 (got %d)", who,
+                  kDecodeMaxRows, p.K);
+  }
+  return run_attn(p, stream, who);
+}
+
 }  // namespace
 
 extern "C" {
@@ -354,6 +446,12 @@ mslk_status mslk_attn_partial_band(const void* q, const void* k, const void* v,
   return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_partial_band");
 }
 
+mslk_status mslk_attn(const mslk_attn_args* args, void* stream) {
+  const char* who = "mslk_attn";
+  if (args == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: args is null", who);
+  return attn_general(*args, static_cast<cudaStream_t>(stream), who);
+}
+
 mslk_status mslk_attn_fwd_lanes(const void* q, const void* k, const void* v, const mslk_strides* sq,
                                 const mslk_strides* sk, const mslk_strides* sv, const mslk_strides* so,
                                 int32_t M, int32_t Mkv, int32_t H, int32_t K, int32_t Kv, float scale,
@@ -361,16 +459,13 @@ mslk_status mslk_attn_fwd_lanes(const void* q, const void* k, const void* v, con
                                 const mslk_kv_lanes* lanes, const mslk_band* band, void* out,
                                 float* lse, void* stream) {
   const char* who = "mslk_attn_fwd_lanes";
-  mslk_status s = check_lanes(lanes, mask_kind, who);
-  if (s != MSLK_OK) return s;
-  const mslk_seqlens sl = lanes_seqlens(seqlens, lanes);
-  AttnProblem p;
-  s = validate_attn(p, q, k, v, sq, sk, sv, so, 1, M, Mkv, H, K, Kv, scale, mask_kind,
-                    seqlens ? &sl : nullptr, band, 0, out, MSLK_DTYPE_BF16, lse, false, false, who);
-  if (s != MSLK_OK) return s;
-  s = apply_lanes(p, lanes, who);
-  if (s != MSLK_OK) return s;
-  return run_attn(p, static_cast<cudaStream_t>(stream), who);
+  if (sq == nullptr || sk == nullptr || sv == nullptr || so == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: null strides", who);
+  if (lanes == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: lanes->seqlen_k is required", who);
+  mslk_attn_args a = make_args(q, k, v, *sq, *sk, *sv, *so, 1, M, Mkv, H, K, Kv, scale, mask_kind,
+                               seqlens, band, out, lse);
+  a.lanes = lanes;
+  return attn_general(a, static_cast<cudaStream_t>(stream), who);
 }
 
 mslk_status mslk_attn_fwd_fp8(const void* q, const void* k, const void* v, const mslk_strides* sq,
@@ -380,44 +475,15 @@ mslk_status mslk_attn_fwd_fp8(const void* q, const void* k, const void* v, const
                               const mslk_band* band, const mslk_kv_lanes* lanes,
                               const mslk_fp8_scales* scales, void* out, float* lse, void* stream) {
   const char* who = "mslk_attn_fwd_fp8";
-  if (scales == nullptr || scales->descale_q == nullptr || scales->descale_k == nullptr ||
-      scales->descale_v == nullptr)
+  if (scales == nullptr)
     return fail(MSLK_ERR_INVALID_ARG, "%s: descale_q, descale_k and descale_v are required", who);
-  if (scales->per_tensor != 0 && scales->per_tensor != 1)
-    return fail(MSLK_ERR_INVALID_ARG, "%s: scales.per_tensor must be 0 or 1", who);
-  if ((reinterpret_cast<uintptr_t>(scales->descale_q) | reinterpret_cast<uintptr_t>(scales->descale_k) |
-       reinterpret_cast<uintptr_t>(scales->descale_v)) & 3u)
-    return fail(MSLK_ERR_MISALIGNED, "%s: descales must be 4-byte aligned", who);
-  mslk_status s = ok();
-  mslk_seqlens sl{};
-  if (lanes != nullptr) {
-    s = check_lanes(lanes, mask_kind, who);
-    if (s != MSLK_OK) return s;
-    if (B != 1) return fail(MSLK_ERR_INVALID_ARG, "%s: key lanes take packed queries (B = 1), got B = %d", who, B);
-    sl = lanes_seqlens(seqlens, lanes);
-  } else if (seqlens != nullptr) {
-    sl = *seqlens;
-  }
-  AttnProblem p;
-  s = validate_attn(p, q, k, v, sq, sk, sv, so, B, M, Mkv, H, K, Kv, scale, mask_kind,
-                    seqlens ? &sl : nullptr, band, 0, out, MSLK_DTYPE_BF16, lse, false, false, who, 1);
-  if (s != MSLK_OK) return s;
-  p.fp8 = true;
-  p.descale_q = scales->descale_q;
-  p.descale_k = scales->descale_k;
-  p.descale_v = scales->descale_v;
-  p.descale_per_tensor = scales->per_tensor == 1;
-  if (lanes != nullptr) {
-    s = apply_lanes(p, lanes, who);
-    if (s != MSLK_OK) return s;
-  }
-  const int rows = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
-  const bool decode = rows <= kDecodeMaxRows && g_path_policy.load() != 1;
-  if (!decode && K != 128 && p.B > 0 && p.H > 0 && p.M > 0)
-    return fail(MSLK_ERR_UNSUPPORTED,
-                "%s: E4M3 inputs with more than %d query rows need head dim 128 (got %d)", who,
-                kDecodeMaxRows, K);
-  return run_attn(p, static_cast<cudaStream_t>(stream), who);
+  if (sq == nullptr || sk == nullptr || sv == nullptr || so == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: null strides", who);
+  mslk_attn_args a = make_args(q, k, v, *sq, *sk, *sv, *so, B, M, Mkv, H, K, Kv, scale, mask_kind,
+                               seqlens, band, out, lse);
+  a.lanes = lanes;
+  a.fp8 = scales;
+  return attn_general(a, static_cast<cudaStream_t>(stream), who);
 }
 
 mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split, int32_t n_chunks,

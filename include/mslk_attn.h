@@ -253,6 +253,41 @@ mslk_status mslk_attn_fwd_fp8(const void* q, const void* k, const void* v,
                               void* stream);
 
 /*
+ * Every option of the forward and partial calls in one argument struct (read during the
+ * call), for callers that need a combination the calls above do not take — in particular
+ * grouped-query attention (Hkv K/V heads for H query heads).
+ *   Hkv        K/V heads: 0 means H; otherwise Hkv divides H and query head h reads K/V
+ *              head h / (H / Hkv) (the pages' BMGHK layout flattened group-major,
+ *              bmghk2bmhk).  A k/v head stride of 0 still means one shared head.
+ *   seqlens, band, lanes, fp8   as in the calls above (each may be NULL).
+ *   partial    0: forward (mslk_attn_fwd*); 1: one K/V chunk (mslk_attn_partial*): lse
+ *              required, kv_offset read, no bottom-right alignment, no key lanes.
+ *   out_dtype  MSLK_DTYPE_BF16 or MSLK_DTYPE_FP32 for either mode.
+ * Few query rows with a group ratio r > 1 fold up to 8 / rows query heads of a K/V head
+ * into one block of rows, so that head's keys and values are streamed once for them.
+ */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  mslk_strides sq, sk, sv, so;
+  int32_t B, M, Mkv, H, Hkv, K, Kv;
+  float scale;
+  int32_t mask_kind;
+  const mslk_seqlens* seqlens;
+  const mslk_band* band;
+  const mslk_kv_lanes* lanes;
+  const mslk_fp8_scales* fp8;
+  int32_t partial;
+  int64_t kv_offset;
+  void* out;
+  int32_t out_dtype;
+  float* lse;
+} mslk_attn_args;
+
+mslk_status mslk_attn(const mslk_attn_args* args, void* stream);
+
+/*
  * mslk_merge_attentions — exact log-sum-exp merge of n chunk results into preallocated
  * outputs.  MSLK kernel reference, "Attention - Core fMHA" > merge_attentions (exact
  * normalised output over the union of chunks, not an average; write_lse; output_dtype)

@@ -276,3 +276,80 @@ def test_fp8_pass_validation(lib):
                     sl=_capi.Seqlens(FAKE, None, 4, 16, 64))):
         st, why = _fp8_call(lib, **kw)
         assert st == _capi.MSLK_ERR_CUDA, why
+
+
+def test_attn_args_layout_matches_header(tmp_path):
+    """The ctypes mirror of mslk_attn_args has the C struct's size and field offsets."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f for f, _ in _capi.AttnArgs._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "mslk_attn.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(mslk_attn_args));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(mslk_attn_args, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [ctypes.sizeof(_capi.AttnArgs)] + [getattr(_capi.AttnArgs, f).offset for f in fields]
+    assert got == want
+
+
+def _args(**kw):
+    s = S(8 * 128 * 64, 8 * 128, 128)
+    a = _capi.AttnArgs()
+    a.q = a.k = a.v = a.out = a.lse = FAKE
+    a.sq = a.sk = a.sv = a.so = s
+    a.B, a.M, a.Mkv, a.H, a.Hkv, a.K, a.Kv = 2, 64, 64, 8, 0, 128, 128
+    for k_, v_ in kw.items():
+        setattr(a, k_, v_)
+    return a
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(Hkv=3), _capi.MSLK_ERR_INVALID_ARG, "divide"),
+    (dict(Hkv=-1), _capi.MSLK_ERR_INVALID_ARG, "negative Hkv"),
+    (dict(partial=2), _capi.MSLK_ERR_INVALID_ARG, "partial"),
+    (dict(partial=1, lse=None), _capi.MSLK_ERR_INVALID_ARG, "lse is required"),
+    (dict(out_dtype=7), _capi.MSLK_ERR_INVALID_ARG, "out_dtype"),
+])
+def test_general_entry_rejects(lib, kw, status, needle):
+    a = _args(**kw)
+    st = lib.mslk_attn(ctypes.byref(a), None)
+    why = lib.mslk_last_error().decode()
+    assert st == status, why
+    assert needle in why
+
+
+def test_general_entry_rejects_lanes_partial_and_null(lib):
+    lanes = L(FAKE, FAKE, None, 0, 0)
+    sl = _capi.Seqlens(FAKE, None, 2, 32, 64)
+    a = _args(partial=1, B=1, mask_kind=3, lanes=ctypes.addressof(lanes), seqlens=ctypes.addressof(sl))
+    assert lib.mslk_attn(ctypes.byref(a), None) == _capi.MSLK_ERR_UNSUPPORTED
+    assert lib.mslk_attn(None, None) == _capi.MSLK_ERR_INVALID_ARG
+
+
+def test_general_entry_passes_validation(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for kw in (dict(), dict(Hkv=2), dict(Hkv=8, partial=1, out_dtype=1), dict(Hkv=1, M=4)):
+        a = _args(**kw)
+        st = lib.mslk_attn(ctypes.byref(a), None)
+        assert st == _capi.MSLK_ERR_CUDA, lib.mslk_last_error().decode()
+
+
+def test_binding_checks_kv_heads():
+    import torch
+    from attention_fmha_fwd_gb300 import api
+    q = torch.empty(2, 5, 8, 64)
+    assert api._kv_heads(q, torch.empty(2, 7, 2, 64), torch.empty(2, 7, 2, 64)) == 2
+    for k, v in ((torch.empty(2, 7, 3, 64), torch.empty(2, 7, 3, 64)),   # 3 does not divide 8
+                 (torch.empty(2, 7, 2, 64), torch.empty(2, 6, 2, 64)),   # key counts differ
+                 (torch.empty(1, 7, 2, 64), torch.empty(1, 7, 2, 64)),   # batch differs
+                 (torch.empty(2, 7, 2, 32), torch.empty(2, 7, 2, 32))):  # head dim differs
+        with pytest.raises(ValueError):
+            api._kv_heads(q, k, v)
