@@ -626,6 +626,19 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
                                                 "frac_hbm": b_f8 / t_f8 / 1e9 / peaks["hbm_gbs"],
                                                 "speedup_vs_bf16": t_one / t_f8, "launches": 1}
     del k8, v8
+    # grouped-query decode: 32 query heads on the same 8 K/V heads (group 4), one launch;
+    # each K/V head is streamed once for its 4 query heads
+    qg = torch.randn((w.B, 1, 32, w.K), device=dev).to(torch.bfloat16)
+    og = torch.empty((w.B, 1, 32, w.Kv), dtype=torch.float32, device=dev)
+    lg = torch.empty((w.B, 32, 1), dtype=torch.float32, device=dev)
+    gqa = lambda: fa.attn_partial(qg, kd, vd, scale=w.scale, out=og, lse=lg)  # noqa: E731
+    for _ in range(3):
+        gqa()
+    t_g = _time_it(gqa, 10, stream, flush)
+    res["decode_gqa_16x32768_32q_8kv"] = {"us": t_g * 1e6, "GB/s": kv_bytes / t_g / 1e9,
+                                          "frac_hbm": kv_bytes / t_g / 1e9 / peaks["hbm_gbs"],
+                                          "query_heads_per_kv_head": 4, "launches": 1}
+    del qg
     del kd, vd, k, v
     # varlen packed block-diagonal causal
     w = inputs.WORKLOADS["varlen_packed"]
