@@ -120,6 +120,11 @@ struct TcArgs {
   long long so_b, so_m, so_h;
   float* lse;
   int tma_store;    // 1: write output tiles through shared memory with TMA stores
+  // Folded query heads (fold = r > 1): one query position per batch / packed sequence, and
+  // the unit's rows are the r query heads of K/V head h (q/out tensor maps are views of r
+  // rows x H/r heads); every row sits at query position 0.
+  int fold;
+  long long lse_sb, lse_sh, lse_sm;  // lse element of (Q/O batch coordinate, head, row)
   // E4M3 inputs: element x of head h stands for x * descale[h] (descale[0] when
   // desc_per_tensor); q and k descales fold into the score scale, v's into the output.
   const float* dq;
@@ -215,6 +220,7 @@ MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32
 // One work unit: 256 query rows of one (batch or packed sequence, head).
 struct Unit {
   int b, h, hk, z;
+  int qb;  // batch coordinate of the unit's Q/O rows (a packed row when folded and varlen)
   int q_base, Lq, k_base, Lk;
   int r0;
   int lo, hi;  // the band of this unit's sequence (see TcArgs), clamped to +-2^30
@@ -265,12 +271,21 @@ MSLK_DEV bool decode_unit(const TcArgs& a, int i, Unit& u) {
     u.k_base = 0;
     u.Lk = a.Mkv;
   }
+  u.qb = u.b;
+  int lq_pos = u.Lq;  // query positions of the block (1 when heads are folded into rows)
+  if (a.fold) {
+    if (u.Lq <= 0) return false;  // a packed sequence without a query
+    u.qb = a.varlen ? u.q_base : z;
+    u.q_base = 0;
+    u.Lq = a.fold;
+    lq_pos = 1;
+  }
   u.r0 = unit_m * kUnitRows;
-  if (u.r0 >= u.Lq) return false;
+  if (u.r0 < 0 || u.r0 >= u.Lq) return false;  // (a unit index past the unit space)
   {
     long long lo = a.lo, hi = a.hi;
     if (a.band_seq) {
-      const long long shift = static_cast<long long>(u.Lk) - u.Lq;
+      const long long shift = static_cast<long long>(u.Lk) - lq_pos;
       if (lo > -kBandOpen) lo += shift;
       if (hi < kBandOpen) hi += shift;
     }
@@ -285,8 +300,9 @@ MSLK_DEV bool decode_unit(const TcArgs& a, int i, Unit& u) {
     u.tlo[t] = u.thi[t] = 0;
     if (row0 >= u.Lq) continue;  // rows past the sequence: nothing to compute
     const long long row1 = min(row0 + kBlockM, static_cast<long long>(u.Lq)) - 1;
-    const long long k_first = max(0LL, row0 + u.lo);
-    const long long k_last = min(static_cast<long long>(u.Lk) - 1, row1 + u.hi);
+    const long long p0 = a.fold ? 0 : row0, p1 = a.fold ? 0 : row1;  // query positions
+    const long long k_first = max(0LL, p0 + u.lo);
+    const long long k_last = min(static_cast<long long>(u.Lk) - 1, p1 + u.hi);
     if (k_first > k_last) continue;
     u.tlo[t] = static_cast<int>(k_first / kBlockN);
     u.thi[t] = static_cast<int>(k_last / kBlockN) + 1;
@@ -391,7 +407,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       mbar_arrive_expect_tx_elect(q_full(t), L::kTileBytes);
       for (int kb = 0; kb < L::kKBlocks; ++kb)
         tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, q_full(t), kb * (128 / L::kEsz),
-                          u.q_base + u.r0 + t * kBlockM, u.h, u.b);
+                          u.q_base + u.r0 + t * kBlockM, u.h, u.qb);
       ++q_issued[t];
     };
     auto load_kv = [&](int j, int which, const Unit& u) {  // K_j (which = 0) or V_j
@@ -591,20 +607,23 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       const int tlo_t = t == 0 ? u.tlo[0] : u.tlo[1];
       const int n_t = (t == 0 ? u.thi[0] : u.thi[1]) - tlo_t;
       float sl2 = a.scale_log2;
-      if constexpr (F8) sl2 *= a.dq[a.desc_per_tensor ? 0 : u.h] * a.dk[a.desc_per_tensor ? 0 : u.hk];
+      if constexpr (F8) {
+        const int hq = a.fold ? u.h * a.fold + min(r, a.fold - 1) : u.h;  // this row's query head
+        sl2 *= a.dq[a.desc_per_tensor ? 0 : hq] * a.dk[a.desc_per_tensor ? 0 : u.hk];
+      }
       if (n_t <= 0) {  // no allowed key for any row of this Q tile
         if (valid) {
           for (int c = 0; c < D; c += 4) {
             if (a.out_fp32) {
-              float* o = static_cast<float*>(a.out) + u.b * a.so_b + row * a.so_m + u.h * a.so_h + c;
+              float* o = static_cast<float*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + c;
               *reinterpret_cast<float4*>(o) = make_float4(0.f, 0.f, 0.f, 0.f);
             } else {
               __nv_bfloat16* o =
-                  static_cast<__nv_bfloat16*>(a.out) + u.b * a.so_b + row * a.so_m + u.h * a.so_h + c;
+                  static_cast<__nv_bfloat16*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + c;
               *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
             }
           }
-          if (a.lse != nullptr) a.lse[(static_cast<long long>(u.b) * a.H + u.h) * a.M + row] = -INFINITY;
+          if (a.lse != nullptr) a.lse[u.qb * a.lse_sb + u.h * a.lse_sh + row * a.lse_sm] = -INFINITY;
         }
         continue;
       }
@@ -621,13 +640,17 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         // the first row's upper band edge and its first key is within the last row's lower
         // edge; otherwise column c is allowed iff lim_lo <= c <= lim_c (this row's band
         // edges, and key < Lk).
+        // (query positions: the row's own, or 0 for every row when heads are folded)
+        const int pos_first = a.fold ? 0 : row_first;
+        const int pos_last = a.fold ? 0 : row_first + kBlockM - 1;
+        const int pos = a.fold ? 0 : r;
         const bool need_mask = (key0 + kBlockN > u.Lk) ||
-                               (key0 + kBlockN - 1 > row_first + u.hi) ||
-                               (kLowerEdge && key0 < row_first + kBlockM - 1 + u.lo);
+                               (key0 + kBlockN - 1 > pos_first + u.hi) ||
+                               (kLowerEdge && key0 < pos_last + u.lo);
         int lim_c = kBlockN - 1, lim_lo = 0;
         if (need_mask) {
-          lim_c = max(-1, min(min(u.Lk - 1, r + u.hi) - key0, kBlockN - 1));
-          if constexpr (kLowerEdge) lim_lo = max(0, min(max(0, r + u.lo) - key0, kBlockN));
+          lim_c = max(-1, min(min(u.Lk - 1, pos + u.hi) - key0, kBlockN - 1));
+          if constexpr (kLowerEdge) lim_lo = max(0, min(max(0, pos + u.lo) - key0, kBlockN));
         }
         // The whole S row comes out of tensor memory in one load (128 registers): mask it
         // (only tiles crossing a mask limit), take the row max, then form
@@ -734,7 +757,8 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       // Output tiles go through this warpgroup's staging buffer and one TMA store per
       // 128-byte column band, except the tail tile of a packed sequence (a whole 128-row
       // box would spill into the next sequence), which is stored row by row.
-      const bool use_tma = a.tma_store && !(a.varlen && row_first + kBlockM > u.Lq);
+      // (folded rows: the view's row extent is r, so a 128-row box is clipped there)
+      const bool use_tma = a.tma_store && (a.fold || !(a.varlen && row_first + kBlockM > u.Lq));
       const bool leader = (warp % 4) == 0 && lane == 0;
       uint8_t* stage = smem + L::kOutOff + t * L::kStageOutBytes + row_in_tile * 128;
       const uint32_t stage_base = s_base + L::kOutOff + t * L::kStageOutBytes;
@@ -762,11 +786,11 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
             fence_proxy_async_smem();
             named_bar_sync(1 + t, kBlockM);
             if (leader) {
-              tma_store_4d(&tm_o, stage_base, band * 32, u.q_base + row_first, u.h, u.b);
+              tma_store_4d(&tm_o, stage_base, band * 32, u.q_base + row_first, u.h, u.qb);
               bulk_commit();
             }
           } else if (valid) {
-            float* op = static_cast<float*>(a.out) + u.b * a.so_b + row * a.so_m + u.h * a.so_h + band * 32;
+            float* op = static_cast<float*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + band * 32;
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
               *reinterpret_cast<float4*>(op + c) =
@@ -802,12 +826,12 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
             fence_proxy_async_smem();
             named_bar_sync(1 + t, kBlockM);
             if (leader) {
-              tma_store_4d(&tm_o, stage_base, band * 64, u.q_base + row_first, u.h, u.b);
+              tma_store_4d(&tm_o, stage_base, band * 64, u.q_base + row_first, u.h, u.qb);
               bulk_commit();
             }
           } else if (valid) {
             __nv_bfloat16* op =
-                static_cast<__nv_bfloat16*>(a.out) + u.b * a.so_b + row * a.so_m + u.h * a.so_h + band * 64;
+                static_cast<__nv_bfloat16*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + band * 64;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) *reinterpret_cast<uint4*>(op + ch * 8) = w[ch];
           }
@@ -815,7 +839,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       }
       if (valid) {
         if (a.lse != nullptr)
-          a.lse[(static_cast<long long>(u.b) * a.H + u.h) * a.M + row] =
+          a.lse[u.qb * a.lse_sb + u.h * a.lse_sh + row * a.lse_sm] =
               (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
       }
       ++uc;
@@ -940,8 +964,17 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
     return cudaErrorNotSupported;
   }
   const long long hk = p.Hkv;
+  const bool varlen = is_blockdiag(p.mask_kind);
+  // Folded heads: q and out as [batch or packed row][r rows (head stride)][H / r heads].
+  const int R = p.fold;
+  const long long q_rows = R ? R : p.M, q_heads = R ? p.Hkv : p.H;
+  const long long q_batch = R ? (varlen ? p.M : p.B) : p.B;
+  const long long sq_m = R ? p.sq.h : p.sq.m, sq_h = R ? R * p.sq.h : p.sq.h;
+  const long long sq_b = R ? (varlen ? p.sq.m : p.sq.b) : p.sq.b;
+  const long long so_m = R ? p.so.h : p.so.m, so_h = R ? R * p.so.h : p.so.h;
+  const long long so_b = R ? (varlen ? p.so.m : p.so.b) : p.so.b;
   CUtensorMap tq, tk, tv;
-  if (!encode_bhmd(enc, &tq, p.q, D, p.M, p.H, p.B, p.sq.m, p.sq.h, p.sq.b, F8) ||
+  if (!encode_bhmd(enc, &tq, p.q, D, q_rows, q_heads, q_batch, sq_m, sq_h, sq_b, F8) ||
       !encode_bhmd(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, F8) ||
       !encode_bhmd(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, F8)) {
     *why = "cuTensorMapEncodeTiled rejected a q/k/v layout";
@@ -949,12 +982,24 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   }
   // Output tiles: bands of 128 bytes (64 bf16 / 32 fp32 columns) x 128 rows.
   CUtensorMap to{};
-  const bool tma_store = encode_out(enc, &to, p.out, p.out_fp32, D, p.M, p.H, p.B, p.so.m, p.so.h, p.so.b);
+  const bool tma_store =
+      encode_out(enc, &to, p.out, p.out_fp32, D, q_rows, q_heads, q_batch, so_m, so_h, so_b);
   TcArgs a{};
+  a.fold = R;
+  if (R) {
+    // lse [B, H, 1] (dense) or [1, H, total_q] (packed): query head = K/V head * r + row
+    a.lse_sb = varlen ? 1 : p.H;
+    a.lse_sh = varlen ? static_cast<long long>(R) * p.M : R;
+    a.lse_sm = varlen ? p.M : 1;
+  } else {
+    a.lse_sb = static_cast<long long>(p.H) * p.M;
+    a.lse_sh = p.M;
+    a.lse_sm = 1;
+  }
   a.M = p.M;
   a.Mkv = p.Mkv;
-  a.H = p.H;
-  a.kv_group = p.kv_group;
+  a.H = R ? p.Hkv : p.H;
+  a.kv_group = R ? 1 : p.kv_group;
   a.lo = p.band_lo <= -kBandOpen ? -kBandOpen : p.band_lo - p.kv_offset;
   a.hi = p.band_hi >= kBandOpen ? kBandOpen : p.band_hi - p.kv_offset;
   a.band_seq = p.band_seq_shift ? 1 : 0;
@@ -965,16 +1010,16 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.page_size = p.page_size;
   a.max_pages = p.max_pages;
   a.varlen = is_blockdiag(p.mask_kind) ? 1 : 0;
-  const int rows = a.varlen ? p.max_seqlen_q : p.M;
+  const int rows = R ? R : (a.varlen ? p.max_seqlen_q : p.M);
   a.units_m = (rows + kUnitRows - 1) / kUnitRows;
   a.scale_log2 = p.scale * kLog2e;
   a.cu_q = p.cu_q;
   a.cu_k = p.cu_k;
   a.out = p.out;
   a.out_fp32 = p.out_fp32 ? 1 : 0;
-  a.so_b = p.so.b;
-  a.so_m = p.so.m;
-  a.so_h = p.so.h;
+  a.so_b = so_b;
+  a.so_m = so_m;
+  a.so_h = so_h;
   a.lse = p.lse;
   a.tma_store = tma_store ? 1 : 0;
   a.dq = p.descale_q;
@@ -984,7 +1029,7 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.err = ctl.err;
   a.timeout_ns = ctl.timeout_ns;
   a.Z = a.varlen ? p.n_seqs : p.B;
-  const long long total = static_cast<long long>(a.units_m) * p.H * a.Z;
+  const long long total = static_cast<long long>(a.units_m) * a.H * a.Z;  // the kernel's head count
   if (total == 0) return cudaSuccess;
   if (total > 0x7fffffffLL) {
     *why = "too many work units";

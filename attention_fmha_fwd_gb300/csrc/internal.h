@@ -47,6 +47,9 @@ struct AttnProblem {
   // K/V heads: query head h reads K/V head h / kv_group (kv_group = H / Hkv).  A k/v head
   // stride of 0 is one shared head (Hkv = 1).
   int Hkv, kv_group;
+  // > 1: one query position per batch / packed sequence, run on the tensor cores with the
+  // kv_group query heads of a K/V head as the rows of one unit (set by the dispatcher).
+  int fold;
 };
 
 struct MergeProblem {
@@ -86,6 +89,11 @@ constexpr int64_t kBandOpen = int64_t(1) << 40;
 
 // Largest query-row count the CUDA-core decode kernel takes.
 constexpr int kDecodeMaxRows = 8;
+// Folded grouped heads on the tensor cores: at most one 256-row unit of heads, and at
+// least this many (batch or sequence, K/V head) units (below it the CUDA-core kernel,
+// which splits keys over thread-block clusters, fills the SMs better).
+constexpr int kFoldMaxRows = 256;
+constexpr long long kFoldMinUnits = 64;
 
 // Tensor-core (tcgen05) forward/partial kernel.  `why` receives a reason on failure.
 cudaError_t launch_fmha_tc(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,

@@ -238,11 +238,22 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   const DeviceCtl ctl = device_ctl();
   if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "%s: no CUDA device / module", who);
   const int policy = g_path_policy.load();
-  const bool decode_ok = is_blockdiag(p.mask_kind) ? p.max_seqlen_q <= kDecodeMaxRows
-                                                   : p.M <= kDecodeMaxRows;
+  const int rows_q = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
+  const bool decode_ok = rows_q <= kDecodeMaxRows;
   cudaError_t e;
   const char* why = "launch failed";
-  if (decode_ok && policy != 1) {
+  // Grouped heads with one query position per batch / sequence: the tensor cores take the
+  // group's query heads as the rows of one unit and stream each K/V head once at the
+  // memory rate (the CUDA-core kernel's cost grows with the rows), when there are enough
+  // (batch, K/V head) units to fill the SMs.
+  const long long fold_units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.Hkv;
+  const bool fold = p.kv_group > 1 && rows_q == 1 && p.kv_group <= kFoldMaxRows &&
+                    (!p.fp8 || p.K == 128) && (policy == 1 || fold_units >= kFoldMinUnits);
+  if (fold) {
+    AttnProblem f = p;
+    f.fold = p.kv_group;
+    e = launch_fmha_tc(f, ctl, stream, &why);
+  } else if (decode_ok && policy != 1) {
     e = launch_fmha_decode(p, ctl, stream, &why);
   } else {
     e = launch_fmha_tc(p, ctl, stream, &why);

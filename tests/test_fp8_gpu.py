@@ -71,7 +71,7 @@ def _p_rounding_check(out, ref, q, k, v, scale, kind, what, cu_q=None, cu_k=None
     model_var = np.zeros_like(ref)
     for b in range(B):
         for h in range(H):
-            hk = 0 if k.shape[2] == 1 else h
+            hk = h // (H // k.shape[2])  # grouped K/V heads
             x = s64 * (q[b, :, h] @ k[b, :, hk].T) + bias
             rows = allowed.any(axis=1)
             mx = np.where(rows, np.max(np.where(allowed, x, -np.inf), axis=1), 0.0)
