@@ -226,6 +226,20 @@ DeviceCtl device_ctl() {
   return DeviceCtl{error_word_ptr(), static_cast<unsigned long long>(g_timeout_ns.load())};
 }
 
+// Few query rows: the CUDA-core kernel splits each head's keys over a thread-block cluster
+// but its work grows with the rows; the tensor-core kernel pays the same per key tile for 1
+// to 128 rows but streams one (batch, head) unit per CTA.  Rates measured on GB300 (keys
+// per second): tensor cores min(memory rate, ~1e8 per unit); CUDA cores min(memory rate,
+// ~1.9e10 / rows) — e.g. 16 x 8 heads x 32768 keys at 8 rows: 351 vs 1817 us, at 4 x 8
+// heads: 339 vs 472 us; at 1 row the CUDA cores are always ahead.
+bool few_rows_prefer_tensor_cores(int rows, long long units, int K, bool fp8) {
+  if (rows < 2 || (fp8 && K != 128)) return false;
+  const double bytes_per_key = 4.0 * K;  // k + v, bf16 (E4M3 halves both rates alike)
+  const double tc = std::min(6.2e12 / bytes_per_key, static_cast<double>(units) * 1.0e8);
+  const double cc = std::min(6.6e12 / bytes_per_key, 1.9e10 / rows);
+  return tc > 1.05 * cc;
+}
+
 mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who) {
   if (p.B == 0 || p.H == 0 || p.M == 0) return ok();
   if (p.Mkv == 0) {
@@ -239,7 +253,9 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "%s: no CUDA device / module", who);
   const int policy = g_path_policy.load();
   const int rows_q = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
-  const bool decode_ok = rows_q <= kDecodeMaxRows;
+  const long long units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.H;
+  const bool decode_ok = rows_q <= kDecodeMaxRows &&
+                         (policy == 2 || !few_rows_prefer_tensor_cores(rows_q, units, p.K, p.fp8));
   cudaError_t e;
   const char* why = "launch failed";
   // Grouped heads with one query position per batch / sequence: the tensor cores take the
@@ -248,7 +264,8 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   // (batch, K/V head) units to fill the SMs.
   const long long fold_units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.Hkv;
   const bool fold = p.kv_group > 1 && rows_q == 1 && p.kv_group <= kFoldMaxRows &&
-                    (!p.fp8 || p.K == 128) && (policy == 1 || fold_units >= kFoldMinUnits);
+                    (!p.fp8 || p.K == 128) && policy != 2 &&
+                    (policy == 1 || fold_units >= kFoldMinUnits);
   if (fold) {
     AttnProblem f = p;
     f.fold = p.kv_group;

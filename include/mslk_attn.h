@@ -340,10 +340,13 @@ void mslk_set_wait_timeout_ns(int64_t ns);
 mslk_status mslk_diag_bounded_wait(void* stream);
 
 /*
- * Kernel choice, process-wide: 0 automatic (default: the CUDA-core decode kernel for
- * M <= 8 with dense masks, the tensor-core kernel otherwise), 1 always the tensor-core
- * kernel, 2 same as 0.  Both kernels compute the same function; tests use this to run
- * one problem through both.
+ * Kernel choice, process-wide: 0 automatic (default: for at most 8 query rows per batch
+ * or packed sequence, the CUDA-core kernel unless a measured rate model says the
+ * tensor-core kernel streams the keys faster — more rows and enough (batch, head) units;
+ * grouped heads with one query position go to the tensor cores with enough units; the
+ * tensor-core kernel otherwise), 1 always the tensor-core kernel, 2 the CUDA-core kernel
+ * wherever it applies (at most 8 query rows).  All choices compute the same function;
+ * tests use this to run one problem through each kernel.
  */
 void mslk_set_path_policy(int32_t policy);
 

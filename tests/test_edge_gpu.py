@@ -101,3 +101,20 @@ def test_odd_unit_counts(B, M, Mkv, H, D, mask):
     out, lse = _run(q, k, v, s, mask)
     ro, rl = oracle.attention(f32(q), f32(k), f32(v), s, KIND[mask])
     compare(out, lse, ro, rl, f"B{B} M{M} Mkv{Mkv} H{H} D{D} {mask}")
+
+
+@pytest.mark.parametrize("M,policy", [(4, 0), (4, 2), (8, 0), (2, 0)])
+def test_few_rows_many_heads_dispatch(M, policy):
+    """Few query rows over 16 x 8 (batch, head) units: the automatic choice sends 2+ rows to
+    the tensor cores (policy 0), policy 2 keeps the CUDA-core kernel; both match the oracle."""
+    B, Mkv, H, D = 16, 3000, 8, 128
+    q, k, v = inputs.qkv(B, M, Mkv, H, D, seed=M + 100)
+    s = D ** -0.5
+    fa.set_path_policy(policy)
+    try:
+        out, lse = fa.attn_fwd(*to_dev(q, k, v), mask="causal", scale=s, bottom_right=True)
+        torch.cuda.synchronize()
+    finally:
+        fa.set_path_policy(0)
+    ro, rl = oracle.attention(f32(q), f32(k), f32(v), s, oracle.MASK_CAUSAL, bottom_right=True)
+    compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"M{M} policy{policy}")
