@@ -234,7 +234,7 @@ DeviceCtl device_ctl() {
 // heads: 339 vs 472 us; at 1 row the CUDA cores are always ahead.
 bool few_rows_prefer_tensor_cores(int rows, long long units, int K, bool fp8) {
   if (rows < 2 || (fp8 && K != 128)) return false;
-  const double bytes_per_key = 4.0 * K;  // k + v, bf16 (E4M3 halves both rates alike)
+  const double bytes_per_key = (fp8 ? 2.0 : 4.0) * K;  // k + v
   const double tc = std::min(6.2e12 / bytes_per_key, static_cast<double>(units) * 1.0e8);
   const double cc = std::min(6.6e12 / bytes_per_key, 1.9e10 / rows);
   return tc > 1.05 * cc;
