@@ -1,13 +1,13 @@
-// fmha_decode.cu — attention forward / partial for a handful of query rows (M <= 8)
-// with dense masks, on the CUDA cores.
+// fmha_decode.cu — attention forward / partial for a handful of query rows (at most 8 per
+// batch or packed sequence), on the CUDA cores.
 //
 // With one query row per head each K/V element is used once, so the work is a stream
 // of K and V from HBM (about 1 FLOP per byte); tensor-core tiles would be 128-fold
 // padding.  The keys of one (batch, head) are split over a thread-block cluster of CS
 // CTAs (CS = 1..16, above 8 only where the device schedules it, chosen from how many such
 // clusters stay resident, to minimise waves x keys per CTA); inside a CTA one
-// producer warp streams tiles of T keys (T * D = 4096 elements: 8 KiB of K plus 8 KiB of
-// V) through a ring of shared-memory stages with TMA, so up to 192 KiB per SM are in
+// producer warp streams tiles of T keys (8 KiB of K plus 8 KiB of V: T = 4096 / D bf16 or
+// 8192 / D E4M3 keys) through a ring of shared-memory stages with TMA, so up to 192 KiB per SM are in
 // flight whatever the register budget.  Eight consumer warps take the tiles round robin.  Lane l holds
 // head-dim elements [l*V, l*V+V) of every row (V = D/32) and reads them from shared
 // memory (one 256/128-byte row per warp instruction); a halving butterfly leaves key l's
@@ -19,6 +19,15 @@
 // Semantics follow MSLK's memory_efficient_attention / _partial ("Attention - Core
 // fMHA"): out = softmax(scale q.k^T + mask) v over the allowed keys; lse = ln sum exp;
 // rows without an allowed key get out = 0, lse = -inf.
+//
+// Modes: dense batches or packed sequences (grid row = sequence: its queries from
+// cu_seqlens_q, its keys from cu_seqlens_k or a key lane, padded or paged through an
+// incremental page cursor); every mask as a band on key - row with a per-sequence
+// bottom-right shift; grouped K/V heads, with up to 8 / rows query heads of a K/V head
+// folded into one CTA's rows (each row's query position in shared memory); E4M3 inputs
+// (fmha_decode_fp8_kernel: 8 KiB tiles hold twice the keys, products by f32-accumulating
+// mixed-precision FMAs on exact f16 values, probabilities rounded to f16 for P.V).
+// Tiles of 64 or more keys are folded 32 + 32 keys per step.
 
 #include <cuda_bf16.h>
 

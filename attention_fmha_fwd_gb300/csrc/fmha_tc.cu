@@ -42,6 +42,20 @@
 //
 // Every mbarrier wait is bounded (globaltimer); a timeout sets the device error word,
 // raises a CTA-wide abort flag, drains in-flight copies/MMAs and returns.
+//
+// Variants and modes:
+//  * masks are one band lo <= key - row <= hi (causal, windows, bottom-right, kv_offset);
+//    a unit only streams key tiles inside its rows' band; kLowerEdge compiles the lower
+//    edge check in (windows);
+//  * packed sequences (cu_seqlens) and key lanes (padded starts or a page table): a unit's
+//    rows and keys come from its sequence; the V rows past a lane's end in its last tile
+//    are zeroed in shared memory before the PV MMA (an unwritten cache tail may be NaN);
+//  * grouped K/V heads: query head h reads K/V head h / kv_group;
+//  * folded heads (fold = r): one query position per batch / sequence, the unit's rows are
+//    the r query heads of one K/V head (q/out tensor maps are views), all at position 0;
+//  * E4M3 inputs (fmha_tc_fp8_kernel, head dim 128): kind::f8f6f4 MMAs, one 128-byte
+//    swizzle atom per row, E4M3 probabilities four per TMEM column, descales folded into
+//    the exponent scale (q, k) and the output normalisation (v).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
