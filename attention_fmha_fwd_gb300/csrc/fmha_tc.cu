@@ -138,7 +138,10 @@ struct TcArgs {
   // the unit's rows are the r query heads of K/V head h (q/out tensor maps are views of r
   // rows x H/r heads); every row sits at query position 0.
   int fold;
-  long long lse_sb, lse_sh, lse_sm;  // lse element of (Q/O batch coordinate, head, row)
+  long long lse_sb, lse_sh, lse_sm;
+  // Output columns written: D, or the true head dim when a narrower one runs zero-padded
+  // (E4M3 head dim 64 on the 128-wide kernel: the tensor maps zero-fill columns 64..127).
+  int d_out;  // lse element of (Q/O batch coordinate, head, row)
   // E4M3 inputs: element x of head h stands for x * descale[h] (descale[0] when
   // desc_per_tensor); q and k descales fold into the score scale, v's into the output.
   const float* dq;
@@ -627,7 +630,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       }
       if (n_t <= 0) {  // no allowed key for any row of this Q tile
         if (valid) {
-          for (int c = 0; c < D; c += 4) {
+          for (int c = 0; c < a.d_out; c += 4) {
             if (a.out_fp32) {
               float* o = static_cast<float*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + c;
               *reinterpret_cast<float4*>(o) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -778,11 +781,12 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       const uint32_t stage_base = s_base + L::kOutOff + t * L::kStageOutBytes;
       if (a.out_fp32) {
         // 4-byte outputs: bands of 32 columns
+        const int n_bands = a.d_out / 32;
 #pragma unroll 1
-        for (int band = 0; band < D / 32; ++band) {
+        for (int band = 0; band < n_bands; ++band) {
           uint32_t o[32];
           tmem_ld_32x32b_x32(to + band * 32, o);
-          if (band == D / 32 - 1) {
+          if (band == n_bands - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
@@ -814,11 +818,12 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         }
       } else {
         // bf16 outputs: bands of 64 columns
+        const int n_bands = a.d_out / 64;
 #pragma unroll 1
-        for (int band = 0; band < D / 64; ++band) {
+        for (int band = 0; band < n_bands; ++band) {
           uint32_t o[64];
           tmem_ld_32x32b_x64(to + band * 64, o);
-          if (band == D / 64 - 1) {
+          if (band == n_bands - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
@@ -988,18 +993,20 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   const long long so_m = R ? p.so.h : p.so.m, so_h = R ? R * p.so.h : p.so.h;
   const long long so_b = R ? (varlen ? p.so.m : p.so.b) : p.so.b;
   CUtensorMap tq, tk, tv;
-  if (!encode_bhmd(enc, &tq, p.q, D, q_rows, q_heads, q_batch, sq_m, sq_h, sq_b, F8) ||
-      !encode_bhmd(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, F8) ||
-      !encode_bhmd(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, F8)) {
+  const int Dd = p.K;  // the tensors' head dim (below D: columns past it read as zeros)
+  if (!encode_bhmd(enc, &tq, p.q, Dd, q_rows, q_heads, q_batch, sq_m, sq_h, sq_b, F8) ||
+      !encode_bhmd(enc, &tk, p.k, Dd, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, F8) ||
+      !encode_bhmd(enc, &tv, p.v, Dd, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, F8)) {
     *why = "cuTensorMapEncodeTiled rejected a q/k/v layout";
     return cudaErrorInvalidValue;
   }
   // Output tiles: bands of 128 bytes (64 bf16 / 32 fp32 columns) x 128 rows.
   CUtensorMap to{};
   const bool tma_store =
-      encode_out(enc, &to, p.out, p.out_fp32, D, q_rows, q_heads, q_batch, so_m, so_h, so_b);
+      encode_out(enc, &to, p.out, p.out_fp32, Dd, q_rows, q_heads, q_batch, so_m, so_h, so_b);
   TcArgs a{};
   a.fold = R;
+  a.d_out = Dd;
   if (R) {
     // lse [B, H, 1] (dense) or [1, H, total_q] (packed): query head = K/V head * r + row
     a.lse_sb = varlen ? 1 : p.H;
@@ -1078,8 +1085,9 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
 cudaError_t launch_fmha_tc(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
                            const char** why) {
   if (p.fp8) {
-    if (p.K == 128) return launch_d<128, true>(p, ctl, stream, why);
-    *why = "E4M3 inputs on the tensor-core path need head dim 128";
+    // head dim 64 runs on the 128-wide E4M3 kernel, zero-padded by the tensor maps
+    if (p.K == 128 || p.K == 64) return launch_d<128, true>(p, ctl, stream, why);
+    *why = "E4M3 inputs on the tensor-core path need head dim 64 or 128";
     return cudaErrorInvalidValue;
   }
   if (p.K == 128) return launch_d<128, false>(p, ctl, stream, why);

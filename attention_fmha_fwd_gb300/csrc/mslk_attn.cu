@@ -233,7 +233,7 @@ DeviceCtl device_ctl() {
 // ~1.9e10 / rows) — e.g. 16 x 8 heads x 32768 keys at 8 rows: 351 vs 1817 us, at 4 x 8
 // heads: 339 vs 472 us; at 1 row the CUDA cores are always ahead.
 bool few_rows_prefer_tensor_cores(int rows, long long units, int K, bool fp8) {
-  if (rows < 2 || (fp8 && K != 128)) return false;
+  if (rows < 2) return false;
   const double bytes_per_key = (fp8 ? 2.0 : 4.0) * K;  // k + v
   const double tc = std::min(6.2e12 / bytes_per_key, static_cast<double>(units) * 1.0e8);
   const double cc = std::min(6.6e12 / bytes_per_key, 1.9e10 / rows);
@@ -264,7 +264,7 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   // (batch, K/V head) units to fill the SMs.
   const long long fold_units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.Hkv;
   const bool fold = p.kv_group > 1 && rows_q == 1 && p.kv_group <= kFoldMaxRows &&
-                    (!p.fp8 || p.K == 128) && policy != 2 &&
+                    policy != 2 &&
                     (policy == 1 || fold_units >= kFoldMinUnits);
   if (fold) {
     AttnProblem f = p;
@@ -403,14 +403,6 @@ mslk_status attn_general(const mslk_attn_args& a, cudaStream_t stream, const cha
   if (a.lanes != nullptr) {
     s = apply_lanes(p, a.lanes, who);
     if (s != MSLK_OK) return s;
-  }
-  if (p.fp8 && p.B > 0 && p.H > 0 && p.M > 0) {
-    const int rows = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
-    const bool decode = rows <= kDecodeMaxRows && g_path_policy.load() != 1;
-    if (!decode && p.K != 128)
-      return fail(MSLK_ERR_UNSUPPORTED,
-                  "%s: E4M3 inputs with more than %d query rows need head dim 128 (got %d)", who,
-                  kDecodeMaxRows, p.K);
   }
   return run_attn(p, stream, who);
 }

@@ -237,8 +237,8 @@ typedef struct {
  * Masks, windows and bottom-right alignment as mslk_attn_fwd_band (band may be NULL);
  * key lanes as mslk_attn_fwd_lanes when `lanes` is non-NULL (then B must be 1).
  * The result is attention on the dequantized values.  Query blocks of at most 8 rows (per
- * packed sequence) run on the CUDA-core kernel with fp32 probabilities; larger ones on the
- * tensor cores (kind::f8f6f4, K = Kv = 128 only, else MSLK_ERR_UNSUPPORTED), where the
+ * packed sequence) may run on the CUDA-core kernel (probabilities rounded to f16); larger
+ * ones on the tensor cores (kind::f8f6f4; K = Kv = 64 runs zero-padded to 128), where the
  * probabilities are rounded to E4M3 before P.V (relative error <= 2^-4 per probability;
  * the row sum uses the unrounded values).  Paged lanes need page_size a multiple of 128
  * (of 8192 / K when every sequence has at most 8 queries).

@@ -250,7 +250,7 @@ def _fp8_call(lib, scales="ok", B=2, M=64, K=128, sq=None, lanes=None, mask=0, s
     (dict(scales=_capi.Fp8Scales(FAKE, FAKE, FAKE, 2)), _capi.MSLK_ERR_INVALID_ARG, "per_tensor"),
     (dict(scales=_capi.Fp8Scales(FAKE, FAKE + 2, FAKE, 0)), _capi.MSLK_ERR_MISALIGNED, "4-byte"),
     (dict(sq=S(8 * 136 * 64, 8 * 136, 136)), _capi.MSLK_ERR_MISALIGNED, "16 elements"),  # 136 % 16
-    (dict(K=64), _capi.MSLK_ERR_UNSUPPORTED, "head dim 128"),       # > 8 rows on the tensor cores
+    (dict(K=96), _capi.MSLK_ERR_UNSUPPORTED, "head dim"),
     (dict(lanes=L(FAKE, FAKE, None, 0, 0), mask=2), _capi.MSLK_ERR_INVALID_ARG, "B = 1"),
 ])
 def test_fp8_rejects(lib, kw, status, needle):
@@ -271,7 +271,7 @@ def test_fp8_pass_validation(lib):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    for kw in (dict(), dict(K=64, M=4), dict(scales=_capi.Fp8Scales(FAKE, FAKE, FAKE, 1)),
+    for kw in (dict(), dict(K=64, M=4), dict(K=64), dict(scales=_capi.Fp8Scales(FAKE, FAKE, FAKE, 1)),
                dict(B=1, mask=3, lanes=L(FAKE, None, FAKE, 128, 4),
                     sl=_capi.Seqlens(FAKE, None, 4, 16, 64))):
         st, why = _fp8_call(lib, **kw)

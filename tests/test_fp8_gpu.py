@@ -163,6 +163,19 @@ def test_fp8_tensor_core(B, M, Mkv, H, mask, br, wl, per_head):
                       f"fp8 tc B{B} M{M} Mkv{Mkv} {mask} br{br} wl{wl}", br=br, wl=wl)
 
 
+@pytest.mark.parametrize("M,Mkv,mask,br", [(300, 700, "causal", True), (200, 200, "none", False)])
+def test_fp8_tensor_core_head_dim_64(M, Mkv, mask, br):
+    """Head dim 64 on the 128-wide E4M3 kernel: the tensor maps zero-fill columns 64..127."""
+    q8, dq, k8, dk, v8, dv = inputs.qkv_fp8(2, M, Mkv, 2, 64, seed=M + 64)
+    scale = 64 ** -0.5
+    out, lse = _run(q8, k8, v8, dq, dk, dv, mask, scale, bottom_right=br)
+    ro, rl = oracle.attention_fp8(_np(q8), _np(k8), _np(v8), _np(dq), _np(dk), _np(dv), scale,
+                                  KIND[mask], bottom_right=br)
+    _check_lse(lse, rl, f"fp8 tc d64 M{M}")
+    _p_rounding_check(out, ro, _deq(q8, dq), _deq(k8, dk), _deq(v8, dv), scale, mask,
+                      f"fp8 tc d64 M{M} {mask}", br=br)
+
+
 def test_fp8_tensor_core_varlen():
     lq, lk = [100, 300, 20, 260], [200, 300, 400, 129]
     cu_q, cu_k = inputs.cu_seqlens(lq), inputs.cu_seqlens(lk)
