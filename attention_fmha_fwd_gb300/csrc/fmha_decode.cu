@@ -72,6 +72,9 @@ struct DecArgs {
   // Query head h reads K/V head h / kv_group; each CTA takes `fold` query heads of one K/V
   // head (a divisor of kv_group) as extra rows, so that K/V head is streamed once for them.
   int kv_group, fold;
+  // Head-dim elements that exist (head dim 96 runs on the 128-wide kernel: the tensor maps
+  // zero-fill K/V columns 96..127, and lanes past them neither load q nor store out).
+  int d_real;
   int cs;  // CTAs per (batch, head): the cluster size
   // Key j is allowed for query row m iff m + lo <= j <= m + hi (kv_offset folded in;
   // +-kBandOpen: open), plus each packed sequence's Lk - Lq when band_seq is set.
@@ -517,9 +520,11 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
 #pragma unroll
       for (int e = 0; e < VE / 2; ++e) qh[m][e] = 0u;
       qscale[m] = a.scale_log2;
-      if (m < nrows) {
-        const int hq = hq0 + m / nq;  // row m: query head hq, position pos[m]
-        if constexpr (F8) qscale[m] *= a.dq[a.desc_per_tensor ? 0 : hq] * a.dk[a.desc_per_tensor ? 0 : hk];
+      const int hq = hq0 + (nq > 0 ? m / nq : 0);  // row m: query head hq, position pos[m]
+      // (warp-uniform: after the reduction lane j holds key j's score, scaled by qscale)
+      if constexpr (F8)
+        if (m < nrows) qscale[m] *= a.dq[a.desc_per_tensor ? 0 : hq] * a.dk[a.desc_per_tensor ? 0 : hk];
+      if (m < nrows && lane * VE < a.d_real) {
         const long long el = bc * a.sq_b + (qrow0 + m % nq) * a.sq_m + hq * a.sq_h + lane * VE;
         const VT x = *reinterpret_cast<const VT*>(a.q + el * L::kEsz);
         if constexpr (F8) {
@@ -625,7 +630,9 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
       }
       float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
       if constexpr (F8) inv *= a.dv[a.desc_per_tensor ? 0 : hk];
-      if (a.out_fp32) {
+      if (lane * VE >= a.d_real) {
+        // (padding lanes of a narrower head dim write nothing)
+      } else if (a.out_fp32) {
         float* op = static_cast<float*>(a.out) + bc * a.so_b + qrow * a.so_m + hq * a.so_h + lane * VE;
 #pragma unroll
         for (int e = 0; e < VE; ++e) op[e] = o[e] * inv;
@@ -767,13 +774,13 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
     *why = "cuTensorMapEncodeTiled is not available from the driver";
     return cudaErrorNotSupported;
   }
-  const int D = p.K;
+  const int D = p.K > 64 ? 128 : 64;  // the kernel's width (96 runs zero-padded to 128)
   const int esz = p.fp8 ? 1 : 2;
   const int T = 8192 / (D * esz);
   const long long hk = p.Hkv;
   CUtensorMap tk, tv;
-  if (!encode_rows_plain(enc, &tk, p.k, D, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, D, T, p.fp8) ||
-      !encode_rows_plain(enc, &tv, p.v, D, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, D, T, p.fp8)) {
+  if (!encode_rows_plain(enc, &tk, p.k, p.K, p.Mkv, hk, p.B, p.sk.m, p.sk.h, p.sk.b, D, T, p.fp8) ||
+      !encode_rows_plain(enc, &tv, p.v, p.K, p.Mkv, hk, p.B, p.sv.m, p.sv.h, p.sv.b, D, T, p.fp8)) {
     *why = "cuTensorMapEncodeTiled rejected a k/v layout";
     return cudaErrorInvalidValue;
   }
@@ -790,6 +797,7 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   a.Mkv = p.Mkv;
   a.H = p.H;
   a.kv_group = p.kv_group;
+  a.d_real = p.K;
   a.lo = p.band_lo <= -kBandOpen ? -kBandOpen : p.band_lo - p.kv_offset;
   a.hi = p.band_hi >= kBandOpen ? kBandOpen : p.band_hi - p.kv_offset;
   a.scale_log2 = p.scale * kLog2e;

@@ -140,7 +140,8 @@ struct TcArgs {
   int fold;
   long long lse_sb, lse_sh, lse_sm;
   // Output columns written: D, or the true head dim when a narrower one runs zero-padded
-  // (E4M3 head dim 64 on the 128-wide kernel: the tensor maps zero-fill columns 64..127).
+  // (head dim 96, or E4M3 head dim 64, on the 128-wide kernel: the tensor maps zero-fill
+  // the missing columns).
   int d_out;  // lse element of (Q/O batch coordinate, head, row)
   // E4M3 inputs: element x of head h stands for x * descale[h] (descale[0] when
   // desc_per_tensor); q and k descales fold into the score scale, v's into the output.
@@ -781,7 +782,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       const uint32_t stage_base = s_base + L::kOutOff + t * L::kStageOutBytes;
       if (a.out_fp32) {
         // 4-byte outputs: bands of 32 columns
-        const int n_bands = a.d_out / 32;
+        const int n_bands = (a.d_out + 31) / 32;
 #pragma unroll 1
         for (int band = 0; band < n_bands; ++band) {
           uint32_t o[32];
@@ -818,7 +819,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         }
       } else {
         // bf16 outputs: bands of 64 columns
-        const int n_bands = a.d_out / 64;
+        const int n_bands = (a.d_out + 63) / 64;  // a partial last band is clipped by the map
 #pragma unroll 1
         for (int band = 0; band < n_bands; ++band) {
           uint32_t o[64];
@@ -852,7 +853,8 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
             __nv_bfloat16* op =
                 static_cast<__nv_bfloat16*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + band * 64;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) *reinterpret_cast<uint4*>(op + ch * 8) = w[ch];
+            for (int ch = 0; ch < 8; ++ch)
+              if (band * 64 + ch * 8 < a.d_out) *reinterpret_cast<uint4*>(op + ch * 8) = w[ch];
           }
         }
       }
@@ -1085,12 +1087,12 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
 cudaError_t launch_fmha_tc(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t stream,
                            const char** why) {
   if (p.fp8) {
-    // head dim 64 runs on the 128-wide E4M3 kernel, zero-padded by the tensor maps
-    if (p.K == 128 || p.K == 64) return launch_d<128, true>(p, ctl, stream, why);
-    *why = "E4M3 inputs on the tensor-core path need head dim 64 or 128";
+    // head dims 64 and 96 run on the 128-wide E4M3 kernel, zero-padded by the tensor maps
+    if (p.K == 128 || p.K == 96 || p.K == 64) return launch_d<128, true>(p, ctl, stream, why);
+    *why = "E4M3 inputs on the tensor-core path need head dim 64, 96 or 128";
     return cudaErrorInvalidValue;
   }
-  if (p.K == 128) return launch_d<128, false>(p, ctl, stream, why);
+  if (p.K == 128 || p.K == 96) return launch_d<128, false>(p, ctl, stream, why);  // 96: zero-padded
   if (p.K == 64) return launch_d<64, false>(p, ctl, stream, why);
   *why = "head dim must be 64 or 128";
   return cudaErrorInvalidValue;

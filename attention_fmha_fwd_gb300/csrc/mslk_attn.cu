@@ -103,8 +103,8 @@ mslk_status validate_attn(AttnProblem& p, const void* q, const void* k, const vo
     return fail(MSLK_ERR_INVALID_ARG, "%s: null strides", who);
   if (K != Kv)
     return fail(MSLK_ERR_UNSUPPORTED, "%s: K (%d) != Kv (%d) is not supported", who, K, Kv);
-  if (K != 64 && K != 128)
-    return fail(MSLK_ERR_UNSUPPORTED, "%s: head dim %d not supported (64 or 128)", who, K);
+  if (K != 64 && K != 96 && K != 128)
+    return fail(MSLK_ERR_UNSUPPORTED, "%s: head dim %d not supported (64, 96 or 128)", who, K);
   p = AttnProblem{};
   p.q = q;
   p.k = k;
@@ -316,7 +316,8 @@ mslk_seqlens lanes_seqlens(const mslk_seqlens* seqlens, const mslk_kv_lanes* lan
 mslk_status apply_lanes(AttnProblem& p, const mslk_kv_lanes* lanes, const char* who) {
   if (lanes->block_table != nullptr) {
     const bool decode = p.max_seqlen_q <= kDecodeMaxRows && g_path_policy.load() != 1;
-    const int multiple = decode ? (p.fp8 ? 8192 / p.K : 64) : 128;
+    const int width = p.K > 64 ? 128 : 64;  // the decode kernel's head-dim width
+    const int multiple = decode ? (p.fp8 ? 8192 / width : 64) : 128;
     if (lanes->page_size % multiple)
       return fail(MSLK_ERR_UNSUPPORTED, "%s: page_size %d must be a multiple of %d", who,
                   lanes->page_size, multiple);

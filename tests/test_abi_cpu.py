@@ -65,7 +65,7 @@ def _fwd(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,status,needle", [
-    (dict(K=96, Kv=96), _capi.MSLK_ERR_UNSUPPORTED, "head dim"),
+    (dict(K=80, Kv=80), _capi.MSLK_ERR_UNSUPPORTED, "head dim"),
     (dict(K=128, Kv=64), _capi.MSLK_ERR_UNSUPPORTED, "Kv"),
     (dict(mask=7), _capi.MSLK_ERR_INVALID_ARG, "mask_kind"),
     (dict(B=-1), _capi.MSLK_ERR_INVALID_ARG, "negative"),
@@ -250,7 +250,7 @@ def _fp8_call(lib, scales="ok", B=2, M=64, K=128, sq=None, lanes=None, mask=0, s
     (dict(scales=_capi.Fp8Scales(FAKE, FAKE, FAKE, 2)), _capi.MSLK_ERR_INVALID_ARG, "per_tensor"),
     (dict(scales=_capi.Fp8Scales(FAKE, FAKE + 2, FAKE, 0)), _capi.MSLK_ERR_MISALIGNED, "4-byte"),
     (dict(sq=S(8 * 136 * 64, 8 * 136, 136)), _capi.MSLK_ERR_MISALIGNED, "16 elements"),  # 136 % 16
-    (dict(K=96), _capi.MSLK_ERR_UNSUPPORTED, "head dim"),
+    (dict(K=80), _capi.MSLK_ERR_UNSUPPORTED, "head dim"),
     (dict(lanes=L(FAKE, FAKE, None, 0, 0), mask=2), _capi.MSLK_ERR_INVALID_ARG, "B = 1"),
 ])
 def test_fp8_rejects(lib, kw, status, needle):

@@ -118,3 +118,56 @@ def test_few_rows_many_heads_dispatch(M, policy):
         fa.set_path_policy(0)
     ro, rl = oracle.attention(f32(q), f32(k), f32(v), s, oracle.MASK_CAUSAL, bottom_right=True)
     compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"M{M} policy{policy}")
+
+
+# ------------------------------------------------------------------ head dim 96
+# Runs on the 128-wide kernels: the tensor maps zero-fill columns 96..127; padding lanes of
+# the CUDA-core kernel neither load q nor store out.
+
+@pytest.mark.parametrize("B,M,Mkv,H,Hkv,mask,policy", [
+    (2, 300, 700, 2, 2, "causal", 0),    # tensor cores
+    (2, 1, 3000, 4, 4, "causal", 0),     # CUDA cores
+    (2, 5, 2000, 4, 4, "none", 2),
+    (16, 1, 900, 16, 4, "causal", 0),    # folded grouped heads on the tensor cores
+])
+def test_head_dim_96(B, M, Mkv, H, Hkv, mask, policy):
+    q, k, v = inputs.qkv(B, M, Mkv, H, 96, Hkv=Hkv, seed=M + 96)
+    s = 96 ** -0.5
+    fa.set_path_policy(policy)
+    try:
+        out, lse = fa.attn_fwd(*to_dev(q, k, v), mask=mask, scale=s, bottom_right=True)
+        torch.cuda.synchronize()
+    finally:
+        fa.set_path_policy(0)
+    ro, rl = oracle.attention(f32(q), f32(k), f32(v), s, KIND[mask], bottom_right=True)
+    compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"d96 B{B} M{M} {mask}")
+
+
+def test_head_dim_96_split_kv_and_fp8():
+    q, k, v = inputs.qkv(1, 200, 1500, 2, 96, seed=96)
+    s = 96 ** -0.5
+    qd, kd, vd = to_dev(q, k, v)
+    outs, lses = [], []
+    for a, b in inputs.equal_chunks(1500, 3):
+        o, l_ = fa.attn_partial(qd, kd[:, a:b], vd[:, a:b], scale=s)
+        outs.append(o)
+        lses.append(l_)
+    out, lse = fa.merge_attentions(torch.stack(outs), torch.stack(lses))
+    ro, rl = oracle.attention(f32(q), f32(k), f32(v), s, oracle.MASK_NONE)
+    compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, "d96 split-KV")
+    # E4M3 at head dim 96: decode rows (CUDA cores) and a prefill block (tensor cores)
+    from tests.test_fp8_gpu import _check_lse, _deq, _np, _p_rounding_check
+    for M in (3, 300):
+        q8, dq, k8, dk, v8, dv = inputs.qkv_fp8(1, M, 1200, 2, 96, seed=M)
+        o, l_ = fa.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), dq.cuda(), dk.cuda(), dv.cuda(),
+                                mask="causal", scale=s, bottom_right=True)
+        torch.cuda.synchronize()
+        ro, rl = oracle.attention_fp8(_np(q8), _np(k8), _np(v8), _np(dq), _np(dk), _np(dv), s,
+                                      oracle.MASK_CAUSAL, bottom_right=True)
+        o, l_ = o.double().cpu().numpy(), l_.double().cpu().numpy()
+        if M <= 8:
+            compare(o, l_, ro, rl, "d96 fp8 decode")
+        else:
+            _check_lse(l_, rl, "d96 fp8 tc")
+            _p_rounding_check(o, ro, _deq(q8, dq), _deq(k8, dk), _deq(v8, dv), s, "causal",
+                              "d96 fp8 tc", br=True)
