@@ -71,7 +71,11 @@ class AttnArgs(ctypes.Structure):
                 ("Kv", ctypes.c_int32), ("scale", ctypes.c_float), ("mask_kind", ctypes.c_int32),
                 ("seqlens", ctypes.c_void_p), ("band", ctypes.c_void_p), ("lanes", ctypes.c_void_p),
                 ("fp8", ctypes.c_void_p), ("partial", ctypes.c_int32), ("kv_offset", ctypes.c_int64),
-                ("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int32), ("lse", ctypes.c_void_p)]
+                ("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int32), ("lse", ctypes.c_void_p),
+                ("flags", ctypes.c_uint32)]
+
+
+FLAG_INDEPENDENT = 1
 
 
 class MslkError(RuntimeError):

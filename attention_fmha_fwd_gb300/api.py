@@ -107,7 +107,7 @@ def _addr(x):
 
 
 def _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, *, lanes=None,
-             fp8=None, partial=0, kv_offset=0):
+             fp8=None, partial=0, kv_offset=0, flags=0):
     """mslk_attn with every option in one argument struct (grouped K/V heads)."""
     B, M, H, K = q.shape
     a = _capi.AttnArgs()
@@ -120,6 +120,7 @@ def _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, *, 
     a.seqlens, a.band, a.lanes, a.fp8 = _addr(sl), _addr(band), _addr(lanes), _addr(fp8)
     a.partial, a.kv_offset = int(partial), int(kv_offset)
     a.out, a.out_dtype, a.lse = out.data_ptr(), _DTYPES[out_dtype], _ptr(lse)
+    a.flags = int(flags)
     check(_capi.load().mslk_attn(ctypes.byref(a), _stream_handle(stream, q.device)))
 
 
@@ -152,7 +153,7 @@ def _seqlens(mask_kind, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k):
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", scale=None,
              cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
              out=None, lse=True, stream=None, bottom_right=False, window_left=None,
-             window_right=None):
+             window_right=None, independent=False):
     """Fused attention forward; returns (out, lse) with lse None when ``lse=False``.
 
     q [B,M,H,K], k [B,Mkv,H,K], v [B,Mkv,H,Kv] bf16 CUDA tensors (BMK inputs are viewed
@@ -176,8 +177,9 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", 
         lse = None
     sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
     band = _band(bottom_right, window_left, window_right)
-    if Hkv != H:  # grouped K/V heads
-        _general(q, k, v, Hkv, mk, scale, sl, band, out, torch.bfloat16, lse, stream)
+    if Hkv != H or independent:  # grouped K/V heads, or a launch that may overlap the previous
+        _general(q, k, v, Hkv, mk, scale, sl, band, out, torch.bfloat16, lse, stream,
+                 flags=_capi.FLAG_INDEPENDENT if independent else 0)
         return out, lse
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")
@@ -376,11 +378,14 @@ def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descale_q, d
 def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none",
                  scale=None, kv_offset: int = 0, cu_seqlens_q=None, cu_seqlens_k=None,
                  max_seqlen_q=None, max_seqlen_k=None, out_dtype=torch.float32, out=None,
-                 lse=None, stream=None, window_left=None, window_right=None):
+                 lse=None, stream=None, window_left=None, window_right=None, independent=False):
     """Attention over one disjoint K/V chunk; returns (out, lse) for merge_attentions.
 
     ``kv_offset`` is the position of the chunk's first key (read by causal masks and
     windows; a bottom-right alignment over the full keys is folded into it).
+    ``independent=True`` states that q, k and v are not written by the launch just before
+    this one on the stream (e.g. the previous chunk of the same split): the call may then
+    start while that launch finishes.
     """
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
     _check_inputs(q, k, v)
@@ -398,9 +403,9 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
         lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
     sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
     band = _band(False, window_left, window_right)
-    if Hkv != H:  # grouped K/V heads
+    if Hkv != H or independent:  # grouped K/V heads, or a launch that may overlap the previous
         _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, partial=1,
-                 kv_offset=kv_offset)
+                 kv_offset=kv_offset, flags=_capi.FLAG_INDEPENDENT if independent else 0)
         return out, lse
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")

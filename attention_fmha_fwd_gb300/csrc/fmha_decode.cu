@@ -75,6 +75,7 @@ struct DecArgs {
   // Head-dim elements that exist (head dim 96 runs on the 128-wide kernel: the tensor maps
   // zero-fill K/V columns 96..127, and lanes past them neither load q nor store out).
   int d_real;
+  int independent;  // launched with programmatic stream serialization (see the host side)
   int cs;  // CTAs per (batch, head): the cluster size
   // Key j is allowed for query row m iff m + lo <= j <= m + hi (kv_offset folded in;
   // +-kBandOpen: open), plus each packed sequence's Lk - Lq when band_seq is set.
@@ -387,6 +388,9 @@ MSLK_DEV void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, cons
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbortOff);
   volatile int* issued_ctr = reinterpret_cast<volatile int*>(smem + L::kIssuedOff);
 
+  // A following launch that declared itself independent of this one may start now; a
+  // launch without that declaration still waits for this grid to complete.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int rank = static_cast<int>(blockIdx.x) % a.cs;  // CTA rank inside the cluster
   const int hq0 = static_cast<int>(blockIdx.x) / a.cs * a.fold;  // first query head of the CTA
   const int warp = threadIdx.x / 32;
@@ -744,13 +748,19 @@ cudaError_t launch_dm(const CUtensorMap& tk, const CUtensorMap& tv, DecArgs a, i
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(a.cs);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (a.independent) {
+    // the caller's inputs are not written by the previous launch: start while it finishes
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, kernel, tk, tv, a);
 }
 
@@ -798,6 +808,7 @@ cudaError_t launch_fmha_decode(const AttnProblem& p, const DeviceCtl& ctl, cudaS
   a.H = p.H;
   a.kv_group = p.kv_group;
   a.d_real = p.K;
+  a.independent = p.independent ? 1 : 0;
   a.lo = p.band_lo <= -kBandOpen ? -kBandOpen : p.band_lo - p.kv_offset;
   a.hi = p.band_hi >= kBandOpen ? kBandOpen : p.band_hi - p.kv_offset;
   a.scale_log2 = p.scale * kLog2e;

@@ -50,6 +50,7 @@ struct AttnProblem {
   // > 1: one query position per batch / packed sequence, run on the tensor cores with the
   // kv_group query heads of a K/V head as the rows of one unit (set by the dispatcher).
   int fold;
+  bool independent;  // MSLK_FLAG_INDEPENDENT: may overlap the preceding launch
 };
 
 struct MergeProblem {

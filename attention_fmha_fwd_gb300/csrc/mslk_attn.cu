@@ -376,6 +376,8 @@ mslk_status attn_general(const mslk_attn_args& a, cudaStream_t stream, const cha
   }
   if (a.partial != 0 && a.partial != 1)
     return fail(MSLK_ERR_INVALID_ARG, "%s: partial must be 0 or 1", who);
+  if (a.flags & ~MSLK_FLAG_INDEPENDENT)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: unknown flags %#x", who, a.flags);
   if (a.Hkv < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative Hkv", who);
   mslk_status s = ok();
   mslk_seqlens sl{};
@@ -394,6 +396,7 @@ mslk_status attn_general(const mslk_attn_args& a, cudaStream_t stream, const cha
                     a.scale, a.mask_kind, slp, a.band, a.partial ? a.kv_offset : 0, a.out,
                     a.out_dtype, a.lse, a.partial == 1, a.partial == 1, who, f8 ? 1 : 2, a.Hkv);
   if (s != MSLK_OK) return s;
+  p.independent = (a.flags & MSLK_FLAG_INDEPENDENT) != 0;
   if (f8 != nullptr) {
     p.fp8 = true;
     p.descale_q = f8->descale_q;

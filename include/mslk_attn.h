@@ -283,7 +283,18 @@ typedef struct {
   void* out;
   int32_t out_dtype;
   float* lse;
+  uint32_t flags;  /* MSLK_FLAG_* */
 } mslk_attn_args;
+
+/*
+ * MSLK_FLAG_INDEPENDENT: the caller states that this call's inputs (q, k, v, descales,
+ * sequence tables) are not written by the launch just before it on the stream, e.g. the
+ * next chunk of a split-KV loop.  The call may then start while that launch is still
+ * finishing (programmatic dependent launch), so back-to-back partials overlap their ramp
+ * and tail.  Calls without the flag keep plain stream order, so a merge that reads the
+ * partials' outputs still waits for them.  Used by the few-row (CUDA-core) kernel.
+ */
+#define MSLK_FLAG_INDEPENDENT 1u
 
 mslk_status mslk_attn(const mslk_attn_args* args, void* stream);
 

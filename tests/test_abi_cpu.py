@@ -315,6 +315,7 @@ def _args(**kw):
     (dict(partial=2), _capi.MSLK_ERR_INVALID_ARG, "partial"),
     (dict(partial=1, lse=None), _capi.MSLK_ERR_INVALID_ARG, "lse is required"),
     (dict(out_dtype=7), _capi.MSLK_ERR_INVALID_ARG, "out_dtype"),
+    (dict(flags=6), _capi.MSLK_ERR_INVALID_ARG, "flags"),
 ])
 def test_general_entry_rejects(lib, kw, status, needle):
     a = _args(**kw)
@@ -336,7 +337,8 @@ def test_general_entry_passes_validation(lib):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    for kw in (dict(), dict(Hkv=2), dict(Hkv=8, partial=1, out_dtype=1), dict(Hkv=1, M=4)):
+    for kw in (dict(), dict(Hkv=2), dict(Hkv=8, partial=1, out_dtype=1), dict(Hkv=1, M=4),
+               dict(M=1, partial=1, flags=_capi.FLAG_INDEPENDENT)):
         a = _args(**kw)
         st = lib.mslk_attn(ctypes.byref(a), None)
         assert st == _capi.MSLK_ERR_CUDA, lib.mslk_last_error().decode()

@@ -371,3 +371,43 @@ def test_varlen_workload_sampled():
         ro, rl = oracle.attention_head(qf, kf, vf, 0, h, w.scale, oracle.MASK_BLOCKDIAG_CAUSAL,
                                        cu_seqlens_q=cu, cu_seqlens_k=cu)
         compare(out[0, :, h], lse[0, h], ro, rl, f"varlen h{h}")
+
+
+def test_independent_partials_overlap():
+    """Back-to-back chunk partials declared independent (programmatic dependent launch),
+    eager and captured in a CUDA graph, then merged: equal to the oracle and bit-equal to
+    the same partials in plain stream order."""
+    B, M, Mkv, H, D = 16, 1, 8192, 8, 128
+    q, k, v = inputs.qkv(B, M, Mkv, H, D, seed=31)
+    s = D ** -0.5
+    qd, kd, vd = to_dev(q, k, v)
+    bounds = inputs.equal_chunks(Mkv, 8)
+    po = torch.empty((8, B, M, H, D), dtype=torch.float32, device="cuda")
+    pl = torch.empty((8, B, H, M), dtype=torch.float32, device="cuda")
+
+    def parts(independent):
+        for c, (a, b) in enumerate(bounds):
+            fa.attn_partial(qd, kd[:, a:b], vd[:, a:b], scale=s, out=po[c], lse=pl[c],
+                            independent=independent and c > 0)
+
+    parts(False)
+    ref_o, ref_l = po.clone(), pl.clone()
+    parts(True)
+    torch.cuda.synchronize()
+    assert torch.equal(po, ref_o) and torch.equal(pl, ref_l)
+    po.zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        parts(True)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        parts(True)
+    po.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(po, ref_o) and torch.equal(pl, ref_l)
+    out, lse = fa.merge_attentions(po, pl)
+    ro, rl = oracle.attention(f32(q), f32(k), f32(v), s, oracle.MASK_NONE)
+    compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, "independent partials")
