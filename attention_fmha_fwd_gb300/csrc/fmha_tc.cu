@@ -354,6 +354,9 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int G = gridDim.x;
+  // A following launch declared independent of this one may start now (the others wait
+  // for this grid to complete as usual).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int cta = blockIdx.x;
   const int n_rounds = (a.total_units + G - 1) / G;
 
@@ -1068,8 +1071,21 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  kernel<<<grid, kThreads, Lt::kAlloc, stream>>>(tq, tk, tv, to, a);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Lt::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (p.independent) {
+    // the caller's inputs are not written by the previous launch: start while it finishes
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     static thread_local char msg[160];
     cudaFuncAttributes fa{};

@@ -493,17 +493,33 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
         mo = torch.empty((w.B, w.M, w.H, w.Kv), dtype=torch.bfloat16, device=dev)
         ml = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=dev)
 
-        def parts(bounds=bounds, po=po, pl=pl):
-            for c, (a0, b0) in enumerate(bounds):
-                fa.attn_partial(qs, ks[:, a0:b0], vs[:, a0:b0], scale=w.scale, out=po[c], lse=pl[c])
+        kvs = [(ks[:, a0:b0], vs[:, a0:b0]) for a0, b0 in bounds]
+
+        def parts(independent=False, kvs=kvs, po=po, pl=pl):
+            for c, (kc_, vc_) in enumerate(kvs):
+                fa.attn_partial(qs, kc_, vc_, scale=w.scale, out=po[c], lse=pl[c],
+                                independent=independent and c > 0)
 
         merge = lambda po=po, pl=pl, mo=mo, ml=ml: fa.merge_attentions(po, pl, out=mo, lse=ml)  # noqa: E731
         for _ in range(10):
             parts()
             merge()
-        res[f"split_kv_{n}_chunks_1x128x1024x16x128"] = {
-            "partials_us": _time_it(parts, 50, stream, flush) * 1e6,
-            "merge_us": _time_it(merge, 50, stream, flush) * 1e6, "launches": n + 1}
+        entry = {"eager_partials_us": _time_it(parts, 50, stream, flush) * 1e6,
+                 "merge_us": _time_it(merge, 50, stream, flush) * 1e6, "launches": n + 1}
+        for key, ind in (("graph_partials_us", False), ("graph_independent_partials_us", True)):
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                parts(ind)
+            stream.wait_stream(side)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                parts(ind)
+            gr.replay()
+            torch.cuda.synchronize()
+            entry[key] = _time_it(gr.replay, 50, stream, flush) * 1e6
+            del gr
+        res[f"split_kv_{n}_chunks_1x128x1024x16x128"] = entry
     # merge: 8 chunks of [2, 2048, 32, 128] fp32 -> bf16 out + fp32 lse
     n, B, M, H, Kv = 8, 2, 2048, 32, 128
     g = torch.Generator(device=dev).manual_seed(0)

@@ -292,7 +292,7 @@ typedef struct {
  * next chunk of a split-KV loop.  The call may then start while that launch is still
  * finishing (programmatic dependent launch), so back-to-back partials overlap their ramp
  * and tail.  Calls without the flag keep plain stream order, so a merge that reads the
- * partials' outputs still waits for them.  Used by the few-row (CUDA-core) kernel.
+ * partials' outputs still waits for them.
  */
 #define MSLK_FLAG_INDEPENDENT 1u
 

@@ -411,3 +411,24 @@ def test_independent_partials_overlap():
     out, lse = fa.merge_attentions(po, pl)
     ro, rl = oracle.attention(f32(q), f32(k), f32(v), s, oracle.MASK_NONE)
     compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, "independent partials")
+
+
+def test_independent_partials_tensor_cores():
+    """The same on the tensor-core path (128 query rows per chunk)."""
+    w = inputs.WORKLOADS["split_kv"]
+    q, k, v = inputs.qkv(w.B, w.M, w.Mkv, w.H, w.K, seed=0)
+    qd, kd, vd = to_dev(q, k, v)
+    bounds = inputs.equal_chunks(w.Mkv, 8)
+    outs = {}
+    for ind in (False, True):
+        po = torch.empty((8, w.B, w.M, w.H, w.Kv), dtype=torch.float32, device="cuda")
+        pl = torch.empty((8, w.B, w.H, w.M), dtype=torch.float32, device="cuda")
+        for c, (a, b) in enumerate(bounds):
+            fa.attn_partial(qd, kd[:, a:b], vd[:, a:b], scale=w.scale, out=po[c], lse=pl[c],
+                            independent=ind and c > 0)
+        torch.cuda.synchronize()
+        outs[ind] = (po, pl)
+    assert torch.equal(outs[False][0], outs[True][0]) and torch.equal(outs[False][1], outs[True][1])
+    out, lse = fa.merge_attentions(*outs[True])
+    ro, rl = oracle.attention(f32(q), f32(k), f32(v), w.scale, oracle.MASK_NONE)
+    compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, "independent tc partials")
