@@ -4,7 +4,9 @@
   -inf handling work at the extremes of fp32 exponents;
 * a key late in the row that dominates it (the running max jumps after many tiles);
 * many key tiles per row (accumulation over 512 tiles, sampled rows);
-* unit counts that do not divide the SM count, and many heads on the decode path.
+* unit counts that do not divide the SM count, and many heads on the decode path;
+* tensors of more than 2^31 elements (64-bit offsets): built on the device by repeating a
+  host-generated block, so the oracle sees the block (closed form for repeated keys).
 """
 
 from __future__ import annotations
@@ -171,3 +173,82 @@ def test_head_dim_96_split_kv_and_fp8():
             _check_lse(l_, rl, "d96 fp8 tc")
             _p_rounding_check(o, ro, _deq(q8, dq), _deq(k8, dk), _deq(v8, dv), s, "causal",
                               "d96 fp8 tc", br=True)
+
+
+BIG = 2 ** 31
+
+
+def _repeat_rows(block, rows):
+    """Host [1, n, H, D] block -> device [1, rows, H, D] view whose row i is block row i % n."""
+    n = block.shape[1]
+    return block.cuda().repeat(1, -(-rows // n), 1, 1)[:, :rows]
+
+
+def _big_memory_ok(gib):
+    return torch.cuda.mem_get_info()[0] >= gib << 30
+
+
+def test_queries_past_2g_elements():
+    """q and out with more than 2^31 elements (2,097,452 rows x 8 heads x 128) on the tensor
+    cores: rows sampled at the start, middle and ragged end against the oracle."""
+    if not _big_memory_ok(24):
+        pytest.skip("needs ~9 GB of free device memory")
+    H, D, n = 8, 128, 4096
+    s = D ** -0.5
+    Mq = BIG // (H * D) + 300
+    qb, k, v = inputs.qkv(1, n, 256, H, D, seed=21)
+    q = _repeat_rows(qb, Mq)
+    assert q.numel() > BIG
+    out, lse = fa.attn_fwd(q, k.cuda(), v.cuda(), scale=s)
+    torch.cuda.synchronize()
+    rows = [0, 1, n - 1, Mq // 2, Mq - 300, Mq - 129, Mq - 44, Mq - 1]
+    ro, rl = oracle.attention(f32(qb[:, [r % n for r in rows]]), f32(k), f32(v), s, oracle.MASK_NONE)
+    compare(out[:, rows].double().cpu().numpy(), lse[:, :, rows].double().cpu().numpy(), ro, rl,
+            "queries past 2^31 elements")
+
+
+@pytest.mark.parametrize("policy", [2, 1])
+def test_keys_past_2g_elements(policy):
+    """K and V of 513 copies of a 4096-key block (2,101,248 keys x 8 heads x 128, more than
+    2^31 elements each): every key appears 513 times, so out equals attention over the block
+    and lse is the block's plus ln 513.  CUDA-core decode (cluster split) and tensor cores."""
+    if not _big_memory_ok(24):
+        pytest.skip("needs ~9 GB of free device memory")
+    H, D, n = 8, 128, 4096
+    s = D ** -0.5
+    R = BIG // (H * D * n) + 1
+    q, kb, vb = inputs.qkv(1, 1, n, H, D, seed=22)
+    k, v = _repeat_rows(kb, R * n), _repeat_rows(vb, R * n)
+    assert k.numel() > BIG
+    ro, rl = oracle.attention(f32(q), f32(kb), f32(vb), s, oracle.MASK_NONE)
+    fa.set_path_policy(policy)
+    try:
+        out, lse = fa.attn_fwd(q.cuda(), k, v, scale=s)
+        torch.cuda.synchronize()
+    finally:
+        fa.set_path_policy(0)
+    compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl + np.log(R),
+            f"keys past 2^31 elements, policy {policy}")
+
+
+def test_merge_past_2g_elements():
+    """Two chunk results of [1, 2,097,216 rows, 8, 128] fp32 (more than 2^31 elements in the
+    stack): sampled rows against the oracle's merge of the block they repeat."""
+    if not _big_memory_ok(32):
+        pytest.skip("needs ~13 GB of free device memory")
+    H, D, n = 8, 128, 4096
+    M = BIG // (2 * H * D) + 64
+    g = torch.Generator().manual_seed(23)
+    ob = torch.randn(2, 1, n, H, D, generator=g)
+    lb = torch.randn(2, 1, H, n, generator=g) * 4
+    reps = -(-M // n)
+    outs = ob.cuda().repeat(1, 1, reps, 1, 1)[:, :, :M]
+    lses = lb.cuda().repeat(1, 1, 1, reps)[..., :M].contiguous()
+    assert outs.numel() > BIG
+    out, lse = fa.merge_attentions(outs, lses)
+    torch.cuda.synchronize()
+    rows = [0, n - 1, M // 2, M - 65, M - 1]
+    ro, rl = oracle.merge_attentions(ob[:, :, [r % n for r in rows]].numpy(),
+                                     lb[..., [r % n for r in rows]].numpy())
+    compare(out[:, rows].double().cpu().numpy(), lse[..., rows].double().cpu().numpy(), ro, rl,
+            "merge past 2^31 elements")
