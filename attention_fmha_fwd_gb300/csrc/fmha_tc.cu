@@ -235,6 +235,11 @@ MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32
   }
 }
 
+// Bits [0, n) set, n clamped to [0, 32].
+MSLK_DEV uint32_t low_bits(int n) {
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+}
+
 // One work unit: 256 query rows of one (batch or packed sequence, head).
 struct Unit {
   int b, h, hk, z;
@@ -680,14 +685,15 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         uint32_t sr[128];
         tmem_ld_32x32b_x128(ts, sr);
         if (need_mask) {
-          if (kLowerEdge && __any_sync(0xffffffffu, lim_lo > 0)) {  // a lower window edge here
+          // One allowed-column bit word per 32 columns, then a bit test per column:
+          // -inf is excluded from the max and 2^-inf = 0.
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c)
-              if (c > lim_c || c < lim_lo) sr[c] = 0xFF800000u;  // -inf: excluded from the max
-          } else {
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w = low_bits(lim_c + 1 - 32 * q4);
+            if constexpr (kLowerEdge) w &= ~low_bits(lim_lo - 32 * q4);
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c)
-              if (c > lim_c) sr[c] = 0xFF800000u;  // -inf: excluded from the max, 2^-inf = 0
+            for (int c = 0; c < 32; ++c)
+              if (!((w >> c) & 1u)) sr[32 * q4 + c] = 0xFF800000u;
           }
         }
         float mx8[8];
