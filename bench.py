@@ -828,6 +828,14 @@ def run_profile_other(args):
 
         def step():
             fa.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, scale=128 ** -0.5)
+    elif args.workload == "decode_single":
+        # bf16 decode in one launch (keys split over a cluster), 16 x 8192 keys x 8 heads x
+        # 128 (537 MB of K/V: larger than L2)
+        q, k, v = inputs.qkv(16, 1, 8192, 8, 128, seed=0)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+
+        def step():
+            fa.attn_fwd(qd, kd, vd, scale=128 ** -0.5)
     else:
         w = inputs.WORKLOADS["varlen_packed"]
         lens = inputs.varlen_seqlens(w.n_seqs, w.M, seed=0)
@@ -867,7 +875,7 @@ def main():
                     help="only the warm-up and timed steps (for ncu); prints a short line")
     ap.add_argument("--workload", default="causal_fwd",
                     choices=["causal_fwd", "merge", "decode_split_kv", "varlen_packed", "fp8_causal_fwd",
-                             "fp8_decode"],
+                             "fp8_decode", "decode_single"],
                     help="with --profile-mode: which kernel's workload to run")
     args = ap.parse_args()
     if args.warmup < 3:
