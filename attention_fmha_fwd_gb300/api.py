@@ -86,14 +86,15 @@ def _check_inputs(q, k, v):
 def _kv_heads(q, k, v) -> int:
     """K/V head count, checked against q: equal batch, key count and head dims, and a number
     of K/V heads dividing the query heads (query head h reads K/V head h // (H // Hkv))."""
-    H = q.shape[2]
-    if k.shape[0] != q.shape[0] or v.shape[0] != q.shape[0]:
+    qs, ks, vs = q.shape, k.shape, v.shape  # (each .shape builds a new Size: read once)
+    H = qs[2]
+    if ks[0] != qs[0] or vs[0] != qs[0]:
         raise ValueError("q, k and v must have the same batch size")
-    if k.shape[1] != v.shape[1] or k.shape[2] != v.shape[2]:
+    if ks[1] != vs[1] or ks[2] != vs[2]:
         raise ValueError("k and v must have the same number of keys and heads")
-    if k.shape[3] != q.shape[3]:
+    if ks[3] != qs[3]:
         raise ValueError("q and k head dims differ")
-    Hkv = k.shape[2]
+    Hkv = ks[2]
     if Hkv < 1 or H % Hkv:
         raise ValueError(f"k/v heads ({Hkv}) must divide the query heads ({H})")
     return Hkv
