@@ -53,6 +53,10 @@
 //  * grouped K/V heads: query head h reads K/V head h / kv_group;
 //  * folded heads (fold = r): one query position per batch / sequence, the unit's rows are
 //    the r query heads of one K/V head (q/out tensor maps are views), all at position 0;
+//    with r <= 128 (the kSplit instantiation) both Q tiles hold those rows and take
+//    alternate key tiles, each with its own running max, sum and O, and Q tile 0 merges
+//    the two by log-sum-exp at the epilogue (tile 1's max and sum through shared memory),
+//    so both softmax warpgroups work on a decode unit;
 //  * E4M3 inputs (fmha_tc_fp8_kernel, head dim 128): kind::f8f6f4 MMAs, one 128-byte
 //    swizzle atom per row, E4M3 probabilities four per TMEM column, descales folded into
 //    the exponent scale (q, k) and the output normalisation (v).
@@ -100,10 +104,12 @@ struct Layout {
   static constexpr int kOutOff = kKVOff + kStages * kTileBytes;
   static constexpr int kBarOff = kOutOff + kQTiles * kStageOutBytes;
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2],
-  // o_free[2], drain
-  static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1;
+  // o_free[2], drain, split_full, split_empty
+  static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1 + 2;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // abort flag, tmem slot
-  static constexpr int kBytes = kMiscOff + 16;
+  // Split units: Q tile 1's row max and sum for Q tile 0's merge, [row][2] fp32.
+  static constexpr int kSplitOff = kMiscOff + 16;
+  static constexpr int kBytes = kSplitOff + kBlockM * 8;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
 
@@ -247,17 +253,27 @@ struct Unit {
   int q_base, Lq, k_base, Lk;
   int r0;
   int lo, hi;  // the band of this unit's sequence (see TcArgs), clamped to +-2^30
-  // Key tiles [tlo[t], thi[t]) hold every key some row of Q tile t may see (empty:
-  // tlo == thi); the unit streams [jlo, jhi), their union, which has no gaps because
-  // the band's lower edge never passes its upper edge.
+  // Q tile t takes key tiles tlo[t], tlo[t] + step, ... below thi[t] (empty: tlo == thi);
+  // the unit streams [jlo, jhi), their union, which has no gaps because the band's lower
+  // edge never passes its upper edge.  step = 2 (split): the unit's rows fit one Q tile,
+  // and both Q tiles hold those rows and take alternate key tiles, each with its own
+  // running max, sum and O; the epilogue merges the two by their log-sum-exp.
   int tlo[2], thi[2];
   int jlo, jhi;
+  int step;
   MSLK_DEV bool has(int t) const { return tlo[t] < thi[t]; }
+  MSLK_DEV bool has(int t, int j) const {
+    return tlo[t] <= j && j < thi[t] && (step == 1 || ((j - tlo[t]) & 1) == 0);
+  }
+  MSLK_DEV int count(int t) const { return (thi[t] - tlo[t] + step - 1) / step; }  // (has(t))
+  MSLK_DEV int last(int t) const { return tlo[t] + (count(t) - 1) * step; }         // (has(t))
+  MSLK_DEV int row0(int t) const { return r0 + (step == 2 ? 0 : t * kBlockM); }  // first row
 };
 
 // Unit i of the heavy-first order: unit rows descend level by level (causal units late in
 // the sequence see the most keys), heads vary fastest within a level.  Returns false if
 // the unit has no rows (a packed sequence shorter than the unit's first row).
+template <bool kSplit>
 MSLK_DEV bool decode_unit(const TcArgs& a, int i, Unit& u) {
   const int per_level = a.H * a.Z;
   const int level = i / per_level;
@@ -330,6 +346,13 @@ MSLK_DEV bool decode_unit(const TcArgs& a, int i, Unit& u) {
     u.tlo[t] = static_cast<int>(k_first / kBlockN);
     u.thi[t] = static_cast<int>(k_last / kBlockN) + 1;
   }
+  u.step = 1;
+  if (kSplit && u.r0 + kBlockM >= u.Lq && u.thi[0] - u.tlo[0] >= 2) {
+    // One Q tile of rows over two or more key tiles: split them between both Q tiles.
+    u.step = 2;
+    u.tlo[1] = u.tlo[0] + 1;
+    u.thi[1] = u.thi[0];
+  }
   if (u.has(0) && u.has(1)) {
     u.jlo = min(u.tlo[0], u.tlo[1]);
     u.jhi = max(u.thi[0], u.thi[1]);
@@ -349,7 +372,7 @@ MSLK_DEV int unit_at(int round, int c, int G) {
 // kLowerEdge: the band has a lower edge (a local window), so masked tiles test both
 // edges; without it the per-row lower limit is compiled out of the softmax.
 // F8: E4M3 q, k, v (kind::f8f6f4 MMAs; P is rounded to E4M3 for the PV MMA).
-template <int D, bool kLowerEdge, bool F8>
+template <int D, bool kLowerEdge, bool F8, bool kSplit>
 MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                       const CUtensorMap& tm_o, const TcArgs& a) {
   using L = Layout<D, F8>;
@@ -377,6 +400,9 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
   auto o_done = [&](int t) { return bar0 + 8u * (8 + 2 * L::kStages + t); };
   auto o_free = [&](int t) { return bar0 + 8u * (10 + 2 * L::kStages + t); };
   const uint32_t bar_drain = bar0 + 8u * (12 + 2 * L::kStages);
+  // split units: Q tile 1's row max and sum are in the slot / tile 0 has read them
+  const uint32_t split_full = bar0 + 8u * (13 + 2 * L::kStages);
+  const uint32_t split_empty = bar0 + 8u * (14 + 2 * L::kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff + 8);
   const WaitCtl wc{abort_flag, a.err, a.timeout_ns};
@@ -401,6 +427,8 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       mbar_init(o_free(t), kBlockM / 32);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(split_full, kBlockM / 32);   // one arrival per warp of Q tile 1
+    mbar_init(split_empty, kBlockM / 32);  // one arrival per warp of Q tile 0
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -433,7 +461,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       mbar_arrive_expect_tx_elect(q_full(t), L::kTileBytes);
       for (int kb = 0; kb < L::kKBlocks; ++kb)
         tma_load_4d_elect(q_addr(t) + kb * kSwizzleAtom, &tm_q, q_full(t), kb * (128 / L::kEsz),
-                          u.q_base + u.r0 + t * kBlockM, u.h, u.qb);
+                          u.q_base + u.row0(t), u.h, u.qb);
       ++q_issued[t];
     };
     auto load_kv = [&](int j, int which, const Unit& u) {  // K_j (which = 0) or V_j
@@ -454,7 +482,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
     for (int k = 0; k < n_rounds && ok; ++k) {
       const int i = unit_at(k, cta, G);
       Unit u;
-      if (i >= a.total_units || !decode_unit(a, i, u) || u.jhi <= u.jlo) continue;
+      if (i >= a.total_units || !decode_unit<kSplit>(a, i, u) || u.jhi <= u.jlo) continue;
       load_q(0, u);
       if (ok) load_kv(u.jlo, 0, u);
       if (ok) load_q(1, u);
@@ -488,7 +516,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
     auto next_unit = [&](int k, int& k_out, Unit& uo) {
       for (; k < n_rounds; ++k) {
         const int i = unit_at(k, cta, G);
-        if (i < a.total_units && decode_unit(a, i, uo) && uo.jhi > uo.jlo) {
+        if (i < a.total_units && decode_unit<kSplit>(a, i, uo) && uo.jhi > uo.jlo) {
           k_out = k;
           return true;
         }
@@ -505,7 +533,9 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       const bool have_next = next_unit(ku + 1, kn, un);
       const int jlo = u.jlo;
       const int jhi = u.jhi;
-      const int lo0 = u.tlo[0], hi0 = u.thi[0], lo1 = u.tlo[1], hi1 = u.thi[1];
+      // Q tile t's first and last key tiles (last < first: none)
+      const int lo0 = u.tlo[0], lo1 = u.tlo[1];
+      const int last0 = u.has(0) ? u.last(0) : lo0 - 1, last1 = u.has(1) ? u.last(1) : lo1 - 1;
       const int ik0 = it++;  // K_jlo's ring position
       const int sk0 = ik0 % L::kStages;
       // S_t(jlo): S_t is free (its last P was consumed by the previous unit's PV_t, which
@@ -515,22 +545,22 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         if (!(ok = wait_bar_warp(q_full(0), uc & 1, wc))) break;
         if (!(ok = wait_bar_warp(kv_full(sk0), (ik0 / L::kStages) & 1, wc))) break;
         tc_fence_after();
-        if ((lo0 <= jlo && jlo < hi0)) {
+        if (u.has(0, jlo)) {
           issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(sk0));
           mma_commit_elect(s_full(0));
         }
-        if (lo0 >= hi0 || hi0 == jlo + 1) mma_commit_elect(q_empty(0));  // Q0's last S issued
+        if (!u.has(0) || last0 == jlo) mma_commit_elect(q_empty(0));  // Q0's last S issued
       }
       s0_issued = false;
       if (!(ok = wait_bar_warp(q_full(1), uc & 1, wc))) break;
       if (!(ok = wait_bar_warp(kv_full(sk0), (ik0 / L::kStages) & 1, wc))) break;
       tc_fence_after();
-      if ((lo1 <= jlo && jlo < hi1)) {
+      if (u.has(1, jlo)) {
         issue_qk<D, F8>(tm_s[1], q_desc[1], kv_kdesc(sk0));
         mma_commit_elect(s_full(1));
       }
       mma_commit_elect(kv_empty(sk0));
-      if (lo1 >= hi1 || hi1 == jlo + 1) mma_commit_elect(q_empty(1));
+      if (!u.has(1) || last1 == jlo) mma_commit_elect(q_empty(1));
       for (int j = jlo; j < jhi && ok; ++j) {
         const bool more = j + 1 < jhi;
         const int iv = it;       // V_j's ring position
@@ -551,42 +581,68 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor core
           __syncwarp();
         }
-        // Q tile 0 (while key tile j is in its range): PV0_j, then S0_{j+1}
-        if ((lo0 <= j && j < hi0)) {
-          if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
-          if (j == lo0 && !(ok = wait_bar_warp(o_free(0), (uc0 & 1) ^ 1, wc))) break;
+        if (u.step == 2) {
+          // Split unit: key tile j belongs to Q tile tj, j + 1 to the other one (tn).
+          // S_tn(j+1) goes first, so tn's softmax runs while tj's does; S_tn is free (its
+          // last P was read by PV_tn(j-1), issued before).
+          const int tj = (j - jlo) & 1, tn = tj ^ 1;
+          if (more) {
+            if (!(ok = wait_bar_warp(kv_full(sk), (ik / L::kStages) & 1, wc))) break;
+            tc_fence_after();
+            issue_qk<D, F8>(tm_s[tn], q_desc[tn], kv_kdesc(sk));
+            mma_commit_elect(s_full(tn));
+            if (j + 1 == (tn ? last1 : last0)) mma_commit_elect(q_empty(tn));
+          }
+          const int lo_j = tj ? lo1 : lo0;
+          if (!(ok = wait_bar_warp(p_full(tj), (tj ? jg1 : jg0) & 1, wc))) break;
+          if (j == lo_j && !(ok = wait_bar_warp(o_free(tj), ((tj ? uc1 : uc0) & 1) ^ 1, wc))) break;
           tc_fence_after();
-          issue_pv<D, F8>(tm_o[0], tm_s[0], kv_vdesc(sv), j > lo0 ? 1u : 0u);
-          if (j == hi0 - 1) mma_commit_elect(o_done(0));
-          ++jg0;
-        }
-        if (more) {
-          if (!(ok = wait_bar_warp(kv_full(sk), (ik / L::kStages) & 1, wc))) break;
-          tc_fence_after();
-          if ((lo0 <= j + 1 && j + 1 < hi0)) {
-            issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(sk));
-            mma_commit_elect(s_full(0));
-            if (j + 2 == hi0) mma_commit_elect(q_empty(0));
+          issue_pv<D, F8>(tm_o[tj], tm_s[tj], kv_vdesc(sv), j > lo_j ? 1u : 0u);
+          // o_done(0) after the unit's last PV of either tile: O_0 and O_1 both final
+          // (tile 0 merges them; o_done(1) has no phase in split units)
+          if (!more) mma_commit_elect(o_done(0));
+          if (tj) ++jg1; else ++jg0;
+          mma_commit_elect(kv_empty(sv));
+          if (more) mma_commit_elect(kv_empty(sk));
+        } else {
+          // Q tile 0 (when key tile j is one of its tiles): PV0_j, then S0_{j+1}
+          if (u.has(0, j)) {
+            if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
+            if (j == lo0 && !(ok = wait_bar_warp(o_free(0), (uc0 & 1) ^ 1, wc))) break;
+            tc_fence_after();
+            issue_pv<D, F8>(tm_o[0], tm_s[0], kv_vdesc(sv), j > lo0 ? 1u : 0u);
+            if (j == last0) mma_commit_elect(o_done(0));
+            ++jg0;
+          }
+          if (more) {
+            if (!(ok = wait_bar_warp(kv_full(sk), (ik / L::kStages) & 1, wc))) break;
+            tc_fence_after();
+            if (u.has(0, j + 1)) {
+              issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(sk));
+              mma_commit_elect(s_full(0));
+              if (j + 1 == last0) mma_commit_elect(q_empty(0));
+            }
+          }
+          // Q tile 1: PV1_j, then S1_{j+1}
+          if (u.has(1, j)) {
+            if (!(ok = wait_bar_warp(p_full(1), jg1 & 1, wc))) break;
+            if (j == lo1 && !(ok = wait_bar_warp(o_free(1), (uc1 & 1) ^ 1, wc))) break;
+            tc_fence_after();
+            issue_pv<D, F8>(tm_o[1], tm_s[1], kv_vdesc(sv), j > lo1 ? 1u : 0u);
+            if (j == last1) mma_commit_elect(o_done(1));
+            ++jg1;
+          }
+          mma_commit_elect(kv_empty(sv));
+          if (more) {
+            if (u.has(1, j + 1)) {
+              issue_qk<D, F8>(tm_s[1], q_desc[1], kv_kdesc(sk));
+              mma_commit_elect(s_full(1));
+              if (j + 1 == last1) mma_commit_elect(q_empty(1));  // the unit's last S1 MMA was issued
+            }
+            mma_commit_elect(kv_empty(sk));
           }
         }
-        // Q tile 1: PV1_j, then S1_{j+1}
-        if ((lo1 <= j && j < hi1)) {
-          if (!(ok = wait_bar_warp(p_full(1), jg1 & 1, wc))) break;
-          if (j == lo1 && !(ok = wait_bar_warp(o_free(1), (uc1 & 1) ^ 1, wc))) break;
-          tc_fence_after();
-          issue_pv<D, F8>(tm_o[1], tm_s[1], kv_vdesc(sv), j > lo1 ? 1u : 0u);
-          if (j == hi1 - 1) mma_commit_elect(o_done(1));
-          ++jg1;
-        }
-        mma_commit_elect(kv_empty(sv));
-        if (more) {
-          if ((lo1 <= j + 1 && j + 1 < hi1)) {
-            issue_qk<D, F8>(tm_s[1], q_desc[1], kv_kdesc(sk));
-            mma_commit_elect(s_full(1));
-            if (j + 2 == hi1) mma_commit_elect(q_empty(1));  // the unit's last S1 MMA was issued
-          }
-          mma_commit_elect(kv_empty(sk));
-        } else if (have_next && un.has(0)) {
+        if (!more && have_next && un.has(0)) {
           // The next unit's first S0 right behind this unit's last PV (its Q0 was loaded
           // after this unit's last S0 MMA), before this warp decodes units and waits for
           // Q1.  S0 is free: this unit's last PV0 precedes it in issue order.
@@ -596,14 +652,14 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           tc_fence_after();
           issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(ikn % L::kStages));
           mma_commit_elect(s_full(0));
-          if (un.thi[0] == un.jlo + 1) mma_commit_elect(q_empty(0));
+          if (un.last(0) == un.jlo) mma_commit_elect(q_empty(0));
           s0_issued = true;
         }
       }
       if (!ok) break;
       ++uc;
-      if (lo0 < hi0) ++uc0;
-      if (lo1 < hi1) ++uc1;
+      if (u.has(0)) ++uc0;
+      if (u.has(1)) ++uc1;
       u = un;
       ku = kn;
       have = have_next;
@@ -619,19 +675,23 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
     const uint32_t lane_bits = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t ts = tmem + static_cast<uint32_t>(t * 128) + lane_bits;
     const uint32_t to = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_bits;
-    int uc = 0, jg = 0;
+    // Barrier phase parities, one register: bit 0 o_done(t) (units in which this Q tile
+    // has keys and writes the output), bit 1 s_full(t) (this tile's key tiles), bit 2
+    // split_full / split_empty (split units).
+    uint32_t ph = 0;
     bool ok = true;
     for (int k = 0; k < n_rounds && ok; ++k) {
       const int i = unit_at(k, cta, G);
       Unit u;
-      if (i >= a.total_units || !decode_unit(a, i, u)) continue;
-      const int row_first = u.r0 + t * kBlockM;  // first row of this Q tile (sequence coords)
+      if (i >= a.total_units || !decode_unit<kSplit>(a, i, u)) continue;
+      const bool split = u.step == 2;
+      const int row_first = u.row0(t);  // first row of this Q tile (sequence coords)
       const int r = row_first + row_in_tile;
       const bool valid = r < u.Lq;
       const long long row = static_cast<long long>(u.q_base) + r;
       // this Q tile's key tiles (selects, not a runtime index, keep u in registers)
       const int tlo_t = t == 0 ? u.tlo[0] : u.tlo[1];
-      const int n_t = (t == 0 ? u.thi[0] : u.thi[1]) - tlo_t;
+      const int n_t = ((t == 0 ? u.thi[0] : u.thi[1]) - tlo_t + u.step - 1) / u.step;
       float sl2 = a.scale_log2;
       if constexpr (F8) {
         const int hq = a.fold ? u.h * a.fold + min(r, a.fold - 1) : u.h;  // this row's query head
@@ -655,13 +715,13 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       }
       float m_run = -INFINITY;
       float l_run = 0.f;
-      for (int j = 0; j < n_t; ++j, ++jg) {
+      for (int j = 0; j < n_t; ++j, ph ^= 2u) {
         // tcgen05.ld is warp-collective: take every wait decision warp-uniformly.
-        ok = __all_sync(0xffffffffu, wait_bar(s_full(t), jg & 1, wc));
+        ok = __all_sync(0xffffffffu, wait_bar(s_full(t), (ph >> 1) & 1u, wc));
         if (!ok) break;
         __syncwarp();
         tc_fence_after();
-        const int key0 = (tlo_t + j) * kBlockN;
+        const int key0 = (tlo_t + j * u.step) * kBlockN;
         // The tile is allowed whole for every row iff its last key is below Lk and within
         // the first row's upper band edge and its first key is within the last row's lower
         // edge; otherwise column c is allowed iff lim_lo <= c <= lim_c (this row's band
@@ -772,15 +832,44 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full(t));  // one arrival per warp
       }
-      if (!ok) break;
+      float2* const split_row = reinterpret_cast<float2*>(smem + L::kSplitOff) + row_in_tile;
+      if (split && t == 1) {
+        // Split unit: hand this row's max and sum to Q tile 0, which merges O_1 into its
+        // output (once tile 0 has read the previous split unit's).
+        ok = ok && __all_sync(0xffffffffu, wait_bar(split_empty, ((ph >> 2) & 1u) ^ 1u, wc));
+        if (!ok) break;
+        *split_row = make_float2(m_run, l_run);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(split_full);
+        ph ^= 4u;
+        continue;
+      }
 
-      // ---- epilogue: wait for the unit's last PV_t, read O_t, hand it back, then store.
-      ok = __all_sync(0xffffffffu, wait_bar(o_done(t), uc & 1, wc));
+      // ---- epilogue: wait for the unit's last PV_t (split: both tiles' last PV), read
+      // O_t, hand it back, then store.
+      ok = ok && __all_sync(0xffffffffu, wait_bar(o_done(t), ph & 1u, wc));
+      // split unit: O_1 (tile 1's alternate key tiles) and its row max and sum merge in
+      float c0 = 1.f, c1 = 0.f, m_out = m_run, l_out = l_run;
+      if (split) {
+        ok = ok && __all_sync(0xffffffffu, wait_bar(split_full, (ph >> 2) & 1u, wc));
+        if (!ok) break;
+        const float2 ml1 = *split_row;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(split_empty);
+        ph ^= 4u;
+        m_out = fmaxf(m_run, ml1.x);
+        c0 = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - m_out);
+        c1 = (ml1.x == -INFINITY) ? 0.f : ex2_approx(ml1.x - m_out);
+        l_out = l_run * c0 + ml1.y * c1;
+      }
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
-      float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      float inv_l = (l_out > 0.f) ? 1.f / l_out : 0.f;
       if constexpr (F8) inv_l *= a.dv[a.desc_per_tensor ? 0 : u.hk];
+      c0 *= inv_l;
+      c1 *= inv_l;
+      const uint32_t to1 = tmem + 384u + lane_bits;  // O_1 (split units)
       // Output tiles go through this warpgroup's staging buffer and one TMA store per
       // 128-byte column band, except the tail tile of a packed sequence (a whole 128-row
       // box would spill into the next sequence), which is stored row by row.
@@ -796,10 +885,22 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         for (int band = 0; band < n_bands; ++band) {
           uint32_t o[32];
           tmem_ld_32x32b_x32(to + band * 32, o);
+          if (split) {
+            uint32_t o1[32];
+            tmem_ld_32x32b_x32(to1 + band * 32, o1);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * c0 + u2f(o1[e]) * c1);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * c0);
+          }
           if (band == n_bands - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
+            if (lane == 0) {
+              mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
+              if (split) mbar_arrive(o_free(1));
+            }
           }
           if (use_tma) {
             if (leader) bulk_wait_read0();  // the previous band's store has read the buffer
@@ -808,8 +909,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
             for (int c = 0; c < 32; c += 4) {
               const int chunk = (c / 4) ^ (row_in_tile & 7);  // 128-byte swizzle
               *reinterpret_cast<float4*>(stage + chunk * 16) =
-                  make_float4(u2f(o[c]) * inv_l, u2f(o[c + 1]) * inv_l, u2f(o[c + 2]) * inv_l,
-                              u2f(o[c + 3]) * inv_l);
+                  make_float4(u2f(o[c]), u2f(o[c + 1]), u2f(o[c + 2]), u2f(o[c + 3]));
             }
             fence_proxy_async_smem();
             named_bar_sync(1 + t, kBlockM);
@@ -822,8 +922,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
               *reinterpret_cast<float4*>(op + c) =
-                  make_float4(u2f(o[c]) * inv_l, u2f(o[c + 1]) * inv_l, u2f(o[c + 2]) * inv_l,
-                              u2f(o[c + 3]) * inv_l);
+                  make_float4(u2f(o[c]), u2f(o[c + 1]), u2f(o[c + 2]), u2f(o[c + 3]));
           }
         }
       } else {
@@ -833,18 +932,33 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         for (int band = 0; band < n_bands; ++band) {
           uint32_t o[64];
           tmem_ld_32x32b_x64(to + band * 64, o);
+          if (split) {
+#pragma unroll
+            for (int hb = 0; hb < 64; hb += 32) {  // O_1 32 columns at a time (registers)
+              uint32_t o1[32];
+              tmem_ld_32x32b_x32(to1 + band * 64 + hb, o1);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[hb + e] = f2u(u2f(o[hb + e]) * c0 + u2f(o1[e]) * c1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) o[e] = f2u(u2f(o[e]) * c0);
+          }
           if (band == n_bands - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
+            if (lane == 0) {
+              mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
+              if (split) mbar_arrive(o_free(1));
+            }
           }
           uint4 w[8];
 #pragma unroll
           for (int c = 0; c < 64; c += 8) {
-            w[c / 8].x = pack_bf16x2(u2f(o[c]) * inv_l, u2f(o[c + 1]) * inv_l);
-            w[c / 8].y = pack_bf16x2(u2f(o[c + 2]) * inv_l, u2f(o[c + 3]) * inv_l);
-            w[c / 8].z = pack_bf16x2(u2f(o[c + 4]) * inv_l, u2f(o[c + 5]) * inv_l);
-            w[c / 8].w = pack_bf16x2(u2f(o[c + 6]) * inv_l, u2f(o[c + 7]) * inv_l);
+            w[c / 8].x = pack_bf16x2(u2f(o[c]), u2f(o[c + 1]));
+            w[c / 8].y = pack_bf16x2(u2f(o[c + 2]), u2f(o[c + 3]));
+            w[c / 8].z = pack_bf16x2(u2f(o[c + 4]), u2f(o[c + 5]));
+            w[c / 8].w = pack_bf16x2(u2f(o[c + 6]), u2f(o[c + 7]));
           }
           if (use_tma) {
             if (leader) bulk_wait_read0();  // the previous band's store has read the buffer
@@ -870,9 +984,9 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       if (valid) {
         if (a.lse != nullptr)
           a.lse[u.qb * a.lse_sb + u.h * a.lse_sh + row * a.lse_sm] =
-              (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
+              (l_out > 0.f) ? (m_out + lg2_approx(l_out)) * kLn2 : -INFINITY;
       }
-      ++uc;
+      ph ^= 1u;
     }
   }
 
@@ -887,21 +1001,23 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
   }
 }
 
-template <int D, bool kLowerEdge>
+// kSplit: units whose rows fit one Q tile split their key tiles between both Q tiles (the
+// folded-head launches; a separate instantiation, so the others keep their code).
+template <int D, bool kLowerEdge, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const TcArgs a) {
-  tc_body<D, kLowerEdge, false>(tm_q, tm_k, tm_v, tm_o, a);
+  tc_body<D, kLowerEdge, false, kSplit>(tm_q, tm_k, tm_v, tm_o, a);
 }
 
 // E4M3 q, k, v (head dim 128), bf16 or fp32 output.
-template <bool kLowerEdge>
+template <bool kLowerEdge, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_tc_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                        const TcArgs a) {
-  tc_body<128, kLowerEdge, true>(tm_q, tm_k, tm_v, tm_o, a);
+  tc_body<128, kLowerEdge, true, kSplit>(tm_q, tm_k, tm_v, tm_o, a);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1070,8 +1186,15 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.total_units = static_cast<int>(total);
   // Persistent: one CTA per SM (or fewer when there are fewer units).
   const dim3 grid(static_cast<unsigned>(std::min<long long>(total, num_sms())));
-  auto kernel = a.lo > -kBandOpen ? fmha_tc_kernel<D, true> : fmha_tc_kernel<D, false>;
-  if constexpr (F8) kernel = a.lo > -kBandOpen ? fmha_tc_fp8_kernel<true> : fmha_tc_fp8_kernel<false>;
+  // Split units only for folded heads whose rows fit one Q tile (decode-shaped units over
+  // many key tiles: both softmax warpgroups work on them).
+  const bool split = R > 0 && R <= kBlockM;
+  const bool edge = a.lo > -kBandOpen;
+  auto kernel = edge ? (split ? fmha_tc_kernel<D, true, true> : fmha_tc_kernel<D, true, false>)
+                     : (split ? fmha_tc_kernel<D, false, true> : fmha_tc_kernel<D, false, false>);
+  if constexpr (F8)
+    kernel = edge ? (split ? fmha_tc_fp8_kernel<true, true> : fmha_tc_fp8_kernel<true, false>)
+                  : (split ? fmha_tc_fp8_kernel<false, true> : fmha_tc_fp8_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lt::kAlloc);
   if (e != cudaSuccess) {
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";

@@ -252,3 +252,33 @@ def test_merge_past_2g_elements():
                                      lb[..., [r % n for r in rows]].numpy())
     compare(out[:, rows].double().cpu().numpy(), lse[..., rows].double().cpu().numpy(), ro, rl,
             "merge past 2^31 elements")
+
+
+@pytest.mark.parametrize("B,Mkv,H,Hkv,D,mask,br,wl", [
+    (64, 256, 8, 1, 128, "none", False, None),      # exactly two key tiles: one per Q tile
+    (64, 300, 16, 2, 64, "causal", True, None),     # three key tiles (odd count), head dim 64
+    (4, 1000, 128, 1, 128, "none", False, None),    # 128 folded rows: the largest split unit
+    (8, 700, 32, 4, 128, "causal", True, 200),      # window: each tile masks its own key tiles
+    (16, 129, 8, 2, 128, "none", False, None),      # second key tile holds a single key
+])
+def test_split_units(B, Mkv, H, Hkv, D, mask, br, wl):
+    """Folded decode units (rows fit one Q tile) give both Q tiles the same rows and
+    alternate key tiles, merged by log-sum-exp at the epilogue: forward (bf16 out) and
+    partial (fp32 out) against the oracle."""
+    q, k, v = inputs.qkv(B, 1, Mkv, H, D, Hkv=Hkv, seed=B + Mkv + H)
+    s = D ** -0.5
+    ro, rl = oracle.attention(f32(q), f32(k), f32(v), s, KIND[mask], bottom_right=br,
+                              window_left=wl)
+    fa.set_path_policy(1)
+    try:
+        out, lse = fa.attn_fwd(*to_dev(q, k, v), mask=mask, scale=s, bottom_right=br,
+                               window_left=wl)
+        shift = (Mkv - 1) if br else 0
+        po, pl = fa.attn_partial(*to_dev(q, k, v), mask=mask, scale=s, kv_offset=-shift,
+                                 window_left=wl)
+        torch.cuda.synchronize()
+    finally:
+        fa.set_path_policy(0)
+    what = f"split B{B} Mkv{Mkv} H{H}/{Hkv} D{D} {mask}"
+    compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, what)
+    compare(po.double().cpu().numpy(), pl.double().cpu().numpy(), ro, rl, what + " partial")
