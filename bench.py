@@ -418,7 +418,7 @@ def run_gpu(args):
 
     if rank == 0:
         achieved = flops / t_step / 1e12
-        traffic = traffic_for("fmha_tc_kernel<128, false> causal_fwd")
+        traffic = traffic_for("fmha_tc_kernel<128, false, false> causal_fwd")
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
@@ -432,7 +432,7 @@ def run_gpu(args):
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
                          "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
-                         "kernel": "fmha_tc_kernel<128, false>", "peak_source": peak_src + " bf16 burst"},
+                         "kernel": "fmha_tc_kernel<128, false, false>", "peak_source": peak_src + " bf16 burst"},
             "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
                     "pipeline": "pinned host q/k/v -> device (3 copy streams), attn_fwd, "
