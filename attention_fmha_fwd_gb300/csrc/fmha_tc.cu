@@ -53,10 +53,11 @@
 //  * grouped K/V heads: query head h reads K/V head h / kv_group;
 //  * folded heads (fold = r): one query position per batch / sequence, the unit's rows are
 //    the r query heads of one K/V head (q/out tensor maps are views), all at position 0;
-//    with r <= 128 (the kSplit instantiation) both Q tiles hold those rows and take
-//    alternate key tiles, each with its own running max, sum and O, and Q tile 0 merges
-//    the two by log-sum-exp at the epilogue (tile 1's max and sum through shared memory),
-//    so both softmax warpgroups work on a decode unit;
+//  * split units (the kSplit instantiation, launches with at most 128 rows per unit, e.g.
+//    folded heads with r <= 128): both Q tiles hold the unit's rows and take alternate
+//    key tiles, each with its own running max, sum and O, and Q tile 0 merges the two by
+//    log-sum-exp at the epilogue (tile 1's max and sum through shared memory), so both
+//    softmax warpgroups work on a decode unit;
 //  * E4M3 inputs (fmha_tc_fp8_kernel, head dim 128): kind::f8f6f4 MMAs, one 128-byte
 //    swizzle atom per row, E4M3 probabilities four per TMEM column, descales folded into
 //    the exponent scale (q, k) and the output normalisation (v).
@@ -1001,8 +1002,9 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
   }
 }
 
-// kSplit: units whose rows fit one Q tile split their key tiles between both Q tiles (the
-// folded-head launches; a separate instantiation, so the others keep their code).
+// kSplit: units whose rows fit one Q tile split their key tiles between both Q tiles
+// (launches with at most 128 rows per unit; a separate instantiation, so the others keep
+// their code).
 template <int D, bool kLowerEdge, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1186,9 +1188,10 @@ cudaError_t launch_d(const AttnProblem& p, const DeviceCtl& ctl, cudaStream_t st
   a.total_units = static_cast<int>(total);
   // Persistent: one CTA per SM (or fewer when there are fewer units).
   const dim3 grid(static_cast<unsigned>(std::min<long long>(total, num_sms())));
-  // Split units only for folded heads whose rows fit one Q tile (decode-shaped units over
-  // many key tiles: both softmax warpgroups work on them).
-  const bool split = R > 0 && R <= kBlockM;
+  // Split units when every unit's rows fit one Q tile (decode-shaped units over many key
+  // tiles: both softmax warpgroups work on them); launches with longer rows keep the
+  // instantiation without them.
+  const bool split = rows <= kBlockM;
   const bool edge = a.lo > -kBandOpen;
   auto kernel = edge ? (split ? fmha_tc_kernel<D, true, true> : fmha_tc_kernel<D, true, false>)
                      : (split ? fmha_tc_kernel<D, false, true> : fmha_tc_kernel<D, false, false>);

@@ -228,14 +228,15 @@ DeviceCtl device_ctl() {
 
 // Few query rows: the CUDA-core kernel splits each head's keys over a thread-block cluster
 // but its work grows with the rows; the tensor-core kernel pays the same per key tile for 1
-// to 128 rows but streams one (batch, head) unit per CTA.  Rates measured on GB300 (keys
-// per second): tensor cores min(memory rate, ~1e8 per unit); CUDA cores min(memory rate,
-// ~1.9e10 / rows) — e.g. 16 x 8 heads x 32768 keys at 8 rows: 351 vs 1817 us, at 4 x 8
-// heads: 339 vs 472 us; at 1 row the CUDA cores are always ahead.
+// to 128 rows but streams one (batch, head) unit per CTA (both softmax warpgroups on it).
+// Rates measured on GB300 (keys per second): tensor cores min(memory rate, ~1.7e8 per
+// unit); CUDA cores min(memory rate, ~1.9e10 / rows) — e.g. 16 x 8 heads x 32768 keys at 8
+// rows: 351 vs 1817 us; at 1 row bf16 stays on the CUDA cores (323 vs 330 us) and E4M3
+// goes to the tensor cores (202 vs 221 us).
 bool few_rows_prefer_tensor_cores(int rows, long long units, int K, bool fp8) {
-  if (rows < 2) return false;
   const double bytes_per_key = (fp8 ? 2.0 : 4.0) * K;  // k + v
-  const double tc = std::min(6.2e12 / bytes_per_key, static_cast<double>(units) * 1.0e8);
+  // (a few rows fit one Q tile: the split units' two softmax warpgroups share the keys)
+  const double tc = std::min(6.2e12 / bytes_per_key, static_cast<double>(units) * 1.7e8);
   const double cc = std::min(6.6e12 / bytes_per_key, 1.9e10 / rows);
   return tc > 1.05 * cc;
 }
@@ -254,8 +255,12 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   const int policy = g_path_policy.load();
   const int rows_q = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
   const long long units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.H;
+  // The tensor-core kernel reads 128-key tiles, each inside one page: pages of another
+  // size (accepted for few rows, which the CUDA-core kernel reads) keep few rows there.
+  const bool tc_pages_ok = p.block_table == nullptr || p.page_size % 128 == 0;
   const bool decode_ok = rows_q <= kDecodeMaxRows &&
-                         (policy == 2 || !few_rows_prefer_tensor_cores(rows_q, units, p.K, p.fp8));
+                         (policy == 2 || !tc_pages_ok ||
+                          !few_rows_prefer_tensor_cores(rows_q, units, p.K, p.fp8));
   cudaError_t e;
   const char* why = "launch failed";
   // Grouped heads with one query position per batch / sequence: the tensor cores take the
@@ -264,7 +269,7 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   // (batch, K/V head) units to fill the SMs.
   const long long fold_units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.Hkv;
   const bool fold = p.kv_group > 1 && rows_q == 1 && p.kv_group <= kFoldMaxRows &&
-                    policy != 2 &&
+                    policy != 2 && tc_pages_ok &&
                     (policy == 1 || fold_units >= kFoldMinUnits);
   if (fold) {
     AttnProblem f = p;

@@ -51,11 +51,15 @@ def _np(t):
     return t.numpy() if isinstance(t, torch.Tensor) else np.asarray(t)
 
 
-def _run(q8, k8, v8, dq, dk, dv, mask, scale, **kw):
+def _run(q8, k8, v8, dq, dk, dv, mask, scale, policy=0, **kw):
     dev = lambda t: t.cuda() if isinstance(t, torch.Tensor) else t  # noqa: E731
-    out, lse = fa.attn_fwd_fp8(q8.cuda(), dev(k8), dev(v8), dev(dq), dev(dk), dev(dv), mask=mask,
-                               scale=scale, **kw)
-    torch.cuda.synchronize()
+    fa.set_path_policy(policy)
+    try:
+        out, lse = fa.attn_fwd_fp8(q8.cuda(), dev(k8), dev(v8), dev(dq), dev(dk), dev(dv),
+                                   mask=mask, scale=scale, **kw)
+        torch.cuda.synchronize()
+    finally:
+        fa.set_path_policy(0)
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
@@ -113,7 +117,7 @@ def test_fp8_decode(B, M, Mkv, H, Hkv, D, mask, br, wl, per_head):
     vd = v8.cuda()
     if Hkv == 1:
         kd, vd = kd.expand(-1, -1, H, -1), vd.expand(-1, -1, H, -1)
-    out, lse = _run(q8, kd, vd, dq, dk, dv, mask, scale, bottom_right=br, window_left=wl)
+    out, lse = _run(q8, kd, vd, dq, dk, dv, mask, scale, policy=2, bottom_right=br, window_left=wl)
     ro, rl = oracle.attention_fp8(_np(q8), _np(k8), _np(v8), _np(dq), _np(dk), _np(dv), scale,
                                   KIND[mask], bottom_right=br, window_left=wl)
     compare(out, lse, ro, rl, f"fp8 decode B{B} M{M} Mkv{Mkv} H{H} D{D} {mask}")
@@ -131,7 +135,7 @@ def test_fp8_paged_decode():
     v8[0, torch.from_numpy(~own)] = 0x7F
     scale = D ** -0.5
     out, lse = _run(q8, k8.view(n_pages, ps, H, D), v8.view(n_pages, ps, H, D), dq, dk, dv,
-                    "blockdiag_causal", scale, seqlen_k=_i32(lk), block_table=table.cuda(),
+                    "blockdiag_causal", scale, policy=2, seqlen_k=_i32(lk), block_table=table.cuda(),
                     page_size=ps, cu_seqlens_q=_i32(inputs.cu_seqlens(lq)), max_seqlen_q=max(lq),
                     max_seqlen_k=max(lk), bottom_right=True)
     ro, rl = oracle.attention_lanes_fp8(_np(q8), _np(k8), _np(v8), _np(dq), _np(dk), _np(dv), scale,
@@ -218,7 +222,7 @@ def test_fp8_both_paths_agree_within_bound():
     q8, dq, k8, dk, v8, dv = inputs.qkv_fp8(1, 8, 2000, 2, 128, seed=31)
     scale = 128 ** -0.5
     ro, rl = oracle.attention_fp8(_np(q8), _np(k8), _np(v8), _np(dq), _np(dk), _np(dv), scale)
-    a = _run(q8, k8, v8, dq, dk, dv, "none", scale)
+    a = _run(q8, k8, v8, dq, dk, dv, "none", scale, policy=2)
     compare(a[0], a[1], ro, rl, "fp8 8 rows, CUDA cores")
     fa.set_path_policy(1)
     try:
@@ -227,3 +231,16 @@ def test_fp8_both_paths_agree_within_bound():
         fa.set_path_policy(0)
     _p_rounding_check(b[0], ro, _deq(q8, dq), _deq(k8, dk), _deq(v8, dv), scale, "none",
                       "fp8 8 rows, tensor cores")
+
+
+def test_fp8_single_row_decode_on_tensor_cores():
+    """One query row over 16 x 8 (batch, head) units: the automatic choice sends E4M3 decode
+    to the tensor cores (split units), within the E4M3 probability bound of the oracle."""
+    q8, dq, k8, dk, v8, dv = inputs.qkv_fp8(16, 1, 3000, 8, 128, seed=41)
+    scale = 128 ** -0.5
+    out, lse = _run(q8, k8, v8, dq, dk, dv, "causal", scale, bottom_right=True)
+    ro, rl = oracle.attention_fp8(_np(q8), _np(k8), _np(v8), _np(dq), _np(dk), _np(dv), scale,
+                                  oracle.MASK_CAUSAL, bottom_right=True)
+    assert np.abs(lse - rl).max() <= 1e-3
+    _p_rounding_check(out, ro, _deq(q8, dq), _deq(k8, dk), _deq(v8, dv), scale, "causal",
+                      "fp8 one row, tensor cores", br=True)

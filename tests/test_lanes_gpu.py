@@ -91,6 +91,18 @@ def test_paged_few_queries(lq, mask, br, wl):
     _paged(lq, [1500, 90, 2049, 64, 333], 64, mask=mask, br=br, wl=wl, seed=len(lq) + (wl or 0))
 
 
+@pytest.mark.parametrize("hkv,rows", [(8, 4), (2, 1)])
+def test_paged_small_pages_many_units(hkv, rows):
+    """64-key pages (accepted for a few queries per sequence) with enough (sequence, head)
+    units that the tensor cores would be the faster choice (up to 4 queries per sequence;
+    or one query with the 4 query heads of each K/V head folded): the dispatch keeps such
+    pages on the CUDA-core kernel, since a 128-key tile would straddle pages."""
+    g = torch.Generator().manual_seed(17)
+    lk = torch.randint(100, 2500, (40,), generator=g).tolist()
+    lq = [rows if i % 3 else 1 for i in range(40)]
+    _paged(lq, lk, 64, H=8, hkv=hkv, seed=17 + hkv)
+
+
 def test_paged_shared_kv_head():
     """Multi-query: one K/V head in the pool (head stride 0) serves every query head."""
     _paged([1, 4, 2], [1000, 77, 4100], 128, H=8, hkv=1, seed=3)
