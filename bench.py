@@ -815,8 +815,11 @@ def run_profile_other(args):
 
         def step():
             fa.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, mask="causal", scale=w.scale)
-    elif args.workload == "fp8_decode":
-        # E4M3 decode, 16 x 8192 keys x 8 heads x 128 (268 MB of K/V: larger than L2)
+    elif args.workload in ("fp8_decode", "fp8_decode_tc"):
+        # E4M3 decode, 16 x 8192 keys x 8 heads x 128 (268 MB of K/V: larger than L2):
+        # fp8_decode on the CUDA-core kernel, fp8_decode_tc on the automatic choice (the
+        # tensor cores with split units for these 128 units)
+        fa.set_path_policy(2 if args.workload == "fp8_decode" else 0)
         g = torch.Generator(device=dev).manual_seed(0)
         k = torch.randn((16, 8192, 8, 128), generator=g, device=dev)
         v = torch.randn((16, 8192, 8, 128), generator=g, device=dev)
@@ -875,7 +878,7 @@ def main():
                     help="only the warm-up and timed steps (for ncu); prints a short line")
     ap.add_argument("--workload", default="causal_fwd",
                     choices=["causal_fwd", "merge", "decode_split_kv", "varlen_packed", "fp8_causal_fwd",
-                             "fp8_decode", "decode_single"],
+                             "fp8_decode", "fp8_decode_tc", "decode_single"],
                     help="with --profile-mode: which kernel's workload to run")
     args = ap.parse_args()
     if args.warmup < 3:
