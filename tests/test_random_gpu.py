@@ -89,3 +89,80 @@ def test_random_case(seed):
                                   bottom_right=c["bottom_right"], window_left=wl,
                                   window_right=wr)
     compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"seed {seed}: {c}")
+
+
+# ------------------------------------------------------------------ E4M3 inputs
+
+def _draw_fp8(seed: int) -> dict:
+    rng = np.random.default_rng(5000 + seed)
+    c = dict(
+        B=int(rng.integers(1, 4)),
+        M=int(rng.choice([1, 3, 8, 64, 129, 300])),
+        Mkv=int(rng.choice([7, 128, 200, 777, 1500])),
+        Hkv=int(rng.choice([1, 2])),
+        group=int(rng.choice([1, 2, 4])),
+        D=int(rng.choice([64, 96, 128])),
+        mask=str(rng.choice(["none", "causal"])),
+        per_head=bool(rng.random() < 0.5),
+        scale=float(rng.uniform(0.03, 0.2)),
+        policy=int(rng.choice([0, 0, 1, 2])),
+        bottom_right=bool(rng.random() < 0.5),
+    )
+    c["window_left"] = int(rng.integers(0, 600)) if rng.random() < 0.3 else None
+    c["window_right"] = (int(rng.integers(0, 300)) if c["mask"] == "none" and rng.random() < 0.3
+                         else None)
+    return c
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_fp8_case(seed):
+    """E4M3 q/k/v with tensorwise or per-head descales on either kernel: lse within 1e-3 and
+    the output within the E4M3 probability bound (which the CUDA-core kernel's exact
+    products also meet)."""
+    from tests.test_fp8_gpu import _check_lse, _deq, _p_rounding_check
+    c = _draw_fp8(seed)
+    B, M, Mkv, Hkv, D = c["B"], c["M"], c["Mkv"], c["Hkv"], c["D"]
+    H = Hkv * c["group"]
+    q8, dq, k8, dk, v8, dv = inputs.qkv_fp8(B, M, Mkv, H, D, Hkv=Hkv, seed=seed,
+                                            per_head=c["per_head"])
+    s, wl, wr, br = c["scale"], c["window_left"], c["window_right"], c["bottom_right"]
+    fa.set_path_policy(c["policy"])
+    try:
+        out, lse = fa.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), dq.cuda(), dk.cuda(), dv.cuda(),
+                                   mask=c["mask"], scale=s, bottom_right=br, window_left=wl,
+                                   window_right=wr)
+        torch.cuda.synchronize()
+    finally:
+        fa.set_path_policy(0)
+    ro, rl = oracle.attention_fp8(q8.numpy(), k8.numpy(), v8.numpy(), dq.numpy(), dk.numpy(),
+                                  dv.numpy(), s, KIND[c["mask"]], bottom_right=br, window_left=wl,
+                                  window_right=wr)
+    what = f"fp8 seed {seed}: {c}"
+    _check_lse(lse.double().cpu().numpy(), rl, what)
+    _p_rounding_check(out.double().cpu().numpy(), ro, _deq(q8, dq), _deq(k8, dk), _deq(v8, dv), s,
+                      c["mask"], what, br=br, wl=wl, wr=wr)
+
+
+# ------------------------------------------------------------------ key lanes
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_lanes_case(seed):
+    """Paged key lanes with ragged lengths (spare pages and lane tails poisoned with NaN),
+    a few to a few hundred queries per sequence, page sizes 64 (few queries only), 128 and
+    256, grouped heads, causal / windowed / full block-diagonal masks."""
+    from tests.test_lanes_gpu import _paged
+    rng = np.random.default_rng(9000 + seed)
+    n = int(rng.integers(1, 7))
+    few = rng.random() < 0.5
+    lq = [int(x) for x in rng.choice([0, 1, 2, 5, 8] if few else [0, 1, 8, 100, 300], size=n)]
+    if max(lq) == 0:
+        lq[0] = 1
+    lk = [int(x) for x in rng.integers(1, 3000, size=n)]
+    page_size = int(rng.choice([64, 128, 256] if max(lq) <= 8 else [128, 256]))
+    hkv = int(rng.choice([1, 2, 4]))
+    mask = str(rng.choice(["blockdiag_causal", "blockdiag"]))
+    br = bool(rng.random() < 0.7)
+    wl = int(rng.integers(0, 500)) if rng.random() < 0.3 else None
+    D = int(rng.choice([64, 128]))
+    _paged(lq, lk, page_size, H=4, D=D, mask=mask, br=br, wl=wl, hkv=hkv, seed=seed,
+           policy=int(rng.choice([0, 0, 1, 2])) if max(lq) <= 8 and page_size >= 128 else 0)
