@@ -353,11 +353,13 @@ mslk_status mslk_diag_bounded_wait(void* stream);
 /*
  * Kernel choice, process-wide: 0 automatic (default: for at most 8 query rows per batch
  * or packed sequence, the CUDA-core kernel unless a measured rate model says the
- * tensor-core kernel streams the keys faster — more rows and enough (batch, head) units;
- * grouped heads with one query position go to the tensor cores with enough units; the
- * tensor-core kernel otherwise), 1 always the tensor-core kernel, 2 the CUDA-core kernel
- * wherever it applies (at most 8 query rows).  All choices compute the same function;
- * tests use this to run one problem through each kernel.
+ * tensor-core kernel streams the keys faster — more rows, or E4M3 inputs, and enough
+ * (batch, head) units; grouped heads with one query position go to the tensor cores with
+ * enough units; paged lanes whose page size is not a multiple of 128 stay on the CUDA
+ * cores; the tensor-core kernel otherwise), 1 always the tensor-core kernel, 2 the
+ * CUDA-core kernel wherever it applies (at most 8 query rows).  All choices compute the
+ * same function (E4M3 within the rounding stated at mslk_attn_fwd_fp8); tests use this
+ * to run one problem through each kernel.
  */
 void mslk_set_path_policy(int32_t policy);
 
