@@ -77,6 +77,14 @@ class AttnArgs(ctypes.Structure):
 
 FLAG_INDEPENDENT = 1
 
+# mslk_attn_plan results (bits)
+PLAN_NONE = 0
+PLAN_FILL = 1
+PLAN_CUDA_CORES = 2
+PLAN_TENSOR_CORES = 4
+PLAN_FOLDED_HEADS = 8
+PLAN_SPLIT_UNITS = 16
+
 
 class MslkError(RuntimeError):
     """A non-OK mslk_status, with the library's reason string."""
@@ -112,6 +120,7 @@ SIGNATURES = {
                                  ctypes.c_float, _i32, ctypes.POINTER(Seqlens), ctypes.POINTER(Band),
                                  ctypes.POINTER(KvLanes), ctypes.POINTER(Fp8Scales), _P, _P, _P]),
     "mslk_attn": (_i32, [ctypes.POINTER(AttnArgs), _P]),
+    "mslk_attn_plan": (_i32, [ctypes.POINTER(AttnArgs), ctypes.POINTER(ctypes.c_int32)]),
     "mslk_merge_attentions": (_i32, [_P, _P, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _S, _S,
                                      _P, _i32, _P, _P]),
     "mslk_last_error": (ctypes.c_char_p, []),

@@ -241,6 +241,34 @@ bool few_rows_prefer_tensor_cores(int rows, long long units, int K, bool fp8) {
   return tc > 1.05 * cc;
 }
 
+// Which kernel a validated problem runs on (MSLK_PLAN_* bits), from the problem and the
+// path policy alone (no device access): run_attn launches what this returns.
+int32_t choose_path(const AttnProblem& p, int policy) {
+  if (p.B == 0 || p.H == 0 || p.M == 0) return MSLK_PLAN_NONE;
+  if (p.Mkv == 0) return MSLK_PLAN_FILL;
+  const int rows_q = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
+  const long long units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.H;
+  // The tensor-core kernel reads 128-key tiles, each inside one page: pages of another
+  // size (accepted for few rows, which the CUDA-core kernel reads) keep few rows there.
+  const bool tc_pages_ok = p.block_table == nullptr || p.page_size % 128 == 0;
+  const bool decode_ok = rows_q <= kDecodeMaxRows &&
+                         (policy == 2 || !tc_pages_ok ||
+                          !few_rows_prefer_tensor_cores(rows_q, units, p.K, p.fp8));
+  // Grouped heads with one query position per batch / sequence: the tensor cores take the
+  // group's query heads as the rows of one unit and stream each K/V head once at the
+  // memory rate (the CUDA-core kernel's cost grows with the rows), when there are enough
+  // (batch, K/V head) units to fill the SMs.
+  const long long fold_units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.Hkv;
+  const bool fold = p.kv_group > 1 && rows_q == 1 && p.kv_group <= kFoldMaxRows &&
+                    policy != 2 && tc_pages_ok &&
+                    (policy == 1 || fold_units >= kFoldMinUnits);
+  if (!fold && decode_ok && policy != 1) return MSLK_PLAN_CUDA_CORES;
+  // tensor cores: split units when every unit's rows fit one 128-row Q tile
+  const int rows = fold ? p.kv_group : rows_q;
+  return MSLK_PLAN_TENSOR_CORES | (fold ? MSLK_PLAN_FOLDED_HEADS : 0) |
+         (rows <= 128 ? MSLK_PLAN_SPLIT_UNITS : 0);
+}
+
 mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who) {
   if (p.B == 0 || p.H == 0 || p.M == 0) return ok();
   if (p.Mkv == 0) {
@@ -252,30 +280,14 @@ mslk_status run_attn(const AttnProblem& p, cudaStream_t stream, const char* who)
   }
   const DeviceCtl ctl = device_ctl();
   if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "%s: no CUDA device / module", who);
-  const int policy = g_path_policy.load();
-  const int rows_q = is_blockdiag(p.mask_kind) ? p.max_seqlen_q : p.M;
-  const long long units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.H;
-  // The tensor-core kernel reads 128-key tiles, each inside one page: pages of another
-  // size (accepted for few rows, which the CUDA-core kernel reads) keep few rows there.
-  const bool tc_pages_ok = p.block_table == nullptr || p.page_size % 128 == 0;
-  const bool decode_ok = rows_q <= kDecodeMaxRows &&
-                         (policy == 2 || !tc_pages_ok ||
-                          !few_rows_prefer_tensor_cores(rows_q, units, p.K, p.fp8));
+  const int32_t plan = choose_path(p, g_path_policy.load());
   cudaError_t e;
   const char* why = "launch failed";
-  // Grouped heads with one query position per batch / sequence: the tensor cores take the
-  // group's query heads as the rows of one unit and stream each K/V head once at the
-  // memory rate (the CUDA-core kernel's cost grows with the rows), when there are enough
-  // (batch, K/V head) units to fill the SMs.
-  const long long fold_units = static_cast<long long>(is_blockdiag(p.mask_kind) ? p.n_seqs : p.B) * p.Hkv;
-  const bool fold = p.kv_group > 1 && rows_q == 1 && p.kv_group <= kFoldMaxRows &&
-                    policy != 2 && tc_pages_ok &&
-                    (policy == 1 || fold_units >= kFoldMinUnits);
-  if (fold) {
+  if (plan & MSLK_PLAN_FOLDED_HEADS) {
     AttnProblem f = p;
     f.fold = p.kv_group;
     e = launch_fmha_tc(f, ctl, stream, &why);
-  } else if (decode_ok && policy != 1) {
+  } else if (plan == MSLK_PLAN_CUDA_CORES) {
     e = launch_fmha_decode(p, ctl, stream, &why);
   } else {
     e = launch_fmha_tc(p, ctl, stream, &why);
@@ -368,7 +380,8 @@ mslk_attn_args make_args(const void* q, const void* k, const void* v, const mslk
 }
 
 // Every option of the forward / partial call: validation, then the kernels.
-mslk_status attn_general(const mslk_attn_args& a, cudaStream_t stream, const char* who) {
+mslk_status attn_general(const mslk_attn_args& a, cudaStream_t stream, const char* who,
+                         int32_t* plan = nullptr) {
   const mslk_fp8_scales* f8 = a.fp8;
   if (f8 != nullptr) {
     if (f8->descale_q == nullptr || f8->descale_k == nullptr || f8->descale_v == nullptr)
@@ -412,6 +425,10 @@ mslk_status attn_general(const mslk_attn_args& a, cudaStream_t stream, const cha
   if (a.lanes != nullptr) {
     s = apply_lanes(p, a.lanes, who);
     if (s != MSLK_OK) return s;
+  }
+  if (plan != nullptr) {
+    *plan = choose_path(p, g_path_policy.load());
+    return ok();
   }
   return run_attn(p, stream, who);
 }
@@ -473,6 +490,12 @@ mslk_status mslk_attn_partial_band(const void* q, const void* k, const void* v,
                                       true, true, "mslk_attn_partial_band");
   if (s != MSLK_OK) return s;
   return run_attn(p, static_cast<cudaStream_t>(stream), "mslk_attn_partial_band");
+}
+
+mslk_status mslk_attn_plan(const mslk_attn_args* args, int32_t* plan) {
+  const char* who = "mslk_attn_plan";
+  if (args == nullptr || plan == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: args and plan are required", who);
+  return attn_general(*args, nullptr, who, plan);
 }
 
 mslk_status mslk_attn(const mslk_attn_args* args, void* stream) {

@@ -299,6 +299,24 @@ typedef struct {
 mslk_status mslk_attn(const mslk_attn_args* args, void* stream);
 
 /*
+ * mslk_attn_plan — which kernel mslk_attn would launch for these arguments under the
+ * current path policy, without launching anything or touching the device: the same
+ * validation (and the same error statuses) as mslk_attn, then *plan (caller-owned, host)
+ * receives MSLK_PLAN_NONE (nothing to compute), MSLK_PLAN_FILL (no keys: out = 0 and
+ * lse = -inf are written by a fill kernel), MSLK_PLAN_CUDA_CORES (the few-row kernel), or
+ * MSLK_PLAN_TENSOR_CORES with MSLK_PLAN_FOLDED_HEADS (a group's query heads as the rows
+ * of one unit) and / or MSLK_PLAN_SPLIT_UNITS (rows fit one 128-row tile: both softmax
+ * warpgroups share a unit's key tiles).  Thread-safe; the device pointers are not read.
+ */
+#define MSLK_PLAN_NONE 0
+#define MSLK_PLAN_FILL 1
+#define MSLK_PLAN_CUDA_CORES 2
+#define MSLK_PLAN_TENSOR_CORES 4
+#define MSLK_PLAN_FOLDED_HEADS 8
+#define MSLK_PLAN_SPLIT_UNITS 16
+mslk_status mslk_attn_plan(const mslk_attn_args* args, int32_t* plan);
+
+/*
  * mslk_merge_attentions — exact log-sum-exp merge of n chunk results into preallocated
  * outputs.  MSLK kernel reference, "Attention - Core fMHA" > merge_attentions (exact
  * normalised output over the union of chunks, not an average; write_lse; output_dtype)

@@ -355,3 +355,68 @@ def test_binding_checks_kv_heads():
                  (torch.empty(2, 7, 2, 32), torch.empty(2, 7, 2, 32))):  # head dim differs
         with pytest.raises(ValueError):
             api._kv_heads(q, k, v)
+
+
+# ------------------------------------------------------------------ kernel plan (no device)
+
+TC, CC = _capi.PLAN_TENSOR_CORES, _capi.PLAN_CUDA_CORES
+FOLD, SPLIT = _capi.PLAN_FOLDED_HEADS, _capi.PLAN_SPLIT_UNITS
+
+
+def _plan(lib, a, policy=0):
+    out = ctypes.c_int32(-1)
+    lib.mslk_set_path_policy(policy)
+    try:
+        st = lib.mslk_attn_plan(ctypes.byref(a), ctypes.byref(out))
+    finally:
+        lib.mslk_set_path_policy(0)
+    assert st == _capi.MSLK_OK, lib.mslk_last_error().decode()
+    return out.value
+
+
+@pytest.mark.parametrize("kw,policy,want", [
+    (dict(B=2, M=2048, Mkv=2048, H=32, mask_kind=1), 0, TC),           # causal forward
+    (dict(B=16, M=1, Mkv=32768, H=8), 0, CC),                          # bf16 decode: one row
+    (dict(B=16, M=1, Mkv=32768, H=8), 1, TC | SPLIT),                  # ... forced
+    (dict(B=16, M=4, Mkv=32768, H=8), 0, TC | SPLIT),                  # 4 rows, 128 units
+    (dict(B=16, M=4, Mkv=32768, H=8), 2, CC),                          # ... forced
+    (dict(B=1, M=4, Mkv=32768, H=8), 0, CC),                           # 4 rows, 8 units
+    (dict(B=16, M=1, Mkv=32768, H=32, Hkv=8), 0, TC | FOLD | SPLIT),   # grouped decode
+    (dict(B=2, M=1, Mkv=32768, H=32, Hkv=8), 0, CC),                   # ... too few units
+    (dict(B=4, M=128, Mkv=4096, H=32), 0, TC | SPLIT),                 # one Q tile of rows
+    (dict(B=4, M=129, Mkv=4096, H=32), 0, TC),                         # two Q tiles
+    (dict(B=2, M=64, Mkv=0), 0, _capi.PLAN_FILL),                      # no keys
+    (dict(B=2, M=0), 0, _capi.PLAN_NONE),                              # no queries
+])
+def test_plan_dense(lib, kw, policy, want):
+    assert _plan(lib, _args(**kw), policy) == want
+
+
+def test_plan_fp8_decode(lib):
+    """One E4M3 row over 128 units goes to the tensor cores (split units); over 8 units it
+    stays on the CUDA cores' cluster split."""
+    scales = _capi.Fp8Scales(FAKE, FAKE, FAKE, 0)
+    a = _args(B=16, M=1, Mkv=32768, H=8, fp8=ctypes.addressof(scales))
+    assert _plan(lib, a) == TC | SPLIT
+    a = _args(B=1, M=1, Mkv=32768, H=8, fp8=ctypes.addressof(scales))
+    assert _plan(lib, a) == CC
+
+
+@pytest.mark.parametrize("page_size,want", [(64, CC), (128, TC | SPLIT)])
+def test_plan_paged_pages(lib, page_size, want):
+    """Up to 4 queries per sequence over 64 sequences x 8 heads: the tensor cores would be
+    faster, but 64-key pages (accepted for few queries) stay on the CUDA-core kernel."""
+    lanes = L(FAKE, None, FAKE, page_size, 64)
+    sl = _capi.Seqlens(FAKE, None, 64, 4, 4096)
+    a = _args(B=1, M=256, Mkv=64 * page_size, H=8, mask_kind=3, lanes=ctypes.addressof(lanes),
+              seqlens=ctypes.addressof(sl))
+    assert _plan(lib, a) == want
+
+
+def test_plan_validates_like_the_call(lib):
+    out = ctypes.c_int32(-1)
+    a = _args(Hkv=3)
+    assert lib.mslk_attn_plan(ctypes.byref(a), ctypes.byref(out)) == _capi.MSLK_ERR_INVALID_ARG
+    assert "divide" in lib.mslk_last_error().decode()
+    assert lib.mslk_attn_plan(None, ctypes.byref(out)) == _capi.MSLK_ERR_INVALID_ARG
+    assert lib.mslk_attn_plan(ctypes.byref(_args()), None) == _capi.MSLK_ERR_INVALID_ARG
