@@ -555,6 +555,8 @@ mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split
     return fail(MSLK_ERR_INVALID_ARG, "%s: null pointer", who);
   if (!aligned16(out_split) || !aligned16(out))
     return fail(MSLK_ERR_MISALIGNED, "%s: out_split/out must be 16-byte aligned", who);
+  if ((reinterpret_cast<uintptr_t>(lse_split) & 3u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(MSLK_ERR_MISALIGNED, "%s: lse_split/lse must be 4-byte aligned", who);
   if (n_chunks > 1 && (chunk_stride_out <= 0 || chunk_stride_out % 4))
     return fail(MSLK_ERR_MISALIGNED, "%s: chunk_stride_out must be a positive multiple of 4", who);
   if (n_chunks > 1 && chunk_stride_lse <= 0)

@@ -439,6 +439,10 @@ def run_gpu(args):
                                 "out+lse -> pinned host (1 stream); steps overlap, device "
                                 "buffers double-buffered"},
             "gpu_launches": args.steps,
+            "step_ms": {"mean": t_step * 1e3, "median": statistics.median(per) * 1e3,
+                        "min": min(per) * 1e3, "max": max(per) * 1e3,
+                        "note": "per-step CUDA-event times of the timed steps on this rank; "
+                                "value uses the mean"},
             "clocks": clocks,
             "secondary": secondary,
         }

@@ -12,16 +12,21 @@
  *
  * Conventions shared by every call
  * --------------------------------
- *  - Tensors are [B, M, H, D] (q, out), [B, Mkv, H, D] (k, v): batch, sequence, head,
- *    head dim.  The last dimension has stride 1; the other three strides are free and
- *    given in ELEMENTS by mslk_strides (MSLK kernel reference, memory_efficient_attention
- *    constraints: "last dimension must have stride 1; other dimensions may be
- *    non-contiguous").  The output has the query layout with its last dimension
- *    replaced by the value head dim.
- *  - GQA / MQA: the caller expands K/V to H heads (the pages: MSLK does not broadcast
- *    K/V heads).  A head stride of 0 on k and v (an expand() of one head) is accepted.
- *  - q, k, v are bf16.  K == Kv and K is 64 or 128; other head dims return
- *    MSLK_ERR_UNSUPPORTED.
+ *  - Tensors are [B, M, H, D] (q, out), [B, Mkv, Hkv, D] (k, v): batch, sequence, head,
+ *    head dim.  Only the head dim must be contiguous (stride 1); the batch, sequence and
+ *    head strides may be anything that meets the alignment rule below, and are given in
+ *    ELEMENTS by mslk_strides (MSLK kernel reference > Attention - Core fMHA >
+ *    memory_efficient_attention, constraints).  The output has the query layout with its
+ *    last dimension replaced by the value head dim.
+ *  - Grouped K/V heads (GQA / MQA): mslk_attn takes Hkv K/V heads for H query heads
+ *    (Hkv divides H; query head h reads K/V head h / (H / Hkv)).  The other calls take
+ *    Hkv = H, except that a k/v head stride of 0 (an expand() of one head) means one K/V
+ *    head shared by every query head.  The pages' 5-D BMGHK layout with K/V expanded over
+ *    the H axis is this with Hkv = G once the (G, H) axes are flattened group-major
+ *    (bmghk2bmhk); the Python binding does that flattening on views.
+ *  - q, k, v are bf16 (E4M3 for mslk_attn_fwd_fp8).  K == Kv and the head dim is 64, 96
+ *    or 128 (96 runs on the 128-wide kernels with the missing columns read as zeros);
+ *    other head dims, and K != Kv, return MSLK_ERR_UNSUPPORTED.
  *  - lse is fp32 [B, H, M], contiguous.  Packed variable-length batches (B = 1) use
  *    [1, H, total_q].
  *  - Every pointer is caller-owned DEVICE memory (except the mslk_seqlens struct and
@@ -287,12 +292,16 @@ typedef struct {
 } mslk_attn_args;
 
 /*
- * MSLK_FLAG_INDEPENDENT: the caller states that this call's inputs (q, k, v, descales,
- * sequence tables) are not written by the launch just before it on the stream, e.g. the
- * next chunk of a split-KV loop.  The call may then start while that launch is still
- * finishing (programmatic dependent launch), so back-to-back partials overlap their ramp
- * and tail.  Calls without the flag keep plain stream order, so a merge that reads the
- * partials' outputs still waits for them.
+ * MSLK_FLAG_INDEPENDENT: the call may start before earlier launches on the stream have
+ * finished (programmatic dependent launch), so back-to-back partials of a split-KV loop
+ * overlap their ramp and tail.  Every kernel of this library lets a dependent launch start
+ * as soon as it begins, so a run of flagged calls may overlap one another and the last
+ * launch made WITHOUT the flag before them.  The caller states that no launch in that
+ * window writes this call's inputs (q, k, v, descales, sequence tables) or reads or
+ * writes its outputs (out, lse); e.g. the chunks of one split, each with its own out and
+ * lse slice.  Calls without the flag keep plain stream order: they start only after every
+ * earlier launch on the stream has finished, so a merge that reads the partials' outputs
+ * waits for all of them.
  */
 #define MSLK_FLAG_INDEPENDENT 1u
 
@@ -332,7 +341,8 @@ mslk_status mslk_attn_plan(const mslk_attn_args* args, int32_t* plan);
  *   lse        fp32 [B,H,M] contiguous, or NULL (write_lse = False).
  * Per row: LSE = M* + ln sum_c exp(lse_c - M*) with M* = max_c lse_c;
  * out = sum_c exp(lse_c - LSE) * out_c; a row whose chunks are all -inf gets out = 0 and
- * LSE = -inf.  Kv must be a multiple of 4; out_split and the strides 16-byte aligned.
+ * LSE = -inf.  Kv must be a multiple of 4; out_split, out and their strides 16-byte
+ * aligned; lse_split, the lse chunk stride and lse 4-byte aligned (MSLK_ERR_MISALIGNED).
  */
 mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split,
                                   int32_t n_chunks, int64_t chunk_stride_out,

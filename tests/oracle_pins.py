@@ -631,6 +631,34 @@ def pin_window_split_merge(orc):
         _close(l_, full[1], 1e-12, f"windowed split {bounds} (lse)")
 
 
+def pin_rows_sampling(orc):
+    """attention_head(rows=R) returns, for each sampled row, what the element-by-element
+    brute force gives for that row: causal with a key offset, bottom-right alignment and
+    left windows, rows unsorted and repeated, first and last rows included.  Each row's
+    position must follow its own index (a row treated as row 0 sees only key 0 under a
+    causal mask)."""
+    rng = np.random.default_rng(45)
+    B, M, Mkv, H, Hk, K, Kv = 2, 13, 16, 2, 1, 8, 6
+    q = _bf16_round(_rand(rng, (B, M, H, K)))
+    k = _bf16_round(_rand(rng, (B, Mkv, Hk, K)))
+    v = _bf16_round(_rand(rng, (B, Mkv, Hk, Kv)))
+    rows = [12, 0, 7, 3, 12, 1, 8]
+    cases = [(orc.MASK_CAUSAL, 0, False, None, None), (orc.MASK_CAUSAL, 3, False, None, None),
+             (orc.MASK_CAUSAL, 0, True, None, None), (orc.MASK_CAUSAL, 2, False, 4, None),
+             (orc.MASK_CAUSAL, 0, True, 2, None), (orc.MASK_NONE, 0, True, 3, 1),
+             (orc.MASK_NONE, 0, False, None, None)]
+    for kind, off, br, wl, wr in cases:
+        bo, bl = brute_attention(q, k, v, 0.7, kind, kv_offset=off, bottom_right=br,
+                                 window_left=wl, window_right=wr)
+        for b in range(B):
+            for h in range(H):
+                o, l_ = orc.attention_head(q, k, v, b, h, 0.7, kind, kv_offset=off, rows=rows,
+                                           bottom_right=br, window_left=wl, window_right=wr)
+                what = f"rows kind{kind} off{off} br{br} wl{wl} wr{wr} b{b} h{h}"
+                _close(o, bo[b][rows, h, :], 1e-12, what + " (out)")
+                _close(l_, bl[b, h, rows], 1e-12, what + " (lse)")
+
+
 # --------------------------------------------------------------------------------------
 # padded and paged key lanes
 # --------------------------------------------------------------------------------------
@@ -821,6 +849,7 @@ PINS = [
     pin_bottom_right_reductions,
     pin_band_bruteforce,
     pin_window_split_merge,
+    pin_rows_sampling,
     pin_bruteforce,
     pin_torch_sdpa,
     pin_single_key,

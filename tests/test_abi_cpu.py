@@ -65,7 +65,7 @@ def _fwd(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,status,needle", [
-    (dict(K=80, Kv=80), _capi.MSLK_ERR_UNSUPPORTED, "head dim"),
+    (dict(K=80, Kv=80), _capi.MSLK_ERR_UNSUPPORTED, "head dim 80 not supported (64, 96 or 128)"),
     (dict(K=128, Kv=64), _capi.MSLK_ERR_UNSUPPORTED, "Kv"),
     (dict(mask=7), _capi.MSLK_ERR_INVALID_ARG, "mask_kind"),
     (dict(B=-1), _capi.MSLK_ERR_INVALID_ARG, "negative"),
@@ -155,10 +155,11 @@ def test_band_kinds_pass_validation(lib):
     assert st == _capi.MSLK_ERR_CUDA, why
 
 
-def _merge(lib, n=2, Kv=128, cs_out=2 * 64 * 8 * 128, out_split=FAKE, out=FAKE, dtype=0):
+def _merge(lib, n=2, Kv=128, cs_out=2 * 64 * 8 * 128, out_split=FAKE, out=FAKE, dtype=0,
+           lse_split=FAKE, lse=FAKE):
     s = S(64 * 8 * 128, 8 * 128, 128)
-    st = lib.mslk_merge_attentions(out_split, FAKE, n, cs_out, 2 * 8 * 64, 2, 64, 8, Kv,
-                                   ctypes.byref(s), ctypes.byref(s), out, dtype, FAKE, None)
+    st = lib.mslk_merge_attentions(out_split, lse_split, n, cs_out, 2 * 8 * 64, 2, 64, 8, Kv,
+                                   ctypes.byref(s), ctypes.byref(s), out, dtype, lse, None)
     return st, lib.mslk_last_error().decode()
 
 
@@ -169,6 +170,10 @@ def test_merge_rejects(lib):
     assert _merge(lib, cs_out=6)[0] == _capi.MSLK_ERR_MISALIGNED
     assert _merge(lib, dtype=9)[0] == _capi.MSLK_ERR_INVALID_ARG
     assert _merge(lib, out=None)[0] == _capi.MSLK_ERR_INVALID_ARG
+    # lse pointers are read and written as floats: a misaligned one is rejected before launch
+    assert _merge(lib, lse_split=FAKE + 2) == (_capi.MSLK_ERR_MISALIGNED,
+                                               "mslk_merge_attentions: lse_split/lse must be 4-byte aligned")
+    assert _merge(lib, lse=FAKE + 1)[0] == _capi.MSLK_ERR_MISALIGNED
 
 
 def test_valid_call_without_device_reports_cuda_error(lib):

@@ -29,6 +29,8 @@ MUTANTS = {
     "blockdiag_bottom_right_global_lengths": (
         "_band(mask_kind, bottom_right, window_left, window_right, qe - qs, ke - ks)",
         "_band(mask_kind, bottom_right, window_left, window_right, M, Mkv)"),
+    "rows_position_zero": ("s64, lo, hi, int(i), kv_offset)", "s64, lo, hi, 0, kv_offset)"),
+    "rows_position_off_by_one": ("s64, lo, hi, int(i), kv_offset)", "s64, lo, hi, int(i) + 1, kv_offset)"),
     "scale_dropped": ("x = scale64 * (qb @ kb.T)", "x = (qb @ kb.T)"),
     "scores_use_values": ("x = scale64 * (qb @ kb.T)", "x = scale64 * (qb @ vb.T)"),
     "lse_wrong_sign": ("lse = m + np.log(l)", "lse = m - np.log(l)"),
