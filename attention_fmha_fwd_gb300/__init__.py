@@ -13,11 +13,14 @@ from .api import (  # noqa: F401
     attn_fwd_fp8,
     attn_fwd_lanes,
     attn_partial,
+    attn_split_kv,
     device_status,
     diag_bounded_wait,
     last_error,
     merge_attentions,
     set_path_policy,
     set_wait_timeout_ns,
+    split_kv_workspace_bytes,
+    splitk_size,
     version,
 )

@@ -85,6 +85,8 @@ PLAN_TENSOR_CORES = 4
 PLAN_FOLDED_HEADS = 8
 PLAN_SPLIT_UNITS = 16
 
+MERGE_MAX_VARARGS = 128
+
 
 class MslkError(RuntimeError):
     """A non-OK mslk_status, with the library's reason string."""
@@ -123,6 +125,11 @@ SIGNATURES = {
     "mslk_attn_plan": (_i32, [ctypes.POINTER(AttnArgs), ctypes.POINTER(ctypes.c_int32)]),
     "mslk_merge_attentions": (_i32, [_P, _P, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _S, _S,
                                      _P, _i32, _P, _P]),
+    "mslk_merge_attentions_varargs": (_i32, [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p),
+                                             _i32, _i32, _i32, _i32, _i32, _S, _S, _P, _i32, _P, _P]),
+    "mslk_splitk_size": (_i32, [_i32, _i32, _i32, _i32, _i32]),
+    "mslk_attn_split_kv": (_i32, [ctypes.POINTER(AttnArgs), _i32, _P, ctypes.c_size_t, _P]),
+    "mslk_attn_split_kv_workspace": (_i32, [ctypes.POINTER(AttnArgs), _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "mslk_last_error": (ctypes.c_char_p, []),
     "mslk_device_status": (_i32, [_P]),
     "mslk_set_wait_timeout_ns": (None, [_i64]),

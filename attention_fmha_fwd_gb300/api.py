@@ -72,6 +72,42 @@ def _as_bmhk(t: torch.Tensor) -> torch.Tensor:
     return t
 
 
+def _merge_heads(t: torch.Tensor, name: str) -> torch.Tensor:
+    """[B, M, G, H, D] -> a [B, M, G * H, D] view (group-major head index g * H + h).
+
+    Raises instead of copying when the (G, H) axes cannot be viewed as one."""
+    B, M, G, H, D = t.shape
+    if G > 1 and H > 1 and t.stride(2) != H * t.stride(3):
+        raise ValueError(f"{name}: the G and H axes of a BMGHK tensor must be adjacent in memory "
+                         f"(stride(2) == H * stride(3)) to flatten without a copy")
+    return t.as_strided((B, M, G * H, D),
+                        (t.stride(0), t.stride(1), t.stride(3) if H > 1 else t.stride(2), t.stride(4)))
+
+
+def _bmghk(q, k, v):
+    """The pages' 5-D BMGHK layout flattened to BMHK views (bmghk2bmhk), no copies.
+
+    q [B, M, G, H, K]; k, v [B, Mkv, G, H or 1, K].  K/V that hold one head per group, or are
+    expanded over H with stride 0 (the pages' way of sharing K/V within a group), become
+    G K/V heads (grouped-query attention: query head g * H + h reads K/V head g); K/V with
+    H distinct heads per group become G * H heads.  Returns (q4, k4, v4, G, H).
+    """
+    if k.dim() != 5 or v.dim() != 5:
+        raise ValueError("a 5-D (BMGHK) q needs 5-D k and v")
+    B, M, G, H, K = q.shape
+    if k.shape[2] != G or v.shape[2] != G:
+        raise ValueError(f"k/v have {k.shape[2]}/{v.shape[2]} groups, q has {G}")
+
+    def kv_view(t, name):
+        if t.shape[3] == 1 or t.stride(3) == 0:  # one K/V head per group
+            return t.select(3, 0)
+        if t.shape[3] != H:
+            raise ValueError(f"{name} must have 1 or {H} heads per group (got {t.shape[3]})")
+        return _merge_heads(t, name)
+
+    return _merge_heads(q, "q"), kv_view(k, "k"), kv_view(v, "v"), G, H
+
+
 def _check_inputs(q, k, v):
     bf16 = torch.bfloat16
     if q.dtype is bf16 and k.dtype is bf16 and v.dtype is bf16 and q.is_cuda and k.is_cuda and v.is_cuda:
@@ -107,12 +143,14 @@ def _addr(x):
     return ctypes.addressof(x if isinstance(x, ctypes.Structure) else x._obj)
 
 
-def _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, *, lanes=None,
-             fp8=None, partial=0, kv_offset=0, flags=0):
-    """mslk_attn with every option in one argument struct (grouped K/V heads)."""
+def _args(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, *, lanes=None, fp8=None,
+          partial=0, kv_offset=0, flags=0, ptrs=True):
+    """The mslk_attn_args struct of a call (ptrs=False: sizes only, null pointers)."""
     B, M, H, K = q.shape
     a = _capi.AttnArgs()
-    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    if ptrs:
+        a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+        a.out, a.lse = out.data_ptr(), _ptr(lse)
     a.sq, a.sk, a.sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     a.so = _bmhk_strides(out, "out")
     a.B, a.M, a.Mkv, a.H, a.Hkv, a.K, a.Kv = B, M, k.shape[1], H, Hkv, K, v.shape[3]
@@ -120,8 +158,17 @@ def _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, *, 
     a.mask_kind = mk
     a.seqlens, a.band, a.lanes, a.fp8 = _addr(sl), _addr(band), _addr(lanes), _addr(fp8)
     a.partial, a.kv_offset = int(partial), int(kv_offset)
-    a.out, a.out_dtype, a.lse = out.data_ptr(), _DTYPES[out_dtype], _ptr(lse)
+    a.out_dtype = _DTYPES[out_dtype]
     a.flags = int(flags)
+    a._keep = (band, lanes, fp8)  # the structs the pointers above refer to
+    return a
+
+
+def _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, *, lanes=None,
+             fp8=None, partial=0, kv_offset=0, flags=0):
+    """mslk_attn with every option in one argument struct (grouped K/V heads)."""
+    a = _args(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, lanes=lanes, fp8=fp8,
+              partial=partial, kv_offset=kv_offset, flags=flags)
     check(_capi.load().mslk_attn(ctypes.byref(a), _stream_handle(stream, q.device)))
 
 
@@ -157,13 +204,32 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none", 
              window_right=None, independent=False):
     """Fused attention forward; returns (out, lse) with lse None when ``lse=False``.
 
-    q [B,M,H,K], k [B,Mkv,H,K], v [B,Mkv,H,Kv] bf16 CUDA tensors (BMK inputs are viewed
-    as one head).  ``lse`` may be True (allocate), False (skip) or an fp32 [B,H,M] tensor.
+    q [B,M,H,K], k [B,Mkv,Hkv,K], v [B,Mkv,Hkv,Kv] bf16 CUDA tensors (Hkv dividing H:
+    grouped K/V heads; BMK inputs are viewed as one head), or the 5-D BMGHK layout
+    q [B,M,G,H,K], k/v [B,Mkv,G,H or 1,K] (K/V expanded over H share one head per group),
+    which returns out [B,M,G,H,Kv] and lse [B,G,H,M].  ``lse`` may be True (allocate),
+    False (skip) or an fp32 [B,H,M] tensor.
     ``bottom_right`` / ``window_left`` / ``window_right`` (keys before / after the paired
     key; None = unbounded) select a bottom-right alignment and a local window (the pages'
     ``...FromBottomRight...`` and ``...LocalAttention...`` masks; a causal window of
     ``window_size`` w keys is ``window_left=w - 1``).
     """
+    if q.dim() == 5:  # BMGHK: run on flattened views, return out [B,M,G,H,Kv], lse [B,G,H,M]
+        q4, k4, v4, G, Hg = _bmghk(q, k, v)
+        B, M = q.shape[0], q.shape[1]
+        Kv = v.shape[4]
+        if out is None:
+            out = torch.empty((B, M, G, Hg, Kv), dtype=torch.bfloat16, device=q.device)
+        if lse is True:
+            lse = torch.empty((B, G, Hg, M), dtype=torch.float32, device=q.device)
+        elif lse is False:
+            lse = None
+        attn_fwd(q4, k4, v4, mask=mask, scale=scale, cu_seqlens_q=cu_seqlens_q,
+                 cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                 out=_merge_heads(out, "out"), lse=False if lse is None else lse.view(B, G * Hg, M),
+                 stream=stream, bottom_right=bottom_right, window_left=window_left,
+                 window_right=window_right, independent=independent)
+        return out, lse
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
     _check_inputs(q, k, v)
     Hkv = _kv_heads(q, k, v)
@@ -388,6 +454,19 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
     this one on the stream (e.g. the previous chunk of the same split): the call may then
     start while that launch finishes.
     """
+    if q.dim() == 5:  # BMGHK: out [B,M,G,H,Kv], lse [B,G,H,M] over flattened views
+        q4, k4, v4, G, Hg = _bmghk(q, k, v)
+        B, M = q.shape[0], q.shape[1]
+        if out is None:
+            out = torch.empty((B, M, G, Hg, v.shape[4]), dtype=out_dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, G, Hg, M), dtype=torch.float32, device=q.device)
+        attn_partial(q4, k4, v4, mask=mask, scale=scale, kv_offset=kv_offset,
+                     cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
+                     max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, out_dtype=out_dtype,
+                     out=_merge_heads(out, "out"), lse=lse.view(B, G * Hg, M), stream=stream,
+                     window_left=window_left, window_right=window_right, independent=independent)
+        return out, lse
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
     _check_inputs(q, k, v)
     Hkv = _kv_heads(q, k, v)
@@ -428,42 +507,69 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
     return out, lse
 
 
-def _stacked(parts, what):
-    """A list of equally spaced same-shape tensors -> (base tensor, chunk stride) without copies."""
+def _stacked(parts):
+    """Chunks as (base tensor, chunk stride, n), or None when they are not equally spaced
+    views of one allocation (then the varargs merge reads them where they lie)."""
     if isinstance(parts, torch.Tensor):
         return parts[0], (parts.stride(0) if parts.shape[0] > 1 else 0), parts.shape[0]
-    parts = list(parts)
-    if not parts:
-        raise MslkError(_capi.MSLK_ERR_INVALID_ARG, f"merge_attentions: no {what} chunks")
     base = parts[0]
-    es = base.element_size()
     if len(parts) == 1:
         return base, 0, 1
+    es = base.element_size()
     d = parts[1].data_ptr() - base.data_ptr()
     ok = d > 0 and d % es == 0 and all(
         p.shape == base.shape and p.stride() == base.stride() and p.dtype == base.dtype and
         p.data_ptr() - base.data_ptr() == i * d for i, p in enumerate(parts))
-    if not ok:  # not one strided allocation: stack them (argument marshalling)
-        st = torch.stack(parts)
-        return st[0], st.stride(0), st.shape[0]
-    return base, d // es, len(parts)
+    return (base, d // es, len(parts)) if ok else None
+
+
+def _flat_chunk(o, what):
+    """A 5-D BMGHK chunk output [B,M,G,H,Kv] (or lse [B,G,H,M]) as its 4-D / 3-D view."""
+    if what == "out" and o.dim() == 5:
+        return _merge_heads(o, "out_split chunk")
+    if what == "lse" and o.dim() == 4:
+        return o.view(o.shape[0], o.shape[1] * o.shape[2], o.shape[3])
+    return o
 
 
 def merge_attentions(out_split, lse_split, *, write_lse=True, output_dtype=torch.bfloat16,
                      out=None, lse=None, stream=None):
-    """Exact LSE merge of chunk results (stacked [n,B,M,H,Kv] fp32, or a list of chunks).
+    """Exact LSE merge of chunk results; returns (out, lse) with lse None when ``write_lse``
+    is False.
 
-    Returns (out, lse) with lse None when ``write_lse`` is False.
+    ``out_split`` is a stacked fp32 tensor [n,B,M,H,Kv] or a list of n chunk tensors
+    [B,M,H,Kv] (5-D BMGHK chunks [B,M,G,H,Kv] with lse [B,G,H,M] give a 5-D result);
+    ``lse_split`` likewise [n,B,H,M] or a list.  Equally spaced views of one allocation go
+    to the stacked merge; separately allocated chunks go to the varargs merge, which reads
+    each chunk where it lies (nothing is copied or stacked).
     """
-    o0, cs_o, n = _stacked(out_split, "output")
-    l0, cs_l, n_l = _stacked(lse_split, "lse")
-    if n != n_l:
+    outs = list(out_split.unbind(0)) if isinstance(out_split, torch.Tensor) else list(out_split)
+    lses = list(lse_split.unbind(0)) if isinstance(lse_split, torch.Tensor) else list(lse_split)
+    if not outs:
+        raise MslkError(_capi.MSLK_ERR_INVALID_ARG, "merge_attentions: no chunks")
+    if len(outs) != len(lses):
         raise ValueError("different numbers of output and lse chunks")
-    if o0.dtype != torch.float32 or l0.dtype != torch.float32:
+    five = outs[0].dim() == 5
+    if five:
+        B, M, G, Hg, Kv = outs[0].shape
+        if out is None:
+            out = torch.empty((B, M, G, Hg, Kv), dtype=output_dtype, device=outs[0].device)
+        if write_lse and lse is None:
+            lse = torch.empty((B, G, Hg, M), dtype=torch.float32, device=outs[0].device)
+        merge_attentions([_flat_chunk(o, "out") for o in outs], [_flat_chunk(x, "lse") for x in lses],
+                         write_lse=write_lse, output_dtype=output_dtype, out=_merge_heads(out, "out"),
+                         lse=None if not write_lse else lse.view(B, G * Hg, M), stream=stream)
+        return out, (lse if write_lse else None)
+    o0, l0 = outs[0], lses[0]
+    if any(o.dtype != torch.float32 for o in outs) or any(x.dtype != torch.float32 for x in lses):
         raise ValueError("chunk outputs and lse must be float32")
-    if not l0.is_contiguous():
+    if any(not x.is_contiguous() for x in lses):
         raise ValueError("each lse chunk must be a contiguous [B,H,M] tensor")
     B, M, H, Kv = o0.shape
+    if any(o.shape != o0.shape or o.stride() != o0.stride() for o in outs):
+        raise ValueError("every chunk output must have the same shape and strides")
+    if any(x.shape != (B, H, M) for x in lses):
+        raise ValueError(f"each lse chunk must be [B,H,M] = {(B, H, M)}")
     if output_dtype not in _DTYPES:
         raise ValueError("output_dtype must be torch.bfloat16 or torch.float32")
     if out is None:
@@ -475,10 +581,80 @@ def merge_attentions(out_split, lse_split, *, write_lse=True, output_dtype=torch
     ss = _bmhk_strides(o0, "out_split")
     so = _bmhk_strides(out, "out")
     lib = _capi.load()
-    check(lib.mslk_merge_attentions(o0.data_ptr(), l0.data_ptr(), n, cs_o, cs_l, B, M, H, Kv,
-                                    ctypes.byref(ss), ctypes.byref(so), out.data_ptr(),
-                                    _DTYPES[out.dtype], _ptr(lse), _stream_handle(stream, o0.device)))
+    st_o = out_split if isinstance(out_split, torch.Tensor) else outs
+    st_l = lse_split if isinstance(lse_split, torch.Tensor) else lses
+    so_, sl_ = _stacked(st_o), _stacked(st_l)
+    if so_ is not None and sl_ is not None:
+        (ob, cs_o, n), (lb, cs_l, _) = so_, sl_
+        check(lib.mslk_merge_attentions(ob.data_ptr(), lb.data_ptr(), n, cs_o, cs_l, B, M, H, Kv,
+                                        ctypes.byref(ss), ctypes.byref(so), out.data_ptr(),
+                                        _DTYPES[out.dtype], _ptr(lse),
+                                        _stream_handle(stream, o0.device)))
+        return out, lse
+    n = len(outs)
+    if n > _capi.MERGE_MAX_VARARGS:
+        raise ValueError(f"at most {_capi.MERGE_MAX_VARARGS} separately allocated chunks")
+    optrs = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    lptrs = (ctypes.c_void_p * n)(*[x.data_ptr() for x in lses])
+    check(lib.mslk_merge_attentions_varargs(optrs, lptrs, n, B, M, H, Kv, ctypes.byref(ss),
+                                            ctypes.byref(so), out.data_ptr(), _DTYPES[out.dtype],
+                                            _ptr(lse), _stream_handle(stream, o0.device)))
     return out, lse
+
+
+def splitk_size(batch: int, seqlen_kv: int, kv_heads: int = 1, tile_n: int = 256,
+                sm_count: int | None = None) -> int:
+    """Keys per split-KV chunk (0: one split covers the keys); the library's rule for the
+    pages' get_splitk_heuristic, host-only (see mslk_splitk_size)."""
+    return int(_capi.load().mslk_splitk_size(int(batch), int(seqlen_kv), int(kv_heads), int(tile_n),
+                                             0 if sm_count is None else int(sm_count)))
+
+
+def attn_split_kv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, n_chunks: int = 0,
+                  mask="none", scale=None, out=None, lse=True, out_dtype=torch.bfloat16,
+                  workspace=None, stream=None, bottom_right=False, window_left=None,
+                  window_right=None):
+    """Exact split-KV attention in one library call: partials over ``n_chunks`` equal key
+    chunks (0: the split-size rule), then the merge.  Dense masks.  Returns (out, lse).
+
+    ``workspace`` (optional) is a uint8 CUDA tensor of at least ``split_kv_workspace_bytes``
+    bytes, 256-byte aligned; without it one is allocated here."""
+    q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
+    _check_inputs(q, k, v)
+    Hkv = _kv_heads(q, k, v)
+    B, M, H, K = q.shape
+    Kv = v.shape[3]
+    if out is None:
+        out = torch.empty((B, M, H, Kv), dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    a = _args(q, k, v, Hkv, _mask_kind(mask), scale, None, _band(bottom_right, window_left, window_right),
+              out, out.dtype, lse)
+    lib = _capi.load()
+    need = ctypes.c_size_t(0)
+    check(lib.mslk_attn_split_kv_workspace(ctypes.byref(a), int(n_chunks), ctypes.byref(need)))
+    if workspace is None:
+        workspace = torch.empty(max(need.value, 1), dtype=torch.uint8, device=q.device)
+    check(lib.mslk_attn_split_kv(ctypes.byref(a), int(n_chunks), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_handle(stream, q.device)))
+    return out, lse
+
+
+def split_kv_workspace_bytes(q, k, v, *, n_chunks: int = 0, mask="none", out_dtype=torch.bfloat16,
+                             bottom_right=False, window_left=None, window_right=None) -> int:
+    """Bytes of workspace ``attn_split_kv`` needs for these tensors and chunk count."""
+    q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
+    Hkv = _kv_heads(q, k, v)
+    B, M, H, K = q.shape
+    out = torch.empty((B, M, H, v.shape[3]), dtype=out_dtype, device="meta")
+    a = _args(q, k, v, Hkv, _mask_kind(mask), None, None, _band(bottom_right, window_left, window_right),
+              out, out_dtype, None, ptrs=False)
+    need = ctypes.c_size_t(0)
+    check(_capi.load().mslk_attn_split_kv_workspace(ctypes.byref(a), int(n_chunks), ctypes.byref(need)))
+    return int(need.value)
 
 
 def device_status(stream=None) -> int:
@@ -509,6 +685,7 @@ def version() -> int:
 
 
 __all__: Sequence[str] = [
-    "attn_fwd", "attn_partial", "merge_attentions", "device_status", "set_wait_timeout_ns",
+    "attn_fwd", "attn_partial", "merge_attentions", "attn_split_kv", "split_kv_workspace_bytes",
+    "splitk_size", "device_status", "set_wait_timeout_ns",
     "diag_bounded_wait", "set_path_policy", "last_error", "version", "MslkError", "MASKS",
 ]

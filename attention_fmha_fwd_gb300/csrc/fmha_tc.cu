@@ -81,14 +81,25 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kQTiles = 2;
 constexpr int kUnitRows = kQTiles * kBlockM;
-constexpr int kThreads = 320;
-constexpr int kWarpMma = 8;
-constexpr int kWarpLoad = 9;
+constexpr int kThreads = 512;
+constexpr int kWarpOut = 8;   // warps 8-11: the output warpgroup
+constexpr int kWarpMma = 12;
+constexpr int kWarpLoad = 13;
+// Registers per thread after the warpgroups rebalance (setmaxnreg).  Each scheduler
+// partition holds one warp of every warpgroup, so the four shares add up to its 16384
+// registers: 176 + 176 (softmax) + 96 (output) + 64 (MMA / TMA) = 512 per lane.
+constexpr int kRegsSoftmax = 176;
+constexpr int kRegsOut = 96;
+constexpr int kRegsIssue = 64;
+static_assert(2 * kRegsSoftmax + kRegsOut + kRegsIssue == 65536 / 4 / 32, "register split");
 constexpr int kTmemCols = 512;
 constexpr int kSwizzleAtom = 16384;  // one 64-column K-block of a 128-row tile (bytes)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest un-rescaled p (256)
+// P published in two halves of 64 keys (the first half's P.V MMAs start while the second
+// half's exponentials run), or all at once.
+constexpr bool kHalfP = true;
 
 // F8: q, k, v are E4M3 bytes; a 128-wide row is then one 128-byte swizzle atom.
 template <int D, bool F8>
@@ -99,18 +110,19 @@ struct Layout {
   static constexpr int kStages = kTileBytes == 32768 ? 4 : 8;  // a 128 KiB K/V ring
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
-  // Output staging: one 16 KiB buffer per softmax warpgroup (128 rows x 128 bytes, the
+  // Output staging: one 16 KiB buffer for the output warpgroup (128 rows x 128 bytes, the
   // 128-byte-swizzled layout of one TMA store box).
   static constexpr int kStageOutBytes = kBlockM * 128;
   static constexpr int kOutOff = kKVOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kOutOff + kQTiles * kStageOutBytes;
-  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2],
-  // o_free[2], drain, split_full, split_empty
-  static constexpr int kNumBars = 4 + 2 * kStages + 8 + 1 + 2;
+  static constexpr int kBarOff = kOutOff + kStageOutBytes;
+  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_half[2], p_full[2],
+  // o_done[2], o_free[2], st_full[2], st_empty[2], drain
+  static constexpr int kNumBars = 4 + 2 * kStages + 14 + 1;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // abort flag, tmem slot
-  // Split units: Q tile 1's row max and sum for Q tile 0's merge, [row][2] fp32.
-  static constexpr int kSplitOff = kMiscOff + 16;
-  static constexpr int kBytes = kSplitOff + kBlockM * 8;
+  // Row statistics a softmax warpgroup hands to the output warpgroup at a unit's end:
+  // [Q tile][row] (running max, running sum), fp32.
+  static constexpr int kStatsOff = kMiscOff + 16;
+  static constexpr int kBytes = kStatsOff + kQTiles * kBlockM * 8;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
 
@@ -225,20 +237,27 @@ MSLK_DEV void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
 // per MMA (16 bf16 keys, or 32 E4M3 keys); V is read MN-major: 8-key groups 1024 bytes
 // apart (SBO), 128-byte column blocks of the head dim 16 KiB apart (LBO; bf16 has two);
 // one MMA's keys span 2048 (bf16) or 4096 (E4M3) bytes.
+// Half h of the tile's keys ([64 h, 64 h + 64)): the softmax publishes P in two halves so
+// the first half's MMAs run while the second half's exponentials are computed.
 template <int D, bool F8>
-MSLK_DEV void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t accumulate) {
+MSLK_DEV void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t accumulate,
+                            int h) {
   if constexpr (F8) {
     constexpr uint32_t idesc = idesc_e4m3_f32(kBlockM, D, true);
 #pragma unroll
-    for (int kk = 0; kk < kBlockN / 32; ++kk)
+    for (int i = 0; i < kBlockN / 64; ++i) {
+      const int kk = h * (kBlockN / 64) + i;
       mma_f8_ts_elect(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint32_t>(kk * 4096 / 16),
                       idesc, kk > 0 ? 1u : accumulate);
+    }
   } else {
     constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, D, true);
 #pragma unroll
-    for (int kk = 0; kk < kBlockN / 16; ++kk)
+    for (int i = 0; i < kBlockN / 32; ++i) {
+      const int kk = h * (kBlockN / 32) + i;
       mma_f16_ts_elect(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint32_t>(kk * 2048 / 16),
                        idesc, kk > 0 ? 1u : accumulate);
+    }
   }
 }
 
@@ -380,7 +399,9 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned, derived from the shared array itself so accesses stay shared-space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int warp = threadIdx.x / 32;
+  // (broadcast from lane 0: the compiler then knows the role branches are warp-uniform,
+  // which the per-role register budgets below rely on)
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
   const int G = gridDim.x;
   // A following launch declared independent of this one may start now (the others wait
@@ -397,13 +418,15 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
   auto kv_full = [&](int s) { return bar0 + 8u * (4 + s); };
   auto kv_empty = [&](int s) { return bar0 + 8u * (4 + L::kStages + s); };
   auto s_full = [&](int t) { return bar0 + 8u * (4 + 2 * L::kStages + t); };
-  auto p_full = [&](int t) { return bar0 + 8u * (6 + 2 * L::kStages + t); };
-  auto o_done = [&](int t) { return bar0 + 8u * (8 + 2 * L::kStages + t); };
-  auto o_free = [&](int t) { return bar0 + 8u * (10 + 2 * L::kStages + t); };
-  const uint32_t bar_drain = bar0 + 8u * (12 + 2 * L::kStages);
-  // split units: Q tile 1's row max and sum are in the slot / tile 0 has read them
-  const uint32_t split_full = bar0 + 8u * (13 + 2 * L::kStages);
-  const uint32_t split_empty = bar0 + 8u * (14 + 2 * L::kStages);
+  // P_t's first 64 keys / all 128 are in tensor memory (the PV MMAs over them may start)
+  auto p_half = [&](int t) { return bar0 + 8u * (6 + 2 * L::kStages + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (8 + 2 * L::kStages + t); };
+  auto o_done = [&](int t) { return bar0 + 8u * (10 + 2 * L::kStages + t); };  // O_t final
+  auto o_free = [&](int t) { return bar0 + 8u * (12 + 2 * L::kStages + t); };  // O_t read out
+  // softmax warpgroup t wrote its rows' max and sum / the output warpgroup read them
+  auto st_full = [&](int t) { return bar0 + 8u * (14 + 2 * L::kStages + t); };
+  auto st_empty = [&](int t) { return bar0 + 8u * (16 + 2 * L::kStages + t); };
+  const uint32_t bar_drain = bar0 + 8u * (18 + 2 * L::kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff + 8);
   const WaitCtl wc{abort_flag, a.err, a.timeout_ns};
@@ -424,12 +447,13 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
       mbar_init(p_full(t), kBlockM / 32);  // one arrival per softmax warp
+      mbar_init(p_half(t), kBlockM / 32);
       mbar_init(o_done(t), 1);
-      mbar_init(o_free(t), kBlockM / 32);
+      mbar_init(o_free(t), kBlockM / 32);  // one arrival per output warp
+      mbar_init(st_full(t), kBlockM / 32);
+      mbar_init(st_empty(t), kBlockM / 32);
     }
     mbar_init(bar_drain, 1);
-    mbar_init(split_full, kBlockM / 32);   // one arrival per warp of Q tile 1
-    mbar_init(split_empty, kBlockM / 32);  // one arrival per warp of Q tile 0
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -449,6 +473,8 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp >= kWarpMma) {
+    setmaxnreg_dec<kRegsIssue>();  // MMA, TMA and two idle warps
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer (whole warp)
     // Order per unit: Q0, K_lo, Q1, V_lo, K_lo+1, V_lo+1, ...  Each Q tile waits only for its own
@@ -527,7 +553,18 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
     Unit u;
     int ku = 0;
     bool have = next_unit(0, ku, u);
-    bool s0_issued = false;  // the unit's first S0 was issued at the end of the previous unit
+    bool s0_issued = false;  // the unit's first S0 was issued during the previous unit
+    // The next unit's first S0 (its Q0 was loaded after this unit's last S0 MMA; its first K
+    // is ring entry ikn).  S0 is free: this unit's last PV0 precedes it in issue order.
+    auto issue_next_s0 = [&](const Unit& un, int ikn) {
+      if (!(ok = wait_bar_warp(q_full(0), (uc + 1) & 1, wc))) return;
+      if (!(ok = wait_bar_warp(kv_full(ikn % L::kStages), (ikn / L::kStages) & 1, wc))) return;
+      tc_fence_after();
+      issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(ikn % L::kStages));
+      mma_commit_elect(s_full(0));
+      if (un.last(0) == un.jlo) mma_commit_elect(q_empty(0));
+      s0_issued = true;
+    };
     while (have && ok) {
       Unit un;
       int kn = 0;
@@ -595,10 +632,13 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
             if (j + 1 == (tn ? last1 : last0)) mma_commit_elect(q_empty(tn));
           }
           const int lo_j = tj ? lo1 : lo0;
-          if (!(ok = wait_bar_warp(p_full(tj), (tj ? jg1 : jg0) & 1, wc))) break;
+          if (!(ok = wait_bar_warp(kHalfP ? p_half(tj) : p_full(tj), (tj ? jg1 : jg0) & 1, wc))) break;
           if (j == lo_j && !(ok = wait_bar_warp(o_free(tj), ((tj ? uc1 : uc0) & 1) ^ 1, wc))) break;
           tc_fence_after();
-          issue_pv<D, F8>(tm_o[tj], tm_s[tj], kv_vdesc(sv), j > lo_j ? 1u : 0u);
+          issue_pv_half<D, F8>(tm_o[tj], tm_s[tj], kv_vdesc(sv), j > lo_j ? 1u : 0u, 0);
+          if (!(ok = wait_bar_warp(p_full(tj), (tj ? jg1 : jg0) & 1, wc))) break;
+          tc_fence_after();
+          issue_pv_half<D, F8>(tm_o[tj], tm_s[tj], kv_vdesc(sv), 1u, 1);
           // o_done(0) after the unit's last PV of either tile: O_0 and O_1 both final
           // (tile 0 merges them; o_done(1) has no phase in split units)
           if (!more) mma_commit_elect(o_done(0));
@@ -608,12 +648,22 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         } else {
           // Q tile 0 (when key tile j is one of its tiles): PV0_j, then S0_{j+1}
           if (u.has(0, j)) {
-            if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
+            if (!(ok = wait_bar_warp(kHalfP ? p_half(0) : p_full(0), jg0 & 1, wc))) break;
             if (j == lo0 && !(ok = wait_bar_warp(o_free(0), (uc0 & 1) ^ 1, wc))) break;
             tc_fence_after();
-            issue_pv<D, F8>(tm_o[0], tm_s[0], kv_vdesc(sv), j > lo0 ? 1u : 0u);
+            issue_pv_half<D, F8>(tm_o[0], tm_s[0], kv_vdesc(sv), j > lo0 ? 1u : 0u, 0);
+            if (!(ok = wait_bar_warp(p_full(0), jg0 & 1, wc))) break;
+            tc_fence_after();
+            issue_pv_half<D, F8>(tm_o[0], tm_s[0], kv_vdesc(sv), 1u, 1);
             if (j == last0) mma_commit_elect(o_done(0));
             ++jg0;
+          }
+          if (!more && j == last0 && have_next && un.has(0)) {
+            // Both tiles end here: the next unit's S0 goes ahead of PV1, so softmax 0
+            // starts the next unit while softmax 1 finishes this one.  (Its first K
+            // follows V_j in the ring: entry it.)
+            issue_next_s0(un, it);
+            if (!ok) break;
           }
           if (more) {
             if (!(ok = wait_bar_warp(kv_full(sk), (ik / L::kStages) & 1, wc))) break;
@@ -626,10 +676,13 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           }
           // Q tile 1: PV1_j, then S1_{j+1}
           if (u.has(1, j)) {
-            if (!(ok = wait_bar_warp(p_full(1), jg1 & 1, wc))) break;
+            if (!(ok = wait_bar_warp(kHalfP ? p_half(1) : p_full(1), jg1 & 1, wc))) break;
             if (j == lo1 && !(ok = wait_bar_warp(o_free(1), (uc1 & 1) ^ 1, wc))) break;
             tc_fence_after();
-            issue_pv<D, F8>(tm_o[1], tm_s[1], kv_vdesc(sv), j > lo1 ? 1u : 0u);
+            issue_pv_half<D, F8>(tm_o[1], tm_s[1], kv_vdesc(sv), j > lo1 ? 1u : 0u, 0);
+            if (!(ok = wait_bar_warp(p_full(1), jg1 & 1, wc))) break;
+            tc_fence_after();
+            issue_pv_half<D, F8>(tm_o[1], tm_s[1], kv_vdesc(sv), 1u, 1);
             if (j == last1) mma_commit_elect(o_done(1));
             ++jg1;
           }
@@ -641,20 +694,20 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
               if (j + 1 == last1) mma_commit_elect(q_empty(1));  // the unit's last S1 MMA was issued
             }
             mma_commit_elect(kv_empty(sk));
+            if (j == last0 && j + 2 == jhi && have_next && un.has(0)) {
+              // Q tile 0 is done one key tile before Q tile 1 (causal): the next unit's S0
+              // runs while softmax 1 works on this unit's last tile.  Ring: V_{j+1} is entry
+              // it, the next unit's first K entry it + 1 (within the ring: it - 3 was waited on).
+              issue_next_s0(un, it + 1);
+              if (!ok) break;
+            }
           }
         }
-        if (!more && have_next && un.has(0)) {
-          // The next unit's first S0 right behind this unit's last PV (its Q0 was loaded
-          // after this unit's last S0 MMA), before this warp decodes units and waits for
-          // Q1.  S0 is free: this unit's last PV0 precedes it in issue order.
-          const int ikn = it;  // the next unit's first K follows V_{jhi-1} in the ring
-          if (!(ok = wait_bar_warp(q_full(0), (uc + 1) & 1, wc))) break;
-          if (!(ok = wait_bar_warp(kv_full(ikn % L::kStages), (ikn / L::kStages) & 1, wc))) break;
-          tc_fence_after();
-          issue_qk<D, F8>(tm_s[0], q_desc[0], kv_kdesc(ikn % L::kStages));
-          mma_commit_elect(s_full(0));
-          if (un.last(0) == un.jlo) mma_commit_elect(q_empty(0));
-          s0_issued = true;
+        if (!more && have_next && un.has(0) && !s0_issued) {
+          // Otherwise the next unit's first S0 right behind this unit's last PV, before this
+          // warp decodes units and waits for Q1 (its first K follows V_{jhi-1}: entry it).
+          issue_next_s0(un, it);
+          if (!ok) break;
         }
       }
       if (!ok) break;
@@ -669,16 +722,17 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       mma_commit_elect(bar_drain);
       wait_bar_warp(bar_drain, 0, wc, false);
     }
-  } else {
+  }
+  } else if (warp < kWarpOut) {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp / 4;                   // Q tile
     const int row_in_tile = (warp % 4) * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t ts = tmem + static_cast<uint32_t>(t * 128) + lane_bits;
     const uint32_t to = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_bits;
-    // Barrier phase parities, one register: bit 0 o_done(t) (units in which this Q tile
-    // has keys and writes the output), bit 1 s_full(t) (this tile's key tiles), bit 2
-    // split_full / split_empty (split units).
+    // Barrier phase parities, one register: bit 1 s_full(t) (this tile's key tiles), bit 2
+    // st_empty(t) (units in which this tile handed row statistics over).
     uint32_t ph = 0;
     bool ok = true;
     for (int k = 0; k < n_rounds && ok; ++k) {
@@ -698,22 +752,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         const int hq = a.fold ? u.h * a.fold + min(r, a.fold - 1) : u.h;  // this row's query head
         sl2 *= a.dq[a.desc_per_tensor ? 0 : hq] * a.dk[a.desc_per_tensor ? 0 : u.hk];
       }
-      if (n_t <= 0) {  // no allowed key for any row of this Q tile
-        if (valid) {
-          for (int c = 0; c < a.d_out; c += 4) {
-            if (a.out_fp32) {
-              float* o = static_cast<float*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + c;
-              *reinterpret_cast<float4*>(o) = make_float4(0.f, 0.f, 0.f, 0.f);
-            } else {
-              __nv_bfloat16* o =
-                  static_cast<__nv_bfloat16*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + c;
-              *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
-            }
-          }
-          if (a.lse != nullptr) a.lse[u.qb * a.lse_sb + u.h * a.lse_sh + row * a.lse_sm] = -INFINITY;
-        }
-        continue;
-      }
+      if (n_t <= 0) continue;  // no allowed key for any row: the output warpgroup writes them
       float m_run = -INFINITY;
       float l_run = 0.f;
       for (int j = 0; j < n_t; ++j, ph ^= 2u) {
@@ -739,34 +778,46 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           lim_c = max(-1, min(min(u.Lk - 1, pos + u.hi) - key0, kBlockN - 1));
           if constexpr (kLowerEdge) lim_lo = max(0, min(max(0, pos + u.lo) - key0, kBlockN));
         }
-        // The whole S row comes out of tensor memory in one load (128 registers): mask it
-        // (only tiles crossing a mask limit), take the row max, then form
-        // p = 2^(s*scale*log2e - m) and the row sum and write P as bf16 pairs over S's first
-        // 64 columns, a quarter (16 columns) at a time.
+        // The whole S row comes out of tensor memory in one load (128 registers).  On a
+        // tile that crosses a mask limit each 32-column quarter is classified: allowed
+        // whole (left alone), masked whole, or cut (masked column by column), so a causal
+        // diagonal tile masks one quarter per warp instead of all four.  Then the row max,
+        // the lazy rescale of O, and p = 2^(s*scale*log2e - m) with the row sum; P goes to
+        // S's first 64 columns as bf16 pairs, published in two halves of 64 keys so the
+        // MMA warp starts P.V on the first half while the second is computed.
         uint32_t sr[128];
-        tmem_ld_32x32b_x128(ts, sr);
+        tmem_ld_32x32b_x64_nowait(ts, sr);
+        tmem_ld_32x32b_x64_nowait(ts + 64, sr + 64);
+        tmem_ld_wait();
         if (need_mask) {
-          // One allowed-column bit word per 32 columns, then a bit test per column:
-          // -inf is excluded from the max and 2^-inf = 0.
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t w = low_bits(lim_c + 1 - 32 * q4);
             if constexpr (kLowerEdge) w &= ~low_bits(lim_lo - 32 * q4);
+            if (w == 0u) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (!((w >> c) & 1u)) sr[32 * q4 + c] = 0xFF800000u;
+              for (int c = 0; c < 32; ++c) sr[32 * q4 + c] = 0xFF800000u;  // -inf: 2^-inf = 0
+            } else if (w != 0xffffffffu) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (!((w >> c) & 1u)) sr[32 * q4 + c] = 0xFF800000u;
+            }
           }
         }
-        float mx8[8];
+        float qm[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmax3(u2f(sr[e]), u2f(sr[8 + e]), u2f(sr[16 + e]));
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float m4[4];
 #pragma unroll
-        for (int c = 24; c < 120; c += 16)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], u2f(sr[c + e]), u2f(sr[c + 8 + e]));
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], u2f(sr[120 + e]));
-        const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7])));
+          for (int e = 0; e < 4; ++e) {
+            const int c = 32 * q4 + e;
+            m4[e] = fmax3(fmax3(u2f(sr[c]), u2f(sr[c + 4]), u2f(sr[c + 8])),
+                          fmax3(u2f(sr[c + 12]), u2f(sr[c + 16]), u2f(sr[c + 20])),
+                          fmaxf(u2f(sr[c + 24]), u2f(sr[c + 28])));
+          }
+          qm[q4] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
+        const float mx = fmaxf(fmaxf(qm[0], qm[1]), fmaxf(qm[2], qm[3]));
         const float m_new = fmaxf(m_run, mx * sl2);
         const bool rescale = m_new > m_run + kRescaleThreshold;
         float alpha = 1.f;
@@ -785,30 +836,53 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
             // P as E4M3, four per column, over S's first 32 columns.  p <= 2^8 (the lazy
             // rescale bound) stays inside E4M3's range (448).
             uint32_t pk[8];
+            {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int c = qtr * 32 + 4 * e;
-              const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
-              const float2 y = unpack_f2(ffma2(pack_f2(u2f(sr[c + 2]), u2f(sr[c + 3])), sl2x2, nmx2));
-              const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-              const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
-              rs2[(2 * e) % 4] = fadd2(rs2[(2 * e) % 4], pack_f2(p0, p1));
-              rs2[(2 * e + 1) % 4] = fadd2(rs2[(2 * e + 1) % 4], pack_f2(p2, p3));
-              pk[e] = pack_e4m3x4(p0, p1, p2, p3);
+              for (int e = 0; e < 8; ++e) {
+                const int c = qtr * 32 + 4 * e;
+                const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
+                const float2 y = unpack_f2(ffma2(pack_f2(u2f(sr[c + 2]), u2f(sr[c + 3])), sl2x2, nmx2));
+                const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
+                rs2[(2 * e) % 4] = fadd2(rs2[(2 * e) % 4], pack_f2(p0, p1));
+                rs2[(2 * e + 1) % 4] = fadd2(rs2[(2 * e + 1) % 4], pack_f2(p2, p3));
+                pk[e] = pack_e4m3x4(p0, p1, p2, p3);
+              }
             }
             tmem_st_32x32b_x8(ts + qtr * 8, pk);
           } else {
             uint32_t pk[16];
+            {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int c = qtr * 32 + 2 * e;
-              const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
-              const float p0 = ex2_approx(x.x);
-              const float p1 = ex2_approx(x.y);
-              rs2[e % 4] = fadd2(rs2[e % 4], pack_f2(p0, p1));
-              pk[e] = pack_bf16x2(p0, p1);
+              for (int e = 0; e < 16; ++e) {
+                const int c = qtr * 32 + 2 * e;
+                const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
+                const float p0 = ex2_approx(x.x);
+                const float p1 = ex2_approx(x.y);
+                rs2[e % 4] = fadd2(rs2[e % 4], pack_f2(p0, p1));
+                pk[e] = pack_bf16x2(p0, p1);
+              }
             }
             tmem_st_32x32b_x16(ts + qtr * 16, pk);
+          }
+          if (qtr == 1 && j > 0 && __any_sync(0xffffffffu, rescale)) {
+            // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled, and
+            // PV_t(j) is not issued before this warpgroup publishes P's first half.
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 8) {
+              uint32_t o[8];
+              tmem_ld_32x32b_x8(to + c0, o);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = f2u(u2f(o[e]) * alpha);
+              tmem_st_32x32b_x8(to + c0, o);
+            }
+          }
+          if ((kHalfP && qtr == 1) || qtr == 3) {
+            // keys [0, 64) (qtr 1) or all 128 (qtr 3) of P_t are in tensor memory
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qtr == 1 ? p_half(t) : p_full(t));  // one arrival per warp
           }
         }
         {
@@ -816,183 +890,205 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           const float2 r1 = unpack_f2(fadd2(rs2[2], rs2[3]));
           l_run += (r0.x + r0.y) + (r1.x + r1.y);
         }
-        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-          // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled, and
-          // PV_t(j) is not issued before this warpgroup arrives on p_full.
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(to + c0, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * alpha);
-            tmem_st_32x32b_x32(to + c0, o);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(t));  // one arrival per warp
       }
-      float2* const split_row = reinterpret_cast<float2*>(smem + L::kSplitOff) + row_in_tile;
-      if (split && t == 1) {
-        // Split unit: hand this row's max and sum to Q tile 0, which merges O_1 into its
-        // output (once tile 0 has read the previous split unit's).
-        ok = ok && __all_sync(0xffffffffu, wait_bar(split_empty, ((ph >> 2) & 1u) ^ 1u, wc));
-        if (!ok) break;
-        *split_row = make_float2(m_run, l_run);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(split_full);
-        ph ^= 4u;
-        continue;
-      }
-
-      // ---- epilogue: wait for the unit's last PV_t (split: both tiles' last PV), read
-      // O_t, hand it back, then store.
-      ok = ok && __all_sync(0xffffffffu, wait_bar(o_done(t), ph & 1u, wc));
-      // split unit: O_1 (tile 1's alternate key tiles) and its row max and sum merge in
-      float c0 = 1.f, c1 = 0.f, m_out = m_run, l_out = l_run;
-      if (split) {
-        ok = ok && __all_sync(0xffffffffu, wait_bar(split_full, (ph >> 2) & 1u, wc));
-        if (!ok) break;
-        const float2 ml1 = *split_row;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(split_empty);
-        ph ^= 4u;
-        m_out = fmaxf(m_run, ml1.x);
-        c0 = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - m_out);
-        c1 = (ml1.x == -INFINITY) ? 0.f : ex2_approx(ml1.x - m_out);
-        l_out = l_run * c0 + ml1.y * c1;
-      }
+      // Hand the row's max and sum to the output warpgroup (once it has read the previous
+      // unit's) and go straight on to the next unit: the output warpgroup normalises and
+      // stores O_t while this warpgroup's next tiles run.
+      ok = ok && __all_sync(0xffffffffu, wait_bar(st_empty(t), ((ph >> 2) & 1u) ^ 1u, wc));
       if (!ok) break;
+      reinterpret_cast<float2*>(smem + L::kStatsOff)[t * kBlockM + row_in_tile] = make_float2(m_run, l_run);
       __syncwarp();
-      tc_fence_after();
-      float inv_l = (l_out > 0.f) ? 1.f / l_out : 0.f;
-      if constexpr (F8) inv_l *= a.dv[a.desc_per_tensor ? 0 : u.hk];
-      c0 *= inv_l;
-      c1 *= inv_l;
-      const uint32_t to1 = tmem + 384u + lane_bits;  // O_1 (split units)
-      // Output tiles go through this warpgroup's staging buffer and one TMA store per
-      // 128-byte column band, except the tail tile of a packed sequence (a whole 128-row
-      // box would spill into the next sequence), which is stored row by row.
-      // (folded rows: the view's row extent is r, so a 128-row box is clipped there)
-      const bool use_tma = a.tma_store && (a.fold || !(a.varlen && row_first + kBlockM > u.Lq));
-      const bool leader = (warp % 4) == 0 && lane == 0;
-      uint8_t* stage = smem + L::kOutOff + t * L::kStageOutBytes + row_in_tile * 128;
-      const uint32_t stage_base = s_base + L::kOutOff + t * L::kStageOutBytes;
-      if (a.out_fp32) {
-        // 4-byte outputs: bands of 32 columns
-        const int n_bands = (a.d_out + 31) / 32;
+      if (lane == 0) mbar_arrive(st_full(t));
+      ph ^= 4u;
+    }
+  } else {
+    setmaxnreg_dec<kRegsOut>();
+    // ------------------------------------------------------------ output warpgroup
+    // Per unit and Q tile: wait for O_t to be final and for the softmax warpgroup's row
+    // statistics, read O_t out of tensor memory (then it may take the next unit's P.V),
+    // normalise, and store through the staging buffer with TMA stores.  Split units merge
+    // O_1 and Q tile 1's statistics into Q tile 0's rows by log-sum-exp.
+    const int row_in_tile = (warp % 4) * 32 + lane;
+    const uint32_t lane_bits = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const float2* const stats = reinterpret_cast<const float2*>(smem + L::kStatsOff);
+    const bool leader = warp == kWarpOut && lane == 0;
+    uint8_t* stage = smem + L::kOutOff + row_in_tile * 128;
+    const uint32_t stage_base = s_base + L::kOutOff;
+    int od[2] = {0, 0};  // o_done(t) phases consumed
+    int sc[2] = {0, 0};  // st_full(t) phases consumed
+    bool ok = true;
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int i = unit_at(k, cta, G);
+      Unit u;
+      if (i >= a.total_units || !decode_unit<kSplit>(a, i, u)) continue;
+      const bool split = u.step == 2;
 #pragma unroll 1
-        for (int band = 0; band < n_bands; ++band) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(to + band * 32, o);
-          if (split) {
-            uint32_t o1[32];
-            tmem_ld_32x32b_x32(to1 + band * 32, o1);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * c0 + u2f(o1[e]) * c1);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * c0);
-          }
-          if (band == n_bands - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
-              if (split) mbar_arrive(o_free(1));
+      for (int t = 0; t < (split ? 1 : kQTiles) && ok; ++t) {
+        const int row_first = u.row0(t);
+        const int r = row_first + row_in_tile;
+        const bool valid = r < u.Lq;
+        const long long row = static_cast<long long>(u.q_base) + r;
+        const int n_t = ((t == 0 ? u.thi[0] : u.thi[1]) - (t == 0 ? u.tlo[0] : u.tlo[1]) + u.step - 1) / u.step;
+        if (n_t <= 0) {  // no allowed key for any row of this Q tile
+          if (valid) {
+            for (int c = 0; c < a.d_out; c += 4) {
+              if (a.out_fp32) {
+                float* o = static_cast<float*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + c;
+                *reinterpret_cast<float4*>(o) = make_float4(0.f, 0.f, 0.f, 0.f);
+              } else {
+                __nv_bfloat16* o =
+                    static_cast<__nv_bfloat16*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + c;
+                *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
+              }
             }
+            if (a.lse != nullptr) a.lse[u.qb * a.lse_sb + u.h * a.lse_sh + row * a.lse_sm] = -INFINITY;
           }
-          if (use_tma) {
-            if (leader) bulk_wait_read0();  // the previous band's store has read the buffer
-            named_bar_sync(1 + t, kBlockM);
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              const int chunk = (c / 4) ^ (row_in_tile & 7);  // 128-byte swizzle
-              *reinterpret_cast<float4*>(stage + chunk * 16) =
-                  make_float4(u2f(o[c]), u2f(o[c + 1]), u2f(o[c + 2]), u2f(o[c + 3]));
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(1 + t, kBlockM);
-            if (leader) {
-              tma_store_4d(&tm_o, stage_base, band * 32, u.q_base + row_first, u.h, u.qb);
-              bulk_commit();
-            }
-          } else if (valid) {
-            float* op = static_cast<float*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + band * 32;
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(op + c) =
-                  make_float4(u2f(o[c]), u2f(o[c + 1]), u2f(o[c + 2]), u2f(o[c + 3]));
-          }
+          continue;
         }
-      } else {
-        // bf16 outputs: bands of 64 columns
-        const int n_bands = (a.d_out + 63) / 64;  // a partial last band is clipped by the map
+        // O_t final (split units: after the unit's last P.V of either tile), then the stats
+        ok = __all_sync(0xffffffffu, wait_bar(o_done(t), od[t] & 1, wc));
+        ok = ok && __all_sync(0xffffffffu, wait_bar(st_full(t), sc[t] & 1, wc));
+        if (split) ok = ok && __all_sync(0xffffffffu, wait_bar(st_full(1), sc[1] & 1, wc));
+        if (!ok) break;
+        ++od[t];
+        const float2 ml0 = stats[t * kBlockM + row_in_tile];
+        const float2 ml1 = split ? stats[kBlockM + row_in_tile] : make_float2(-INFINITY, 0.f);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(st_empty(t));
+          if (split) mbar_arrive(st_empty(1));
+        }
+        ++sc[t];
+        if (split) ++sc[1];
+        const float m_out = fmaxf(ml0.x, ml1.x);
+        float c0 = (ml0.x == -INFINITY) ? 0.f : ex2_approx(ml0.x - m_out);
+        float c1 = (ml1.x == -INFINITY) ? 0.f : ex2_approx(ml1.x - m_out);
+        const float l_out = ml0.y * c0 + ml1.y * c1;
+        tc_fence_after();
+        float inv_l = (l_out > 0.f) ? 1.f / l_out : 0.f;
+        if constexpr (F8) inv_l *= a.dv[a.desc_per_tensor ? 0 : u.hk];
+        c0 *= inv_l;
+        c1 *= inv_l;
+        const uint32_t to = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_bits;
+        const uint32_t to1 = tmem + 384u + lane_bits;  // O_1 (split units)
+        // Output tiles go through the staging buffer and one TMA store per 128-byte column
+        // band, except the tail tile of a packed sequence (a whole 128-row box would spill
+        // into the next sequence), which is stored row by row.
+        // (folded rows: the view's row extent is r, so a 128-row box is clipped there)
+        const bool use_tma = a.tma_store && (a.fold || !(a.varlen && row_first + kBlockM > u.Lq));
+        if (a.out_fp32) {
+          // 4-byte outputs: bands of 32 columns
+          const int n_bands = (a.d_out + 31) / 32;
 #pragma unroll 1
-        for (int band = 0; band < n_bands; ++band) {
-          uint32_t o[64];
-          tmem_ld_32x32b_x64(to + band * 64, o);
-          if (split) {
-#pragma unroll
-            for (int hb = 0; hb < 64; hb += 32) {  // O_1 32 columns at a time (registers)
+          for (int band = 0; band < n_bands; ++band) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(to + band * 32, o);
+            if (split) {
               uint32_t o1[32];
-              tmem_ld_32x32b_x32(to1 + band * 64 + hb, o1);
+              tmem_ld_32x32b_x32(to1 + band * 32, o1);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[hb + e] = f2u(u2f(o[hb + e]) * c0 + u2f(o1[e]) * c1);
+              for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * c0 + u2f(o1[e]) * c1);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * c0);
             }
-          } else {
+            if (band == n_bands - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
+                if (split) mbar_arrive(o_free(1));
+              }
+            }
+            if (use_tma) {
+              if (leader) bulk_wait_read0();  // the previous band's store has read the buffer
+              named_bar_sync(1, kBlockM);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) o[e] = f2u(u2f(o[e]) * c0);
-          }
-          if (band == n_bands - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
-              if (split) mbar_arrive(o_free(1));
+              for (int c = 0; c < 32; c += 4) {
+                const int chunk = (c / 4) ^ (row_in_tile & 7);  // 128-byte swizzle
+                *reinterpret_cast<float4*>(stage + chunk * 16) =
+                    make_float4(u2f(o[c]), u2f(o[c + 1]), u2f(o[c + 2]), u2f(o[c + 3]));
+              }
+              fence_proxy_async_smem();
+              named_bar_sync(1, kBlockM);
+              if (leader) {
+                tma_store_4d(&tm_o, stage_base, band * 32, u.q_base + row_first, u.h, u.qb);
+                bulk_commit();
+              }
+            } else if (valid) {
+              float* op = static_cast<float*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + band * 32;
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4*>(op + c) =
+                    make_float4(u2f(o[c]), u2f(o[c + 1]), u2f(o[c + 2]), u2f(o[c + 3]));
             }
           }
-          uint4 w[8];
+        } else {
+          // bf16 outputs: bands of 64 columns, read 32 at a time
+          const int n_bands = (a.d_out + 63) / 64;  // a partial last band is clipped by the map
+#pragma unroll 1
+          for (int band = 0; band < n_bands; ++band) {
+            uint4 w[8];
 #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            w[c / 8].x = pack_bf16x2(u2f(o[c]), u2f(o[c + 1]));
-            w[c / 8].y = pack_bf16x2(u2f(o[c + 2]), u2f(o[c + 3]));
-            w[c / 8].z = pack_bf16x2(u2f(o[c + 4]), u2f(o[c + 5]));
-            w[c / 8].w = pack_bf16x2(u2f(o[c + 6]), u2f(o[c + 7]));
-          }
-          if (use_tma) {
-            if (leader) bulk_wait_read0();  // the previous band's store has read the buffer
-            named_bar_sync(1 + t, kBlockM);
+            for (int hb = 0; hb < 64; hb += 32) {
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(to + band * 64 + hb, o);
+              if (split) {
+                uint32_t o1[32];
+                tmem_ld_32x32b_x32(to1 + band * 64 + hb, o1);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              *reinterpret_cast<uint4*>(stage + ((ch ^ (row_in_tile & 7)) * 16)) = w[ch];
-            fence_proxy_async_smem();
-            named_bar_sync(1 + t, kBlockM);
-            if (leader) {
-              tma_store_4d(&tm_o, stage_base, band * 64, u.q_base + row_first, u.h, u.qb);
-              bulk_commit();
+                for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * c0 + u2f(o1[e]) * c1);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * c0);
+              }
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4& x = w[(hb + c) / 8];
+                x.x = pack_bf16x2(u2f(o[c]), u2f(o[c + 1]));
+                x.y = pack_bf16x2(u2f(o[c + 2]), u2f(o[c + 3]));
+                x.z = pack_bf16x2(u2f(o[c + 4]), u2f(o[c + 5]));
+                x.w = pack_bf16x2(u2f(o[c + 6]), u2f(o[c + 7]));
+              }
             }
-          } else if (valid) {
-            __nv_bfloat16* op =
-                static_cast<__nv_bfloat16*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + band * 64;
+            if (band == n_bands - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                mbar_arrive(o_free(t));  // O_t may now take the next unit's PV
+                if (split) mbar_arrive(o_free(1));
+              }
+            }
+            if (use_tma) {
+              if (leader) bulk_wait_read0();  // the previous band's store has read the buffer
+              named_bar_sync(1, kBlockM);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              if (band * 64 + ch * 8 < a.d_out) *reinterpret_cast<uint4*>(op + ch * 8) = w[ch];
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(stage + ((ch ^ (row_in_tile & 7)) * 16)) = w[ch];
+              fence_proxy_async_smem();
+              named_bar_sync(1, kBlockM);
+              if (leader) {
+                tma_store_4d(&tm_o, stage_base, band * 64, u.q_base + row_first, u.h, u.qb);
+                bulk_commit();
+              }
+            } else if (valid) {
+              __nv_bfloat16* op =
+                  static_cast<__nv_bfloat16*>(a.out) + u.qb * a.so_b + row * a.so_m + u.h * a.so_h + band * 64;
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                if (band * 64 + ch * 8 < a.d_out) *reinterpret_cast<uint4*>(op + ch * 8) = w[ch];
+            }
           }
         }
-      }
-      if (valid) {
-        if (a.lse != nullptr)
+        if (valid && a.lse != nullptr)
           a.lse[u.qb * a.lse_sb + u.h * a.lse_sh + row * a.lse_sm] =
               (l_out > 0.f) ? (m_out + lg2_approx(l_out)) * kLn2 : -INFINITY;
       }
-      ph ^= 1u;
     }
   }
 
   // ---------------------------------------------------------------- teardown
-  if (warp < 8 && (warp % 4) == 0 && lane == 0) bulk_wait0();  // output stores complete
+  if (warp == kWarpOut && lane == 0) bulk_wait0();  // output stores complete
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {

@@ -53,9 +53,16 @@ struct AttnProblem {
   bool independent;  // MSLK_FLAG_INDEPENDENT: may overlap the preceding launch
 };
 
+// Most chunks one varargs merge takes (its pointer table travels as a kernel parameter).
+constexpr int kMergeMaxVarargs = MSLK_MERGE_MAX_VARARGS;
+
 struct MergeProblem {
   const float* out_split;
   const float* lse_split;
+  // Varargs merge: chunk c's output and lse at chunk_out[c] / chunk_lse[c] (host arrays of
+  // n_chunks device pointers); null for the stacked layout above.
+  const float* const* chunk_out;
+  const float* const* chunk_lse;
   int n_chunks;
   int64_t cs_out, cs_lse;
   int B, M, H, Kv;

@@ -38,6 +38,28 @@ struct MergeArgs {
   long long rows;
 };
 
+// Chunk c of a varargs merge: separately allocated [B, M, H, Kv] output and [B, H, M] lse
+// arrays (kernel parameters, so no device-side table has to be written first).
+struct ChunkTable {
+  const float* out[kMergeMaxVarargs];
+  const float* lse[kMergeMaxVarargs];
+};
+
+// Where chunk c's row and lse live: stacked (base + c * chunk stride) or a pointer table.
+struct StackedChunks {
+  MSLK_DEV const float* out(const MergeArgs& a, int c, long long off) const {
+    return a.out_split + c * a.cs_out + off;
+  }
+  MSLK_DEV const float* lse(const MergeArgs& a, int c, long long idx) const {
+    return a.lse_split + c * a.cs_lse + idx;
+  }
+};
+struct TableChunks {
+  const ChunkTable* t;
+  MSLK_DEV const float* out(const MergeArgs&, int c, long long off) const { return t->out[c] + off; }
+  MSLK_DEV const float* lse(const MergeArgs&, int c, long long idx) const { return t->lse[c] + idx; }
+};
+
 MSLK_DEV float4 ldg_f4(const float* p) {
   float4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -48,8 +70,8 @@ MSLK_DEV float4 ldg_f4(const float* p) {
 
 // G = chunks folded per memory round trip (2, 4 or 8): fewer for small n keeps the
 // registers low and the number of rows in flight per SM high.
-template <int G>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeArgs a) {
+template <int G, class Chunks>
+MSLK_DEV void merge_rows(const MergeArgs& a, const Chunks& ch) {
   const int lane = threadIdx.x % 32;
   const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + threadIdx.x / 32;
   if (row >= a.rows) return;
@@ -58,8 +80,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeA
   const int m = static_cast<int>(bm_ % a.M);
   const int b = static_cast<int>(bm_ / a.M);
   const long long lse_idx = (static_cast<long long>(b) * a.H + h) * a.M + m;  // [B, H, M]
-  const float* src = a.out_split + b * a.ss_b + m * a.ss_m + h * a.ss_h;
-  const float* lsrc = a.lse_split + lse_idx;
+  const long long src = b * a.ss_b + m * a.ss_m + h * a.ss_h;  // row offset inside a chunk
 
   for (int d0 = lane * 4; d0 < a.Kv; d0 += 128) {
     // Chunks are folded G at a time with a running maximum (all in base 2):
@@ -70,13 +91,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeA
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c0 = 0; c0 < a.n; c0 += G) {
       float4 x[G];
-      const float* p = src + c0 * a.cs_out + d0;
 #pragma unroll
-      for (int u = 0; u < G; ++u) {
-        x[u] = (c0 + u < a.n) ? ldg_f4(p) : make_float4(0.f, 0.f, 0.f, 0.f);
-        p += a.cs_out;
-      }
-      const float mine = (lane < G && c0 + lane < a.n) ? __ldg(lsrc + (c0 + lane) * a.cs_lse) * kLog2e
+      for (int u = 0; u < G; ++u)
+        x[u] = (c0 + u < a.n) ? ldg_f4(ch.out(a, c0 + u, src + d0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float mine = (lane < G && c0 + lane < a.n) ? __ldg(ch.lse(a, c0 + lane, lse_idx)) * kLog2e
                                                        : -INFINITY;
       float l2[G];
 #pragma unroll
@@ -120,6 +138,17 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeA
   }
 }
 
+template <int G>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeArgs a) {
+  merge_rows<G>(a, StackedChunks{});
+}
+
+template <int G>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    merge_table_kernel(const MergeArgs a, const __grid_constant__ ChunkTable t) {
+  merge_rows<G>(a, TableChunks{&t});
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const MergeProblem& p, const DeviceCtl& ctl, cudaStream_t stream) {
@@ -146,12 +175,27 @@ cudaError_t launch_merge(const MergeProblem& p, const DeviceCtl& ctl, cudaStream
   a.rows = static_cast<long long>(p.B) * p.H * p.M;
   if (a.rows == 0) return cudaSuccess;
   const long long blocks = (a.rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const dim3 grid(static_cast<unsigned>(blocks)), block(kWarpsPerBlock * 32);
+  if (p.chunk_out != nullptr) {  // separately allocated chunks: pointer table as a parameter
+    ChunkTable t{};
+    for (int c = 0; c < p.n_chunks; ++c) {
+      t.out[c] = p.chunk_out[c];
+      t.lse[c] = p.chunk_lse[c];
+    }
+    if (a.n <= 2)
+      merge_table_kernel<2><<<grid, block, 0, stream>>>(a, t);
+    else if (a.n <= 4)
+      merge_table_kernel<4><<<grid, block, 0, stream>>>(a, t);
+    else
+      merge_table_kernel<8><<<grid, block, 0, stream>>>(a, t);
+    return cudaGetLastError();
+  }
   if (a.n <= 2)
-    merge_kernel<2><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+    merge_kernel<2><<<grid, block, 0, stream>>>(a);
   else if (a.n <= 4)
-    merge_kernel<4><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+    merge_kernel<4><<<grid, block, 0, stream>>>(a);
   else
-    merge_kernel<8><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+    merge_kernel<8><<<grid, block, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,7 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cmath>
@@ -433,6 +434,151 @@ mslk_status attn_general(const mslk_attn_args& a, cudaStream_t stream, const cha
   return run_attn(p, stream, who);
 }
 
+// The checks every merge entry shares (sizes, dtype, strides, out and lse); fills the
+// problem's common fields.  B, M or H == 0 returns MSLK_OK with nothing to do.
+mslk_status validate_merge(MergeProblem& p, int32_t n_chunks, int32_t B, int32_t M, int32_t H,
+                           int32_t Kv, const mslk_strides* s_split, const mslk_strides* so,
+                           void* out, int32_t out_dtype, float* lse, const char* who) {
+  if (n_chunks < 1) return fail(MSLK_ERR_INVALID_ARG, "%s: n_chunks must be >= 1 (got %d)", who, n_chunks);
+  if (B < 0 || M < 0 || H < 0 || Kv < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative size", who);
+  if (out_dtype != MSLK_DTYPE_BF16 && out_dtype != MSLK_DTYPE_FP32)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: unknown out_dtype %d", who, out_dtype);
+  if (s_split == nullptr || so == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: null strides", who);
+  if (B == 0 || M == 0 || H == 0) return ok();
+  if (Kv == 0 || Kv % 4) return fail(MSLK_ERR_UNSUPPORTED, "%s: Kv (%d) must be a positive multiple of 4", who, Kv);
+  if (out == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: null pointer", who);
+  if (!aligned16(out)) return fail(MSLK_ERR_MISALIGNED, "%s: out_split/out must be 16-byte aligned", who);
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(MSLK_ERR_MISALIGNED, "%s: lse_split/lse must be 4-byte aligned", who);
+  if (const char* w = check_strides(*s_split, B, M, H, 4, false))
+    return fail(MSLK_ERR_MISALIGNED, "%s: out_split %s must be a positive multiple of 4 elements", who, w);
+  const bool out_fp32 = out_dtype == MSLK_DTYPE_FP32;
+  if (const char* w = check_strides(*so, B, M, H, out_fp32 ? 4 : 8, false))
+    return fail(MSLK_ERR_MISALIGNED, "%s: out %s must be a positive multiple of 16 bytes", who, w);
+  p.n_chunks = n_chunks;
+  p.B = B;
+  p.M = M;
+  p.H = H;
+  p.Kv = Kv;
+  p.ss = *s_split;
+  p.so = *so;
+  p.out = out;
+  p.out_fp32 = out_fp32;
+  p.lse = lse;
+  return ok();
+}
+
+mslk_status run_merge(const MergeProblem& p, cudaStream_t stream, const char* who) {
+  const DeviceCtl ctl = device_ctl();
+  if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "%s: no CUDA device / module", who);
+  const cudaError_t e = launch_merge(p, ctl, stream);
+  if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+  return ok();
+}
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// Keys per split (a multiple of tile_n) so that every (batch, K/V head) unit gets enough
+// splits for one (unit, split) pair per SM; 0 when one split covers the keys.
+int32_t splitk_size(int32_t batch, int32_t seqlen_kv, int32_t kv_heads, int32_t tile_n,
+                    int32_t sm_count) {
+  if (batch <= 0 || seqlen_kv <= 0 || kv_heads <= 0) return 0;
+  if (tile_n <= 0) tile_n = 256;
+  if (sm_count <= 0) sm_count = current_sm_count();
+  const long long units = static_cast<long long>(batch) * kv_heads;
+  const long long splits = std::max(1LL, (sm_count + units - 1) / units);
+  long long size = (seqlen_kv + splits - 1) / splits;
+  size = (size + tile_n - 1) / tile_n * tile_n;
+  return size >= seqlen_kv ? 0 : static_cast<int32_t>(size);
+}
+
+// Chunk count of a split-KV call: the caller's, or from splitk_size; at most one per key.
+int32_t split_chunks(const mslk_attn_args& a, int32_t n_chunks) {
+  if (n_chunks <= 0) {
+    const int32_t hkv = a.Hkv > 0 ? a.Hkv : ((a.H > 1 && a.sk.h == 0) ? 1 : a.H);
+    const int32_t size = splitk_size(a.B, a.Mkv, hkv, 256, 0);
+    n_chunks = size == 0 ? 1 : (a.Mkv + size - 1) / size;
+  }
+  return std::max(1, std::min(n_chunks, std::max(1, a.Mkv)));
+}
+
+// Workspace of a split-KV call: the chunks' fp32 outputs [n, B, M, H, Kv] (contiguous),
+// then their lse [n, B, H, M]; the lse block starts on a 256-byte boundary.
+struct SplitLayout {
+  size_t out_chunk_elems, lse_chunk_elems, lse_offset, bytes;
+};
+SplitLayout split_layout(const mslk_attn_args& a, int32_t n) {
+  SplitLayout l{};
+  l.out_chunk_elems = static_cast<size_t>(a.B) * a.M * a.H * a.Kv;
+  l.lse_chunk_elems = static_cast<size_t>(a.B) * a.H * a.M;
+  l.lse_offset = (static_cast<size_t>(n) * l.out_chunk_elems * sizeof(float) + 255) / 256 * 256;
+  l.bytes = l.lse_offset + static_cast<size_t>(n) * l.lse_chunk_elems * sizeof(float);
+  return l;
+}
+
+// The arguments a split-KV call accepts, checked before anything is launched: those of the
+// forward call (validated by planning it), dense masks only, no key lanes.
+mslk_status check_split_args(const mslk_attn_args* a, int32_t n_chunks, const char* who) {
+  if (a == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: args is null", who);
+  if (a->partial != 0) return fail(MSLK_ERR_INVALID_ARG, "%s: args must describe a forward (partial = 0)", who);
+  if (a->lanes != nullptr) return fail(MSLK_ERR_UNSUPPORTED, "%s: key lanes are not split", who);
+  if (is_blockdiag(a->mask_kind))
+    return fail(MSLK_ERR_UNSUPPORTED, "%s: block-diagonal masks are not split (dense masks only)", who);
+  if (a->fp8 != nullptr) return fail(MSLK_ERR_UNSUPPORTED, "%s: E4M3 inputs are not split (bf16 only)", who);
+  if (n_chunks < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: n_chunks must be >= 0 (got %d)", who, n_chunks);
+  int32_t plan = 0;
+  return attn_general(*a, nullptr, who, &plan);
+}
+
+// Partials over n equal contiguous key chunks into the workspace, then the merge into
+// args.out / args.lse.  Chunk c > 0 is launched independent of chunk c - 1 (they read the
+// same q, k, v and write separate workspace slices); the merge waits for all of them.
+mslk_status run_split_kv(const mslk_attn_args& a, int32_t n, float* ws_out, float* ws_lse,
+                         cudaStream_t stream, const char* who) {
+  const SplitLayout l = split_layout(a, n);
+  const int esz = 2;  // bf16 keys and values
+  const bool br = is_bottom_right(a.mask_kind) || (a.band != nullptr && a.band->bottom_right);
+  // A bottom-right alignment is a shift of the key positions: folded into kv_offset.
+  const int64_t shift = br ? static_cast<int64_t>(a.Mkv) - a.M : 0;
+  mslk_band band{0, -1, -1};
+  if (a.band != nullptr) band = *a.band;
+  band.bottom_right = 0;
+  const mslk_strides s_ws{static_cast<int64_t>(a.M) * a.H * a.Kv, static_cast<int64_t>(a.H) * a.Kv, a.Kv};
+  for (int32_t c = 0; c < n; ++c) {
+    const int32_t k0 = static_cast<int32_t>(static_cast<int64_t>(c) * a.Mkv / n);
+    const int32_t k1 = static_cast<int32_t>(static_cast<int64_t>(c + 1) * a.Mkv / n);
+    mslk_attn_args ca = a;
+    ca.k = static_cast<const uint8_t*>(a.k) + static_cast<int64_t>(k0) * a.sk.m * esz;
+    ca.v = static_cast<const uint8_t*>(a.v) + static_cast<int64_t>(k0) * a.sv.m * esz;
+    ca.Mkv = k1 - k0;
+    ca.mask_kind = a.mask_kind == MSLK_MASK_CAUSAL_BOTTOM_RIGHT ? MSLK_MASK_CAUSAL : a.mask_kind;
+    ca.band = &band;
+    ca.partial = 1;
+    ca.kv_offset = k0 - shift;
+    ca.out = ws_out + c * l.out_chunk_elems;
+    ca.so = s_ws;
+    ca.out_dtype = MSLK_DTYPE_FP32;
+    ca.lse = ws_lse + c * l.lse_chunk_elems;
+    ca.flags = c > 0 ? MSLK_FLAG_INDEPENDENT : (a.flags & MSLK_FLAG_INDEPENDENT);
+    const mslk_status s = attn_general(ca, stream, who);
+    if (s != MSLK_OK) return s;
+  }
+  MergeProblem m{};
+  mslk_status s = validate_merge(m, n, a.B, a.M, a.H, a.Kv, &s_ws, &a.so, a.out, a.out_dtype, a.lse, who);
+  if (s != MSLK_OK) return s;
+  m.out_split = ws_out;
+  m.lse_split = ws_lse;
+  m.cs_out = static_cast<int64_t>(l.out_chunk_elems);
+  m.cs_lse = static_cast<int64_t>(l.lse_chunk_elems);
+  return run_merge(m, stream, who);
+}
+
 }  // namespace
 
 extern "C" {
@@ -544,48 +690,94 @@ mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split
                                   const mslk_strides* so, void* out, int32_t out_dtype, float* lse,
                                   void* stream) {
   const char* who = "mslk_merge_attentions";
-  if (n_chunks < 1) return fail(MSLK_ERR_INVALID_ARG, "%s: n_chunks must be >= 1 (got %d)", who, n_chunks);
-  if (B < 0 || M < 0 || H < 0 || Kv < 0) return fail(MSLK_ERR_INVALID_ARG, "%s: negative size", who);
-  if (out_dtype != MSLK_DTYPE_BF16 && out_dtype != MSLK_DTYPE_FP32)
-    return fail(MSLK_ERR_INVALID_ARG, "%s: unknown out_dtype %d", who, out_dtype);
-  if (s_split == nullptr || so == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: null strides", who);
-  if (B == 0 || M == 0 || H == 0) return ok();
-  if (Kv == 0 || Kv % 4) return fail(MSLK_ERR_UNSUPPORTED, "%s: Kv (%d) must be a positive multiple of 4", who, Kv);
-  if (out_split == nullptr || lse_split == nullptr || out == nullptr)
+  MergeProblem p{};
+  mslk_status s = validate_merge(p, n_chunks, B, M, H, Kv, s_split, so, out, out_dtype, lse, who);
+  if (s != MSLK_OK || B == 0 || M == 0 || H == 0) return s;
+  if (out_split == nullptr || lse_split == nullptr)
     return fail(MSLK_ERR_INVALID_ARG, "%s: null pointer", who);
-  if (!aligned16(out_split) || !aligned16(out))
+  if (!aligned16(out_split))
     return fail(MSLK_ERR_MISALIGNED, "%s: out_split/out must be 16-byte aligned", who);
-  if ((reinterpret_cast<uintptr_t>(lse_split) & 3u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+  if ((reinterpret_cast<uintptr_t>(lse_split) & 3u) != 0)
     return fail(MSLK_ERR_MISALIGNED, "%s: lse_split/lse must be 4-byte aligned", who);
   if (n_chunks > 1 && (chunk_stride_out <= 0 || chunk_stride_out % 4))
     return fail(MSLK_ERR_MISALIGNED, "%s: chunk_stride_out must be a positive multiple of 4", who);
   if (n_chunks > 1 && chunk_stride_lse <= 0)
     return fail(MSLK_ERR_INVALID_ARG, "%s: chunk_stride_lse must be positive", who);
-  if (const char* w = check_strides(*s_split, B, M, H, 4, false))
-    return fail(MSLK_ERR_MISALIGNED, "%s: out_split %s must be a positive multiple of 4 elements", who, w);
-  const bool out_fp32 = out_dtype == MSLK_DTYPE_FP32;
-  if (const char* w = check_strides(*so, B, M, H, out_fp32 ? 4 : 8, false))
-    return fail(MSLK_ERR_MISALIGNED, "%s: out %s must be a positive multiple of 16 bytes", who, w);
-  MergeProblem p{};
   p.out_split = out_split;
   p.lse_split = lse_split;
-  p.n_chunks = n_chunks;
   p.cs_out = chunk_stride_out;
   p.cs_lse = chunk_stride_lse;
-  p.B = B;
-  p.M = M;
-  p.H = H;
-  p.Kv = Kv;
-  p.ss = *s_split;
-  p.so = *so;
-  p.out = out;
-  p.out_fp32 = out_fp32;
-  p.lse = lse;
-  const DeviceCtl ctl = device_ctl();
-  if (ctl.err == nullptr) return fail(MSLK_ERR_CUDA, "%s: no CUDA device / module", who);
-  const cudaError_t e = launch_merge(p, ctl, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail(MSLK_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+  return run_merge(p, static_cast<cudaStream_t>(stream), who);
+}
+
+mslk_status mslk_merge_attentions_varargs(const float* const* out_chunks,
+                                          const float* const* lse_chunks, int32_t n_chunks,
+                                          int32_t B, int32_t M, int32_t H, int32_t Kv,
+                                          const mslk_strides* s_split, const mslk_strides* so,
+                                          void* out, int32_t out_dtype, float* lse, void* stream) {
+  const char* who = "mslk_merge_attentions_varargs";
+  if (n_chunks > kMergeMaxVarargs)
+    return fail(MSLK_ERR_UNSUPPORTED, "%s: at most %d chunks (got %d)", who, kMergeMaxVarargs, n_chunks);
+  MergeProblem p{};
+  mslk_status s = validate_merge(p, n_chunks, B, M, H, Kv, s_split, so, out, out_dtype, lse, who);
+  if (s != MSLK_OK || B == 0 || M == 0 || H == 0) return s;
+  if (out_chunks == nullptr || lse_chunks == nullptr)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: null chunk array", who);
+  for (int c = 0; c < n_chunks; ++c) {
+    if (out_chunks[c] == nullptr || lse_chunks[c] == nullptr)
+      return fail(MSLK_ERR_INVALID_ARG, "%s: chunk %d is null", who, c);
+    if (!aligned16(out_chunks[c]))
+      return fail(MSLK_ERR_MISALIGNED, "%s: chunk %d output must be 16-byte aligned", who, c);
+    if ((reinterpret_cast<uintptr_t>(lse_chunks[c]) & 3u) != 0)
+      return fail(MSLK_ERR_MISALIGNED, "%s: chunk %d lse must be 4-byte aligned", who, c);
+  }
+  p.chunk_out = out_chunks;
+  p.chunk_lse = lse_chunks;
+  return run_merge(p, static_cast<cudaStream_t>(stream), who);
+}
+
+int32_t mslk_splitk_size(int32_t batch, int32_t seqlen_kv, int32_t kv_heads, int32_t tile_n,
+                         int32_t sm_count) {
+  return splitk_size(batch, seqlen_kv, kv_heads, tile_n, sm_count);
+}
+
+mslk_status mslk_attn_split_kv_workspace(const mslk_attn_args* args, int32_t n_chunks,
+                                         size_t* bytes) {
+  const char* who = "mslk_attn_split_kv_workspace";
+  if (bytes == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: bytes is null", who);
+  if (args == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: args is null", who);
+  // Sizes only: the tensor pointers are not read (a stand-in passes the pointer checks,
+  // nothing is launched).
+  mslk_attn_args a = *args;
+  const void* stand_in = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  if (a.q == nullptr) a.q = stand_in;
+  if (a.k == nullptr) a.k = stand_in;
+  if (a.v == nullptr) a.v = stand_in;
+  if (a.out == nullptr) a.out = const_cast<void*>(stand_in);
+  const mslk_status s = check_split_args(&a, n_chunks, who);
+  if (s != MSLK_OK) return s;
+  *bytes = split_layout(a, split_chunks(a, n_chunks)).bytes;
   return ok();
+}
+
+mslk_status mslk_attn_split_kv(const mslk_attn_args* args, int32_t n_chunks, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  const char* who = "mslk_attn_split_kv";
+  mslk_status s = check_split_args(args, n_chunks, who);
+  if (s != MSLK_OK) return s;
+  const mslk_attn_args& a = *args;
+  if (a.B == 0 || a.M == 0 || a.H == 0 || a.Mkv == 0)  // nothing to split: the forward call
+    return attn_general(a, static_cast<cudaStream_t>(stream), who);
+  const int32_t n = split_chunks(a, n_chunks);
+  const SplitLayout l = split_layout(a, n);
+  if (workspace == nullptr) return fail(MSLK_ERR_INVALID_ARG, "%s: workspace is null", who);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(MSLK_ERR_MISALIGNED, "%s: workspace must be 256-byte aligned", who);
+  if (workspace_bytes < l.bytes)
+    return fail(MSLK_ERR_INVALID_ARG, "%s: workspace of %zu bytes is below the %zu needed", who,
+                workspace_bytes, l.bytes);
+  float* ws = static_cast<float*>(workspace);
+  return run_split_kv(a, n, ws, ws + l.lse_offset / sizeof(float), static_cast<cudaStream_t>(stream), who);
 }
 
 const char* mslk_last_error(void) { return g_last_error; }

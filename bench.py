@@ -523,6 +523,14 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
             torch.cuda.synchronize()
             entry[key] = _time_it(gr.replay, 50, stream, flush) * 1e6
             del gr
+        # the same split in one library call (partials + merge, workspace given): the
+        # host cost of n + 1 Python calls becomes one
+        ws = torch.empty(fa.split_kv_workspace_bytes(qs, ks, vs, n_chunks=n), dtype=torch.uint8, device=dev)
+        one_call = lambda n=n, ws=ws, mo=mo, ml=ml: fa.attn_split_kv(  # noqa: E731
+            qs, ks, vs, n_chunks=n, scale=w.scale, out=mo, lse=ml, workspace=ws)
+        for _ in range(10):
+            one_call()
+        entry["one_call_us"] = _time_it(one_call, 50, stream, flush) * 1e6
         res[f"split_kv_{n}_chunks_1x128x1024x16x128"] = entry
     # merge: 8 chunks of [2, 2048, 32, 128] fp32 -> bf16 out + fp32 lse
     n, B, M, H, Kv = 8, 2, 2048, 32, 128
@@ -607,6 +615,16 @@ def measure_secondary(fa, inputs, dev, flush, peaks):
                                       "eager_partial_GB/s": kv_bytes / t_eager / 1e9,
                                       "launches": 17}
     del graph
+    # the 16-chunk split in one library call (partials + merge into bf16 out, workspace given)
+    ws = torch.empty(fa.split_kv_workspace_bytes(qd, kd, vd, n_chunks=16), dtype=torch.uint8, device=dev)
+    one_call = lambda: fa.attn_split_kv(qd, kd, vd, n_chunks=16, scale=w.scale, out=fo, lse=fl,  # noqa: E731
+                                        workspace=ws)
+    for _ in range(3):
+        one_call()
+    t_oc = _time_it(one_call, 10, stream, flush)
+    res["decode_split_kv_16x2048"].update({"one_call_us": t_oc * 1e6,
+                                           "one_call_GB/s": kv_bytes / t_oc / 1e9,
+                                           "one_call_frac_hbm": kv_bytes / t_oc / 1e9 / peaks["hbm_gbs"]})
     # the same step as one call over all 32768 keys (the kernel splits keys on-chip)
     fo32 = torch.empty((w.B, w.M, w.H, w.Kv), dtype=torch.float32, device=dev)
     one = lambda: fa.attn_partial(qd, kd, vd, scale=w.scale, out=fo32, lse=fl)  # noqa: E731

@@ -48,6 +48,7 @@
 #ifndef MSLK_ATTN_H
 #define MSLK_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -350,6 +351,71 @@ mslk_status mslk_merge_attentions(const float* out_split, const float* lse_split
                                   int32_t Kv, const mslk_strides* s_split,
                                   const mslk_strides* so, void* out, int32_t out_dtype,
                                   float* lse, void* stream);
+
+/*
+ * mslk_merge_attentions_varargs — the same merge over chunks that are separate
+ * allocations (MSLK kernel reference, "Attention - Merge & storage utilities" >
+ * torch.ops.mslk.fmha_merge_attentions_varargs, which takes lists of chunk tensors).
+ *
+ *   out_chunks  HOST array of n_chunks DEVICE pointers, chunk c's fp32 [B,M,H,Kv] output,
+ *               every chunk with the strides s_split; read during the call only.
+ *   lse_chunks  HOST array of n_chunks DEVICE pointers, chunk c's fp32 [B,H,M] lse
+ *               (contiguous).
+ *   n_chunks    1 .. MSLK_MERGE_MAX_VARARGS.
+ * Other arguments, the result and the alignment rules as mslk_merge_attentions; every
+ * chunk pointer follows the rule of out_split / lse_split.  Nothing is copied or stacked:
+ * the kernel reads each chunk where it lies.
+ */
+#define MSLK_MERGE_MAX_VARARGS 128
+mslk_status mslk_merge_attentions_varargs(const float* const* out_chunks,
+                                          const float* const* lse_chunks, int32_t n_chunks,
+                                          int32_t B, int32_t M, int32_t H, int32_t Kv,
+                                          const mslk_strides* s_split, const mslk_strides* so,
+                                          void* out, int32_t out_dtype, float* lse,
+                                          void* stream);
+
+/*
+ * mslk_splitk_size — keys per split for split-KV attention (MSLK kernel reference,
+ * "Attention - Standalone Blackwell FMHA" > get_splitk_heuristic: a split size from the
+ * batch, the key count, the K/V heads and the SM count; 0 when one split covers the keys).
+ * This library's rule: enough splits that every (batch, K/V head) unit has one split per
+ * SM share, splits = ceil(sm_count / (batch * kv_heads)); size = ceil(seqlen_kv / splits)
+ * rounded up to a multiple of tile_n; 0 when that size reaches seqlen_kv.  tile_n <= 0
+ * means 256; sm_count <= 0 reads the current device's SM count (148 without a device).
+ * Host-only and thread-safe; non-positive sizes give 0.
+ */
+int32_t mslk_splitk_size(int32_t batch, int32_t seqlen_kv, int32_t kv_heads, int32_t tile_n,
+                         int32_t sm_count);
+
+/*
+ * mslk_attn_split_kv — exact split-KV attention in one call: the keys of a forward
+ * problem are cut into n_chunks equal contiguous chunks (chunk c holds keys
+ * [c * Mkv / n, (c + 1) * Mkv / n)), mslk_attn's partial form runs on each (fp32 results
+ * in `workspace`), and the merge writes args->out and args->lse.  The same result as the
+ * forward call within the merge's rounding ("Attention - Core fMHA" >
+ * memory_efficient_attention_partial then merge_attentions, which is exact).
+ *   args       a FORWARD problem as for mslk_attn (partial = 0): bf16 inputs, dense masks
+ *              (none, causal, bottom-right causal), windows, grouped K/V heads; key lanes,
+ *              block-diagonal masks and E4M3 inputs return MSLK_ERR_UNSUPPORTED.  A bottom-right
+ *              alignment is folded into each chunk's kv_offset.  args->out_dtype and
+ *              args->lse (NULL: not written) apply to the merged result.
+ *   n_chunks   >= 1, or 0 to take ceil(Mkv / mslk_splitk_size(B, Mkv, Hkv, 256, SMs))
+ *              (one chunk when that is 0); more chunks than keys are cut to one per key.
+ *   workspace  caller-owned DEVICE memory, 256-byte aligned, of at least the size that
+ *              mslk_attn_split_kv_workspace returns: the chunks' outputs [n, B, M, H, Kv]
+ *              then their lse [n, B, H, M], fp32.  It is overwritten; it may be reused
+ *              once the call's work on `stream` is done.
+ * Launch order on `stream`: chunk 0, chunks 1.. n-1 declared independent of the one before
+ * (they read the same inputs and write separate workspace slices), then the merge in plain
+ * stream order.  args->flags applies to chunk 0 only.  Every argument error is returned
+ * before the first launch.
+ */
+mslk_status mslk_attn_split_kv(const mslk_attn_args* args, int32_t n_chunks, void* workspace,
+                               size_t workspace_bytes, void* stream);
+/* Bytes of workspace mslk_attn_split_kv needs for these arguments and chunk count; the
+ * tensor pointers in args are not read and may be NULL (the other checks still apply). */
+mslk_status mslk_attn_split_kv_workspace(const mslk_attn_args* args, int32_t n_chunks,
+                                         size_t* bytes);
 
 /*
  * Reason for the last non-OK status returned on the calling thread (like the pages'
