@@ -9,20 +9,25 @@
 //
 // Persistent: one CTA per SM walks a static list of units (heavy-first, snake-assigned);
 // barrier phases carry across units, so the next unit's Q/K/V loads and first MMAs
-// overlap the current unit's last tiles and epilogue.
-// Per CTA (320 threads):
+// overlap the current unit's last tiles and its output.
+// Per CTA (512 threads, four warpgroups):
 //   warps 0-3   softmax for Q tile 0 (thread t owns row t = TMEM lane t)
 //   warps 4-7   softmax for Q tile 1
-//   warp  8     tcgen05.mma issue (one elected thread) + TMEM allocation
-//   warp  9     TMA producer (one elected thread)
+//   warps 8-11  output: normalise O_t, store it (TMA), write lse; the softmax warpgroups
+//               hand over their row max and sum and go straight on to the next unit
+//   warp  12    tcgen05.mma issue (one elected thread) + TMEM allocation
+//   warp  13    TMA producer (one elected thread); warps 14-15 idle
+// Register budgets per warpgroup (setmaxnreg): softmax 176, output 96, MMA/TMA 64.
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D),
 // fp32 accumulators, row r of a tile in lane r.  The bf16 probabilities P_t overwrite the
-// first 64 columns of S_t (two values per column) and feed the PV MMA from tensor memory.
-// Shared memory: Q0, Q1 and a ring of K/V tiles (4 stages at D=128), in the 128-byte-swizzled
-// K-major layout TMA writes (V is read MN-major by the PV MMA).  Each Q tile has its own
-// full/empty barriers: the next unit's Q0 loads as soon as this unit's last S0 MMA has
-// run (a tile earlier than Q1 under a causal mask), and the next unit's first S0 is
-// issued right behind this unit's last PV.
+// first 64 columns of S_t (two values per column) and feed the PV MMA from tensor memory;
+// they are published in two halves of 64 keys so the first half's PV runs while the
+// second half is computed.
+// Shared memory: Q0, Q1, a ring of K/V tiles (4 stages at D=128) and one output staging
+// tile, in the 128-byte-swizzled K-major layout TMA writes (V is read MN-major by the PV
+// MMA).  Each Q tile has its own full/empty barriers: the next unit's Q0 loads as soon as
+// this unit's last S0 MMA has run, and the next unit's first S0 is issued as soon as Q
+// tile 0 of this unit is done (one key tile before Q tile 1 under a causal mask).
 // The MMA and TMA roles run as whole converged warps that issue through one elected lane:
 // their operands stay warp-uniform, so they need few issue slots while the softmax
 // warpgroups keep the SM's schedulers busy.
@@ -55,8 +60,8 @@
 //    the r query heads of one K/V head (q/out tensor maps are views), all at position 0;
 //  * split units (the kSplit instantiation, launches with at most 128 rows per unit, e.g.
 //    folded heads with r <= 128): both Q tiles hold the unit's rows and take alternate
-//    key tiles, each with its own running max, sum and O, and Q tile 0 merges the two by
-//    log-sum-exp at the epilogue (tile 1's max and sum through shared memory), so both
+//    key tiles, each with its own running max, sum and O, and the output warpgroup merges
+//    the two by log-sum-exp (both tiles' max and sum through shared memory), so both
 //    softmax warpgroups work on a decode unit;
 //  * E4M3 inputs (fmha_tc_fp8_kernel, head dim 128): kind::f8f6f4 MMAs, one 128-byte
 //    swizzle atom per row, E4M3 probabilities four per TMEM column, descales folded into
@@ -97,9 +102,6 @@ constexpr int kSwizzleAtom = 16384;  // one 64-column K-block of a 128-row tile 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest un-rescaled p (256)
-// P published in two halves of 64 keys (the first half's P.V MMAs start while the second
-// half's exponentials run), or all at once.
-constexpr bool kHalfP = true;
 
 // F8: q, k, v are E4M3 bytes; a 128-wide row is then one 128-byte swizzle atom.
 template <int D, bool F8>
@@ -632,7 +634,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
             if (j + 1 == (tn ? last1 : last0)) mma_commit_elect(q_empty(tn));
           }
           const int lo_j = tj ? lo1 : lo0;
-          if (!(ok = wait_bar_warp(kHalfP ? p_half(tj) : p_full(tj), (tj ? jg1 : jg0) & 1, wc))) break;
+          if (!(ok = wait_bar_warp(p_half(tj), (tj ? jg1 : jg0) & 1, wc))) break;
           if (j == lo_j && !(ok = wait_bar_warp(o_free(tj), ((tj ? uc1 : uc0) & 1) ^ 1, wc))) break;
           tc_fence_after();
           issue_pv_half<D, F8>(tm_o[tj], tm_s[tj], kv_vdesc(sv), j > lo_j ? 1u : 0u, 0);
@@ -648,7 +650,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         } else {
           // Q tile 0 (when key tile j is one of its tiles): PV0_j, then S0_{j+1}
           if (u.has(0, j)) {
-            if (!(ok = wait_bar_warp(kHalfP ? p_half(0) : p_full(0), jg0 & 1, wc))) break;
+            if (!(ok = wait_bar_warp(p_half(0), jg0 & 1, wc))) break;
             if (j == lo0 && !(ok = wait_bar_warp(o_free(0), (uc0 & 1) ^ 1, wc))) break;
             tc_fence_after();
             issue_pv_half<D, F8>(tm_o[0], tm_s[0], kv_vdesc(sv), j > lo0 ? 1u : 0u, 0);
@@ -676,7 +678,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           }
           // Q tile 1: PV1_j, then S1_{j+1}
           if (u.has(1, j)) {
-            if (!(ok = wait_bar_warp(kHalfP ? p_half(1) : p_full(1), jg1 & 1, wc))) break;
+            if (!(ok = wait_bar_warp(p_half(1), jg1 & 1, wc))) break;
             if (j == lo1 && !(ok = wait_bar_warp(o_free(1), (uc1 & 1) ^ 1, wc))) break;
             tc_fence_after();
             issue_pv_half<D, F8>(tm_o[1], tm_s[1], kv_vdesc(sv), j > lo1 ? 1u : 0u, 0);
@@ -778,46 +780,38 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           lim_c = max(-1, min(min(u.Lk - 1, pos + u.hi) - key0, kBlockN - 1));
           if constexpr (kLowerEdge) lim_lo = max(0, min(max(0, pos + u.lo) - key0, kBlockN));
         }
-        // The whole S row comes out of tensor memory in one load (128 registers).  On a
-        // tile that crosses a mask limit each 32-column quarter is classified: allowed
-        // whole (left alone), masked whole, or cut (masked column by column), so a causal
-        // diagonal tile masks one quarter per warp instead of all four.  Then the row max,
-        // the lazy rescale of O, and p = 2^(s*scale*log2e - m) with the row sum; P goes to
-        // S's first 64 columns as bf16 pairs, published in two halves of 64 keys so the
-        // MMA warp starts P.V on the first half while the second is computed.
+        // The whole S row comes out of tensor memory (two 64-column loads, one wait; 128
+        // registers): mask it (only tiles crossing a mask limit), take the row max, then
+        // form p = 2^(s*scale*log2e - m) and the row sum and write P as bf16 pairs over S's
+        // first 64 columns, a quarter (16 columns) at a time.  P is published in two halves
+        // of 64 keys: the MMA warp issues P.V over the first half while the second half's
+        // exponentials run.
         uint32_t sr[128];
         tmem_ld_32x32b_x64_nowait(ts, sr);
         tmem_ld_32x32b_x64_nowait(ts + 64, sr + 64);
         tmem_ld_wait();
         if (need_mask) {
+          // One allowed-column bit word per 32 columns, then a bit test per column:
+          // -inf is excluded from the max and 2^-inf = 0.
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t w = low_bits(lim_c + 1 - 32 * q4);
             if constexpr (kLowerEdge) w &= ~low_bits(lim_lo - 32 * q4);
-            if (w == 0u) {
 #pragma unroll
-              for (int c = 0; c < 32; ++c) sr[32 * q4 + c] = 0xFF800000u;  // -inf: 2^-inf = 0
-            } else if (w != 0xffffffffu) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c)
-                if (!((w >> c) & 1u)) sr[32 * q4 + c] = 0xFF800000u;
-            }
+            for (int c = 0; c < 32; ++c)
+              if (!((w >> c) & 1u)) sr[32 * q4 + c] = 0xFF800000u;
           }
         }
-        float qm[4];
+        float mx8[8];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float m4[4];
+        for (int e = 0; e < 8; ++e) mx8[e] = fmax3(u2f(sr[e]), u2f(sr[8 + e]), u2f(sr[16 + e]));
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 32 * q4 + e;
-            m4[e] = fmax3(fmax3(u2f(sr[c]), u2f(sr[c + 4]), u2f(sr[c + 8])),
-                          fmax3(u2f(sr[c + 12]), u2f(sr[c + 16]), u2f(sr[c + 20])),
-                          fmaxf(u2f(sr[c + 24]), u2f(sr[c + 28])));
-          }
-          qm[q4] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        }
-        const float mx = fmaxf(fmaxf(qm[0], qm[1]), fmaxf(qm[2], qm[3]));
+        for (int c = 24; c < 120; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], u2f(sr[c + e]), u2f(sr[c + 8 + e]));
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], u2f(sr[120 + e]));
+        const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7])));
         const float m_new = fmaxf(m_run, mx * sl2);
         const bool rescale = m_new > m_run + kRescaleThreshold;
         float alpha = 1.f;
@@ -826,6 +820,19 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           m_run = m_new;
         }
         l_run *= alpha;
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled, and
+          // PV_t(j) is not issued before P's first half is published.  (8 columns at a
+          // time: the S row still occupies 128 registers.)
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 8) {
+            uint32_t o[8];
+            tmem_ld_32x32b_x8(to + c0, o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = f2u(u2f(o[e]) * alpha);
+            tmem_st_32x32b_x8(to + c0, o);
+          }
+        }
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
         const uint64_t sl2x2 = pack_f2(sl2, sl2);
         const uint64_t nmx2 = pack_f2(-msub, -msub);
@@ -836,53 +843,36 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
             // P as E4M3, four per column, over S's first 32 columns.  p <= 2^8 (the lazy
             // rescale bound) stays inside E4M3's range (448).
             uint32_t pk[8];
-            {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int c = qtr * 32 + 4 * e;
-                const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
-                const float2 y = unpack_f2(ffma2(pack_f2(u2f(sr[c + 2]), u2f(sr[c + 3])), sl2x2, nmx2));
-                const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-                const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
-                rs2[(2 * e) % 4] = fadd2(rs2[(2 * e) % 4], pack_f2(p0, p1));
-                rs2[(2 * e + 1) % 4] = fadd2(rs2[(2 * e + 1) % 4], pack_f2(p2, p3));
-                pk[e] = pack_e4m3x4(p0, p1, p2, p3);
-              }
+            for (int e = 0; e < 8; ++e) {
+              const int c = qtr * 32 + 4 * e;
+              const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
+              const float2 y = unpack_f2(ffma2(pack_f2(u2f(sr[c + 2]), u2f(sr[c + 3])), sl2x2, nmx2));
+              const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+              const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
+              rs2[(2 * e) % 4] = fadd2(rs2[(2 * e) % 4], pack_f2(p0, p1));
+              rs2[(2 * e + 1) % 4] = fadd2(rs2[(2 * e + 1) % 4], pack_f2(p2, p3));
+              pk[e] = pack_e4m3x4(p0, p1, p2, p3);
             }
             tmem_st_32x32b_x8(ts + qtr * 8, pk);
           } else {
             uint32_t pk[16];
-            {
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int c = qtr * 32 + 2 * e;
-                const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
-                const float p0 = ex2_approx(x.x);
-                const float p1 = ex2_approx(x.y);
-                rs2[e % 4] = fadd2(rs2[e % 4], pack_f2(p0, p1));
-                pk[e] = pack_bf16x2(p0, p1);
-              }
+            for (int e = 0; e < 16; ++e) {
+              const int c = qtr * 32 + 2 * e;
+              const float2 x = unpack_f2(ffma2(pack_f2(u2f(sr[c]), u2f(sr[c + 1])), sl2x2, nmx2));
+              const float p0 = ex2_approx(x.x);
+              const float p1 = ex2_approx(x.y);
+              rs2[e % 4] = fadd2(rs2[e % 4], pack_f2(p0, p1));
+              pk[e] = pack_bf16x2(p0, p1);
             }
             tmem_st_32x32b_x16(ts + qtr * 16, pk);
           }
-          if (qtr == 1 && j > 0 && __any_sync(0xffffffffu, rescale)) {
-            // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled, and
-            // PV_t(j) is not issued before this warpgroup publishes P's first half.
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 8) {
-              uint32_t o[8];
-              tmem_ld_32x32b_x8(to + c0, o);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = f2u(u2f(o[e]) * alpha);
-              tmem_st_32x32b_x8(to + c0, o);
-            }
-          }
-          if ((kHalfP && qtr == 1) || qtr == 3) {
-            // keys [0, 64) (qtr 1) or all 128 (qtr 3) of P_t are in tensor memory
+          if (qtr == 1) {  // keys [0, 64) of P_t are in tensor memory
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(qtr == 1 ? p_half(t) : p_full(t));  // one arrival per warp
+            if (lane == 0) mbar_arrive(p_half(t));
           }
         }
         {
@@ -890,6 +880,10 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           const float2 r1 = unpack_f2(fadd2(rs2[2], rs2[3]));
           l_run += (r0.x + r0.y) + (r1.x + r1.y);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(t));  // one arrival per warp
       }
       // Hand the row's max and sum to the output warpgroup (once it has read the previous
       // unit's) and go straight on to the next unit: the output warpgroup normalises and
