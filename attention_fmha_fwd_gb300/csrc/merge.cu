@@ -45,21 +45,6 @@ struct ChunkTable {
   const float* lse[kMergeMaxVarargs];
 };
 
-// Where chunk c's row and lse live: stacked (base + c * chunk stride) or a pointer table.
-struct StackedChunks {
-  MSLK_DEV const float* out(const MergeArgs& a, int c, long long off) const {
-    return a.out_split + c * a.cs_out + off;
-  }
-  MSLK_DEV const float* lse(const MergeArgs& a, int c, long long idx) const {
-    return a.lse_split + c * a.cs_lse + idx;
-  }
-};
-struct TableChunks {
-  const ChunkTable* t;
-  MSLK_DEV const float* out(const MergeArgs&, int c, long long off) const { return t->out[c] + off; }
-  MSLK_DEV const float* lse(const MergeArgs&, int c, long long idx) const { return t->lse[c] + idx; }
-};
-
 MSLK_DEV float4 ldg_f4(const float* p) {
   float4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -67,6 +52,33 @@ MSLK_DEV float4 ldg_f4(const float* p) {
                : "l"(p));
   return r;
 }
+
+// Where chunk c's row and lse live: stacked (base + c * chunk stride: the group's G loads
+// walk one pointer) or a pointer table.
+struct StackedChunks {
+  template <int G>
+  MSLK_DEV void load(const MergeArgs& a, int c0, long long off, float4 (&x)[G]) const {
+    const float* p = a.out_split + c0 * a.cs_out + off;
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      x[u] = (c0 + u < a.n) ? ldg_f4(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+      p += a.cs_out;
+    }
+  }
+  MSLK_DEV const float* lse(const MergeArgs& a, int c, long long idx) const {
+    return a.lse_split + c * a.cs_lse + idx;
+  }
+};
+struct TableChunks {
+  const ChunkTable* t;
+  template <int G>
+  MSLK_DEV void load(const MergeArgs& a, int c0, long long off, float4 (&x)[G]) const {
+#pragma unroll
+    for (int u = 0; u < G; ++u)
+      x[u] = (c0 + u < a.n) ? ldg_f4(t->out[c0 + u] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  MSLK_DEV const float* lse(const MergeArgs&, int c, long long idx) const { return t->lse[c] + idx; }
+};
 
 // G = chunks folded per memory round trip (2, 4 or 8): fewer for small n keeps the
 // registers low and the number of rows in flight per SM high.
@@ -91,9 +103,7 @@ MSLK_DEV void merge_rows(const MergeArgs& a, const Chunks& ch) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c0 = 0; c0 < a.n; c0 += G) {
       float4 x[G];
-#pragma unroll
-      for (int u = 0; u < G; ++u)
-        x[u] = (c0 + u < a.n) ? ldg_f4(ch.out(a, c0 + u, src + d0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      ch.template load<G>(a, c0, src + d0, x);
       const float mine = (lane < G && c0 + lane < a.n) ? __ldg(ch.lse(a, c0 + lane, lse_idx)) * kLog2e
                                                        : -INFINITY;
       float l2[G];
