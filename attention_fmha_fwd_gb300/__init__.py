@@ -14,6 +14,7 @@ from .api import (  # noqa: F401
     attn_fwd_lanes,
     attn_partial,
     attn_split_kv,
+    attn_split_kv_static,
     device_status,
     diag_bounded_wait,
     last_error,

@@ -86,6 +86,7 @@ PLAN_FOLDED_HEADS = 8
 PLAN_SPLIT_UNITS = 16
 
 MERGE_MAX_VARARGS = 128
+SPLIT_KV_STATIC_BYTES = 16 << 20
 
 
 class MslkError(RuntimeError):
@@ -129,6 +130,7 @@ SIGNATURES = {
                                              _i32, _i32, _i32, _i32, _i32, _S, _S, _P, _i32, _P, _P]),
     "mslk_splitk_size": (_i32, [_i32, _i32, _i32, _i32, _i32]),
     "mslk_attn_split_kv": (_i32, [ctypes.POINTER(AttnArgs), _i32, _P, ctypes.c_size_t, _P]),
+    "mslk_attn_split_kv_static": (_i32, [ctypes.POINTER(AttnArgs), _i32, _P]),
     "mslk_attn_split_kv_workspace": (_i32, [ctypes.POINTER(AttnArgs), _i32, ctypes.POINTER(ctypes.c_size_t)]),
     "mslk_last_error": (ctypes.c_char_p, []),
     "mslk_device_status": (_i32, [_P]),

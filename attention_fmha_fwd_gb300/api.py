@@ -643,6 +643,34 @@ def attn_split_kv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, n_chunks
     return out, lse
 
 
+def attn_split_kv_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, n_chunks: int = 0,
+                         mask="none", scale=None, out=None, lse=True, out_dtype=torch.bfloat16,
+                         stream=None, bottom_right=False, window_left=None, window_right=None):
+    """``attn_split_kv`` for callers that cannot allocate device memory when they call: the
+    library keeps the workspace in a fixed array of ``SPLIT_KV_STATIC_BYTES`` per device (see
+    mslk_attn_split_kv_static).  With ``out`` and ``lse`` given, nothing is allocated; calls
+    that overlap on the GPU share the array and race, so keep them on one stream."""
+    q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
+    _check_inputs(q, k, v)
+    Hkv = _kv_heads(q, k, v)
+    B, M, H, K = q.shape
+    Kv = v.shape[3]
+    if out is None:
+        out = torch.empty((B, M, H, Kv), dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    a = _args(q, k, v, Hkv, _mask_kind(mask), scale, None, _band(bottom_right, window_left, window_right),
+              out, out.dtype, lse)
+    check(_capi.load().mslk_attn_split_kv_static(ctypes.byref(a), int(n_chunks),
+                                                 _stream_handle(stream, q.device)))
+    return out, lse
+
+
+SPLIT_KV_STATIC_BYTES = _capi.SPLIT_KV_STATIC_BYTES
+
+
 def split_kv_workspace_bytes(q, k, v, *, n_chunks: int = 0, mask="none", out_dtype=torch.bfloat16,
                              bottom_right=False, window_left=None, window_right=None) -> int:
     """Bytes of workspace ``attn_split_kv`` needs for these tensors and chunk count."""
@@ -685,7 +713,8 @@ def version() -> int:
 
 
 __all__: Sequence[str] = [
-    "attn_fwd", "attn_partial", "merge_attentions", "attn_split_kv", "split_kv_workspace_bytes",
+    "attn_fwd", "attn_partial", "merge_attentions", "attn_split_kv", "attn_split_kv_static",
+    "split_kv_workspace_bytes",
     "splitk_size", "device_status", "set_wait_timeout_ns",
     "diag_bounded_wait", "set_path_policy", "last_error", "version", "MslkError", "MASKS",
 ]

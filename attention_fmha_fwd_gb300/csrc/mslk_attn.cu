@@ -579,6 +579,33 @@ mslk_status run_split_kv(const mslk_attn_args& a, int32_t n, float* ws_out, floa
   return run_merge(m, stream, who);
 }
 
+// Workspace of mslk_attn_split_kv_static: a fixed array in every device that loads the
+// library, held until the process exits.  Host code cannot use the array's name as a
+// device address; split_static_workspace() looks the address up (cudaGetSymbolAddress)
+// the first time it runs on each device, with that device current.
+static __device__ __align__(256) unsigned char g_split_static[MSLK_SPLIT_KV_STATIC_BYTES];
+
+float* split_static_workspace(cudaError_t* err) {
+  constexpr int kMaxDevices = 64;
+  static float* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_split_static);
+    if (*err != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<float*>(p);
+  }
+  return ptrs[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -739,6 +766,28 @@ mslk_status mslk_merge_attentions_varargs(const float* const* out_chunks,
 int32_t mslk_splitk_size(int32_t batch, int32_t seqlen_kv, int32_t kv_heads, int32_t tile_n,
                          int32_t sm_count) {
   return splitk_size(batch, seqlen_kv, kv_heads, tile_n, sm_count);
+}
+
+mslk_status mslk_attn_split_kv_static(const mslk_attn_args* args, int32_t n_chunks, void* stream) {
+  const char* who = "mslk_attn_split_kv_static";
+  mslk_status s = check_split_args(args, n_chunks, who);
+  if (s != MSLK_OK) return s;
+  const mslk_attn_args& a = *args;
+  if (a.B == 0 || a.M == 0 || a.H == 0 || a.Mkv == 0)  // nothing to split: the forward call
+    return attn_general(a, static_cast<cudaStream_t>(stream), who);
+  const int32_t n = split_chunks(a, n_chunks);
+  const SplitLayout l = split_layout(a, n);
+  if (l.bytes > static_cast<size_t>(MSLK_SPLIT_KV_STATIC_BYTES))
+    return fail(MSLK_ERR_UNSUPPORTED,
+                "%s: %d chunks of this problem need a %zu-byte workspace, above the library's "
+                "fixed %zu bytes (fewer chunks, or mslk_attn_split_kv with a workspace)",
+                who, n, l.bytes, static_cast<size_t>(MSLK_SPLIT_KV_STATIC_BYTES));
+  cudaError_t e = cudaSuccess;
+  float* ws = split_static_workspace(&e);
+  if (ws == nullptr)
+    return fail(MSLK_ERR_CUDA, "%s: no device address for the fixed workspace (%s)", who,
+                cudaGetErrorString(e));
+  return run_split_kv(a, n, ws, ws + l.lse_offset / sizeof(float), static_cast<cudaStream_t>(stream), who);
 }
 
 mslk_status mslk_attn_split_kv_workspace(const mslk_attn_args* args, int32_t n_chunks,

@@ -412,6 +412,29 @@ int32_t mslk_splitk_size(int32_t batch, int32_t seqlen_kv, int32_t kv_heads, int
  */
 mslk_status mslk_attn_split_kv(const mslk_attn_args* args, int32_t n_chunks, void* workspace,
                                size_t workspace_bytes, void* stream);
+/*
+ * mslk_attn_split_kv_static — mslk_attn_split_kv without a workspace argument, for callers
+ * that cannot allocate device memory when they call: a plug-in run by a host that owns all
+ * device memory and hands kernels only their inputs and outputs, or a latency-critical
+ * loop that cannot take cudaMalloc's device-wide synchronisation.  (The pages have no
+ * counterpart: their split-K calls allocate their partial outputs.)
+ *
+ * The workspace is a fixed array of MSLK_SPLIT_KV_STATIC_BYTES inside the library; every
+ * GPU that loads the library holds it until the process exits.  The call allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *   args, n_chunks  as mslk_attn_split_kv.  A problem whose workspace (as
+ *                   mslk_attn_split_kv_workspace reports it) is larger than the array is
+ *                   refused with MSLK_ERR_UNSUPPORTED before anything is launched.
+ * The array's device address is looked up the first time the call runs on a device, with
+ * that device current; make that first call before any stream capture.  Every call shares
+ * the array, which keeps the previous call's contents; nothing in it needs to start at zero
+ * (each chunk's partial writes all it holds before the merge reads it).  Calls whose work
+ * overlaps on the GPU (different streams, or threads without an order between them) race
+ * on the array: order them on one stream, or give each its own workspace with
+ * mslk_attn_split_kv.
+ */
+#define MSLK_SPLIT_KV_STATIC_BYTES (16u << 20)
+mslk_status mslk_attn_split_kv_static(const mslk_attn_args* args, int32_t n_chunks, void* stream);
 /* Bytes of workspace mslk_attn_split_kv needs for these arguments and chunk count; the
  * tensor pointers in args are not read and may be NULL (the other checks still apply). */
 mslk_status mslk_attn_split_kv_workspace(const mslk_attn_args* args, int32_t n_chunks,
