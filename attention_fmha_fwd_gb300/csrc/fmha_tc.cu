@@ -741,11 +741,8 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       const int i = unit_at(k, cta, G);
       Unit u;
       if (i >= a.total_units || !decode_unit<kSplit>(a, i, u)) continue;
-      const bool split = u.step == 2;
       const int row_first = u.row0(t);  // first row of this Q tile (sequence coords)
       const int r = row_first + row_in_tile;
-      const bool valid = r < u.Lq;
-      const long long row = static_cast<long long>(u.q_base) + r;
       // this Q tile's key tiles (selects, not a runtime index, keep u in registers)
       const int tlo_t = t == 0 ? u.tlo[0] : u.tlo[1];
       const int n_t = ((t == 0 ? u.thi[0] : u.thi[1]) - tlo_t + u.step - 1) / u.step;

@@ -145,6 +145,60 @@ class ClockSampler:
                 "samples": len(win), "samples_in_timed_region": len(inside)}
 
 
+class NvmlClocks:
+    """SM clock and throttle reasons read through NVML (the driver's libnvidia-ml) between
+    the launches of the timed steps: the host queues steps ahead of the GPU, so each read
+    sees the GPU while it runs timed work.  Reading only; no setting is changed."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        import ctypes
+        self.samples = []
+        self.ok = False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            self.lib, self.h = lib, ctypes.c_void_p()
+            bus = None
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(torch_device)
+                bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            except Exception:  # noqa: BLE001 - fall back to the index
+                bus = None
+            if bus is not None and lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0:
+                self.ok = True
+            elif lib.nvmlDeviceGetHandleByIndex_v2(torch_device.index or 0, ctypes.byref(self.h)) == 0:
+                self.ok = True
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint(0)
+            self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 else None
+            if self.max_mhz is not None:
+                self.max_mhz = float(mx.value)
+        except OSError:
+            self.ok = False
+
+    def read(self):
+        if not self.ok:
+            return
+        import ctypes
+        mhz, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0 and \
+                self.reasons_fn(self.h, ctypes.byref(rs)) == 0:
+            self.samples.append((float(mhz.value), int(rs.value)))
+
+    def summary(self):
+        if not self.samples:
+            return None
+        reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples_in_timed_region": len(self.samples), "source": "nvml"}
+
+
 # ---------------------------------------------------------------------------- helpers
 
 def dist_info():
@@ -324,6 +378,11 @@ def run_gpu(args):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    nvml = NvmlClocks(dev) if (rank == 0 and not args.profile_mode) else None
+    # CUDA creates an event when it is first recorded: record every timing event once here,
+    # so that no host-side creation delays a timed step's launch after its start event.
+    for e in starts + ends:
+        e.record(stream)
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
@@ -332,6 +391,8 @@ def run_gpu(args):
         starts[i].record(stream)
         step()
         ends[i].record(stream)
+        if nvml is not None and i % 2 == 1:
+            nvml.read()                     # the GPU is running the steps queued so far
     torch.cuda.synchronize()
     barrier()
     t1 = time.time()
@@ -343,6 +404,10 @@ def run_gpu(args):
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
+    in_region = nvml.summary() if nvml is not None else None
+    if in_region is not None:
+        # NVML reads taken between the timed launches; nvidia-smi's samples around them
+        clocks = dict(in_region, nvidia_smi=clocks)
 
     if args.profile_mode:
         if rank == 0:
@@ -398,6 +463,9 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)  # (created here, recorded again below as the start mark)
+    e1.record(stream)
+    torch.cuda.synchronize()
     e0.record(stream)
     for j in range(3):
         s_in[j].wait_event(e0)
@@ -441,6 +509,7 @@ def run_gpu(args):
             "gpu_launches": args.steps,
             "step_ms": {"mean": t_step * 1e3, "median": statistics.median(per) * 1e3,
                         "min": min(per) * 1e3, "max": max(per) * 1e3,
+                        "each": [round(x * 1e3, 5) for x in per],
                         "note": "per-step CUDA-event times of the timed steps on this rank; "
                                 "value uses the mean"},
             "clocks": clocks,
@@ -461,11 +530,13 @@ def run_gpu(args):
 
 def _time_it(fn, reps, stream, flush):
     import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)  # created on first record, before any timed interval
+    b.record(stream)
     ts = []
     for _ in range(reps):
         flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
         b.record(stream)
