@@ -32,7 +32,8 @@
  *  - Every pointer is caller-owned DEVICE memory (except the mslk_seqlens struct and
  *    the mslk_strides structs, which live on the host and are read during the call).
  *    The library allocates no device memory and keeps no state between calls, apart
- *    from a per-device error word read by mslk_device_status().
+ *    from a per-device error word read by mslk_device_status() and the fixed workspace
+ *    array of mslk_attn_split_kv_static.
  *  - Alignment: q, k, v, out base pointers 16-byte aligned; every free stride times the
  *    element size a multiple of 16 bytes (the tensor-memory-accelerator copy rule).
  *    Violations return MSLK_ERR_MISALIGNED.
