@@ -289,6 +289,23 @@ def test_varlen_small(mask):
     compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"varlen {mask}")
 
 
+@pytest.mark.parametrize("n_seqs", [12, 128, 140])
+def test_varlen_many_sequences(n_seqs):
+    """Many packed sequences of mixed lengths (one empty, two equal) against the oracle: most
+    slots of the unit grid (longest sequence x heads x sequences) are empty and skipped."""
+    g = torch.Generator().manual_seed(40 + n_seqs)
+    lq = torch.randint(1, 700, (n_seqs,), generator=g).tolist()
+    lq[3] = 0
+    lq[7] = lq[8] = 256  # equal unit counts
+    cq = inputs.cu_seqlens(lq)
+    q, k, v = inputs.qkv(1, cq[-1], cq[-1], 2, 64, seed=41)
+    cqd = torch.tensor(cq, dtype=torch.int32, device="cuda")
+    out, lse = fa.attn_fwd(*to_dev(q, k, v), mask="blockdiag_causal", cu_seqlens_q=cqd,
+                           cu_seqlens_k=cqd, max_seqlen_q=max(lq), max_seqlen_k=max(lq))
+    ro, rl = _ref(q, k, v, 1 / 64 ** 0.5, "blockdiag_causal", cu_seqlens_q=cq, cu_seqlens_k=cq)
+    compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"varlen x{n_seqs}")
+
+
 def test_varlen_partial_merge():
     """Block-diagonal causal split per sequence: chunk c holds keys [c*64, c*64+64) of
     every sequence (kv_offset = c*64), merged == the unsplit packed attention."""
