@@ -287,7 +287,9 @@ struct Unit {
   MSLK_DEV bool has(int t, int j) const {
     return tlo[t] <= j && j < thi[t] && (step == 1 || ((j - tlo[t]) & 1) == 0);
   }
-  MSLK_DEV int count(int t) const { return (thi[t] - tlo[t] + step - 1) / step; }  // (has(t))
+  // (has(t)) step is 1 or 2: a shift, not a divide (a divide takes the special-function
+  // unit, which the softmax warps keep busy with exponentials)
+  MSLK_DEV int count(int t) const { return (thi[t] - tlo[t] + step - 1) >> (step - 1); }
   MSLK_DEV int last(int t) const { return tlo[t] + (count(t) - 1) * step; }         // (has(t))
   MSLK_DEV int row0(int t) const { return r0 + (step == 2 ? 0 : t * kBlockM); }  // first row
 };
@@ -541,16 +543,61 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
     // uc: units; uc_t: units in which Q tile t has keys (o_free phases); jg_t: its key tiles.
     int uc = 0, it = 0, uc0 = 0, uc1 = 0, jg0 = 0, jg1 = 0;
     bool ok = true;
-    // The next unit with work at or after round k (k_out = its round), false if none.
-    auto next_unit = [&](int k, int& k_out, Unit& uo) {
-      for (; k < n_rounds; ++k) {
+    // Units are decoded 32 rounds at a time, one per lane (a decode costs ~1.5k cycles of
+    // integer divides and parameter loads, which at every unit boundary sat between this
+    // warp's last P.V and the next S); the MMA fields of round batch + l stay in lane l's
+    // registers and are fetched with shuffles.
+    int batch = -32;          // first round of the decoded batch
+    uint32_t with_work = 0;   // lanes whose unit has key tiles
+    int m_jlo = 0, m_jhi = 0, m_tlo0 = 0, m_thi0 = 0, m_tlo1 = 0, m_thi1 = 0, m_step = 1, m_lk = 0;
+    auto decode_batch = [&](int first) {
+      batch = first;
+      const int k = first + lane;
+      Unit uu;
+      bool work = false;
+      if (k < n_rounds) {
         const int i = unit_at(k, cta, G);
-        if (i < a.total_units && decode_unit<kSplit>(a, i, uo) && uo.jhi > uo.jlo) {
-          k_out = k;
+        work = i < a.total_units && decode_unit<kSplit>(a, i, uu) && uu.jhi > uu.jlo;
+      }
+      if (work) {
+        m_jlo = uu.jlo; m_jhi = uu.jhi; m_tlo0 = uu.tlo[0]; m_thi0 = uu.thi[0];
+        m_tlo1 = uu.tlo[1]; m_thi1 = uu.thi[1]; m_step = uu.step; m_lk = uu.Lk;
+      }
+      with_work = __ballot_sync(0xffffffffu, work);
+    };
+    // The next unit with work at or after round k (k_out = its round), false if none; only
+    // the fields this warp reads are set in uo.
+    auto next_unit = [&](int k, int& k_out, Unit& uo) {
+      if constexpr (F8) {  // (measured: the E4M3 kernel runs better decoding in place)
+        for (; k < n_rounds; ++k) {
+          const int i = unit_at(k, cta, G);
+          if (i < a.total_units && decode_unit<kSplit>(a, i, uo) && uo.jhi > uo.jlo) {
+            k_out = k;
+            return true;
+          }
+        }
+        return false;
+      } else {
+      while (k < n_rounds) {
+        if (k < batch || k >= batch + 32) decode_batch(k & ~31);
+        const uint32_t m = with_work & (0xffffffffu << (k - batch));
+        if (m != 0u) {
+          const int l = __ffs(m) - 1;
+          k_out = batch + l;
+          uo.jlo = __shfl_sync(0xffffffffu, m_jlo, l);
+          uo.jhi = __shfl_sync(0xffffffffu, m_jhi, l);
+          uo.tlo[0] = __shfl_sync(0xffffffffu, m_tlo0, l);
+          uo.thi[0] = __shfl_sync(0xffffffffu, m_thi0, l);
+          uo.tlo[1] = __shfl_sync(0xffffffffu, m_tlo1, l);
+          uo.thi[1] = __shfl_sync(0xffffffffu, m_thi1, l);
+          uo.step = __shfl_sync(0xffffffffu, m_step, l);
+          uo.Lk = __shfl_sync(0xffffffffu, m_lk, l);
           return true;
         }
+        k = batch + 32;
       }
       return false;
+      }
     };
     Unit u;
     int ku = 0;
@@ -745,7 +792,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
       const int r = row_first + row_in_tile;
       // this Q tile's key tiles (selects, not a runtime index, keep u in registers)
       const int tlo_t = t == 0 ? u.tlo[0] : u.tlo[1];
-      const int n_t = ((t == 0 ? u.thi[0] : u.thi[1]) - tlo_t + u.step - 1) / u.step;
+      const int n_t = ((t == 0 ? u.thi[0] : u.thi[1]) - tlo_t + u.step - 1) >> (u.step - 1);
       float sl2 = a.scale_log2;
       if constexpr (F8) {
         const int hq = a.fold ? u.h * a.fold + min(r, a.fold - 1) : u.h;  // this row's query head
@@ -919,7 +966,7 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         const int r = row_first + row_in_tile;
         const bool valid = r < u.Lq;
         const long long row = static_cast<long long>(u.q_base) + r;
-        const int n_t = ((t == 0 ? u.thi[0] : u.thi[1]) - (t == 0 ? u.tlo[0] : u.tlo[1]) + u.step - 1) / u.step;
+        const int n_t = ((t == 0 ? u.thi[0] : u.thi[1]) - (t == 0 ? u.tlo[0] : u.tlo[1]) + u.step - 1) >> (u.step - 1);
         if (n_t <= 0) {  // no allowed key for any row of this Q tile
           if (valid) {
             for (int c = 0; c < a.d_out; c += 4) {
