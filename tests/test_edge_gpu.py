@@ -92,6 +92,29 @@ def test_many_key_tiles_sampled():
         compare(out[:, i:i + 1], lse[:, :, i:i + 1], ro, rl, f"causal row {i}")
 
 
+@pytest.mark.parametrize("mask", ["causal", "none"])
+def test_more_than_32_rounds_per_cta(mask):
+    """16 x 2560 rows x 32 heads = 5120 units of 256 rows: 34 per CTA on 152 SMs, so the MMA
+    warp decodes its units in two batches of 32 rounds.  The last rounds hold the lightest
+    units (the first rows of each sequence under a causal mask): sampled rows from every
+    256-row block of several heads, and rows 0-255 of every head of one batch."""
+    B, M, H, D = 16, 2560, 32, 64
+    q, k, v = inputs.qkv(B, M, M, H, D, seed=77)
+    s = D ** -0.5
+    out, lse = _run(q, k, v, s, mask)
+    qf, kf, vf = f32(q), f32(k), f32(v)
+    rng = np.random.default_rng(5)
+    for b, h in ((0, 0), (7, 13), (15, 31), (11, 2)):
+        rows = np.unique(np.concatenate([np.arange(0, M, 256), np.arange(255, M, 256),
+                                         rng.integers(0, M, 24)]))
+        ro, rl = oracle.attention_head(qf, kf, vf, b, h, s, KIND[mask], rows=rows)
+        compare(out[b, rows, h], lse[b, h, rows], ro, rl, f"b{b} h{h}")
+    rows = np.arange(0, 256)
+    for h in range(H):
+        ro, rl = oracle.attention_head(qf, kf, vf, 3, h, s, KIND[mask], rows=rows)
+        compare(out[3, rows, h], lse[3, h, rows], ro, rl, f"b3 h{h} rows 0-255")
+
+
 @pytest.mark.parametrize("B,M,Mkv,H,D,mask", [
     (3, 300, 300, 40, 64, "causal"),     # 3 x 40 x 2 = 240 units on 152 SMs
     (5, 1, 1000, 96, 128, "none"),       # 480 decode CTAs
