@@ -442,6 +442,29 @@ def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descale_q, d
     return out, lse
 
 
+# Argument structs of earlier attn_partial calls with caller-provided out and lse, keyed by
+# everything they hold (pointers, shapes, strides, dtypes and options): a loop over the same
+# buffers (the chunks of a split, a decode step) replays the struct through mslk_attn
+# instead of rebuilding 21 ctypes arguments.  The library validates every call either way.
+_PARTIAL_ARGS: dict = {}
+_PARTIAL_ARGS_MAX = 256
+
+
+def _partial_key(q, k, v, out, lse, mask, scale, kv_offset, out_dtype, independent):
+    return (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            q.shape, k.shape, v.shape, out.shape, lse.shape, q.stride(), k.stride(), v.stride(),
+            out.stride(), lse.stride(), q.dtype, k.dtype, v.dtype, out.dtype, lse.dtype,
+            q.get_device(), mask, scale, kv_offset, out_dtype, independent)
+
+
+def _remember_partial(key, a):
+    if key is None:
+        return
+    if len(_PARTIAL_ARGS) >= _PARTIAL_ARGS_MAX:
+        _PARTIAL_ARGS.clear()
+    _PARTIAL_ARGS[key] = a
+
+
 def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="none",
                  scale=None, kv_offset: int = 0, cu_seqlens_q=None, cu_seqlens_k=None,
                  max_seqlen_q=None, max_seqlen_k=None, out_dtype=torch.float32, out=None,
@@ -468,6 +491,14 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
                      window_left=window_left, window_right=window_right, independent=independent)
         return out, lse
     q, k, v = _as_bmhk(q), _as_bmhk(k), _as_bmhk(v)
+    key = None
+    if (out is not None and lse is not None and cu_seqlens_q is None and cu_seqlens_k is None
+            and window_left is None and window_right is None):
+        key = _partial_key(q, k, v, out, lse, mask, scale, kv_offset, out_dtype, independent)
+        a = _PARTIAL_ARGS.get(key)
+        if a is not None:
+            check(_capi.load().mslk_attn(ctypes.byref(a), _stream_handle(stream, q.device)))
+            return out, lse
     _check_inputs(q, k, v)
     Hkv = _kv_heads(q, k, v)
     B, M, H, K = q.shape
@@ -484,8 +515,10 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
     sl, _keep = _seqlens(mk, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
     band = _band(False, window_left, window_right)
     if Hkv != H or independent:  # grouped K/V heads, or a launch that may overlap the previous
-        _general(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, stream, partial=1,
-                 kv_offset=kv_offset, flags=_capi.FLAG_INDEPENDENT if independent else 0)
+        a = _args(q, k, v, Hkv, mk, scale, sl, band, out, out_dtype, lse, partial=1,
+                  kv_offset=kv_offset, flags=_capi.FLAG_INDEPENDENT if independent else 0)
+        check(_capi.load().mslk_attn(ctypes.byref(a), _stream_handle(stream, q.device)))
+        _remember_partial(key, a)
         return out, lse
     sq, sk, sv = _bmhk_strides(q, "q"), _bmhk_strides(k, "k"), _bmhk_strides(v, "v")
     so = _bmhk_strides(out, "out")
@@ -497,6 +530,9 @@ def attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, mask="non
                                     Mkv, H, K, Kv, sc, mk, sl, int(kv_offset), out.data_ptr(),
                                     _DTYPES[out_dtype], lse.data_ptr(),
                                     _stream_handle(stream, q.device)))
+        if key is not None:
+            _remember_partial(key, _args(q, k, v, H, mk, scale, None, None, out, out_dtype, lse,
+                                         partial=1, kv_offset=kv_offset))
     else:
         check(lib.mslk_attn_partial_band(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                          ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv),

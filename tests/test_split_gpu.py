@@ -171,3 +171,29 @@ def test_bmghk_expanded_kv_views():
     assert mo.shape == (B, M, G, Hg, D) and ml.shape == (B, G, Hg, M)
     compare(mo.reshape(B, M, G * Hg, D).double().cpu().numpy(),
             ml.reshape(B, G * Hg, M).double().cpu().numpy(), ro, rl, "bmghk split")
+
+
+def test_partial_repeated_calls_on_the_same_buffers():
+    """A second call on the same buffers replays the first call's argument struct: it must
+    read the buffers' new contents, and a changed option (key offset, mask, scale) or a
+    different chunk must not reuse it."""
+    B, M, Mkv, H, D = 1, 70, 300, 4, 128
+    q, k, v = inputs.qkv(B, M, Mkv, H, D, seed=31)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    out = torch.empty(B, M, H, D, device="cuda")
+    lse = torch.empty(B, H, M, device="cuda")
+    s = D ** -0.5
+    for step in range(3):
+        if step == 2:
+            qd.mul_(-0.5)  # same pointer, new contents
+        for a0, b0, mask, off in ((0, 128, "none", 0), (128, 300, "causal", 128), (128, 300, "causal", 140)):
+            fa.attn_partial(qd, kd[:, a0:b0], vd[:, a0:b0], mask=mask, scale=s, kv_offset=off,
+                            out=out, lse=lse)
+            torch.cuda.synchronize()
+            qh = qd.cpu()
+            ro, rl = oracle.attention(qh.float().numpy(), k[:, a0:b0].float().numpy(),
+                                      v[:, a0:b0].float().numpy(), s,
+                                      oracle.MASK_CAUSAL if mask == "causal" else oracle.MASK_NONE,
+                                      kv_offset=off)
+            compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl,
+                    f"step {step} chunk {a0}:{b0} {mask} offset {off}")
