@@ -740,10 +740,10 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
           mma_commit_elect(kv_empty(sv));
           if (more) {
             if constexpr (F8) {
-              // E4M3: V_{j+1} (ring entry it) is waited for here, ahead of S1_{j+1}.  The
-              // tensor core holds only about three queued MMAs, so waits between S1_{j+1}
-              // and PV0_{j+1} are time it idles; measured 55.3-55.6 vs 57.2 us causal.  (The
-              // bf16 kernel runs slower this way: there V_{j+1} is not always in yet.)
+              // E4M3: V_{j+1} (ring entry it) is waited for here, ahead of S1_{j+1}, so the
+              // step from S1_{j+1} to PV0_{j+1} has one wait less; measured 55.3-55.6 vs
+              // 57.2 us causal.  (The bf16 kernel runs slower this way: with its 4-stage
+              // ring V_{j+1} is not always in yet.)
               if (!(ok = wait_bar_warp(kv_full(it % L::kStages), (it / L::kStages) & 1, wc))) break;
               v_ready = true;
             }
