@@ -578,25 +578,25 @@ MSLK_DEV void tc_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CU
         }
         return false;
       } else {
-      while (k < n_rounds) {
-        if (k < batch || k >= batch + 32) decode_batch(k & ~31);
-        const uint32_t m = with_work & (0xffffffffu << (k - batch));
-        if (m != 0u) {
-          const int l = __ffs(m) - 1;
-          k_out = batch + l;
-          uo.jlo = __shfl_sync(0xffffffffu, m_jlo, l);
-          uo.jhi = __shfl_sync(0xffffffffu, m_jhi, l);
-          uo.tlo[0] = __shfl_sync(0xffffffffu, m_tlo0, l);
-          uo.thi[0] = __shfl_sync(0xffffffffu, m_thi0, l);
-          uo.tlo[1] = __shfl_sync(0xffffffffu, m_tlo1, l);
-          uo.thi[1] = __shfl_sync(0xffffffffu, m_thi1, l);
-          uo.step = __shfl_sync(0xffffffffu, m_step, l);
-          uo.Lk = __shfl_sync(0xffffffffu, m_lk, l);
-          return true;
+        while (k < n_rounds) {
+          if (k < batch || k >= batch + 32) decode_batch(k & ~31);
+          const uint32_t m = with_work & (0xffffffffu << (k - batch));
+          if (m != 0u) {
+            const int l = __ffs(m) - 1;
+            k_out = batch + l;
+            uo.jlo = __shfl_sync(0xffffffffu, m_jlo, l);
+            uo.jhi = __shfl_sync(0xffffffffu, m_jhi, l);
+            uo.tlo[0] = __shfl_sync(0xffffffffu, m_tlo0, l);
+            uo.thi[0] = __shfl_sync(0xffffffffu, m_thi0, l);
+            uo.tlo[1] = __shfl_sync(0xffffffffu, m_tlo1, l);
+            uo.thi[1] = __shfl_sync(0xffffffffu, m_thi1, l);
+            uo.step = __shfl_sync(0xffffffffu, m_step, l);
+            uo.Lk = __shfl_sync(0xffffffffu, m_lk, l);
+            return true;
+          }
+          k = batch + 32;
         }
-        k = batch + 32;
-      }
-      return false;
+        return false;
       }
     };
     Unit u;
